@@ -1,0 +1,231 @@
+/*
+ * moe_nvfp4.h - C ABI of the GB300 (sm_103a) routed-MoE forward with online
+ * per-token NVFP4 activation quantization.
+ *
+ * One call of moe_forward runs, on one CUDA stream, with no host
+ * synchronisation and no allocation:
+ *   router logits -> top-k -> expert permutation (expand) -> per-token NVFP4
+ *   quantization -> block-scaled FP4 grouped GEMM on w13 with SwiGLU and
+ *   per-row requantization in its epilogue -> block-scaled FP4 grouped GEMM on
+ *   w2 with the top-k weighted reduction in its epilogue -> bf16 output.
+ *
+ * Where each operation is defined (the pages' titles and sections):
+ *   - "CuTe DSL backend gets per-token NVFP4 online quantization and reload",
+ *     Implementation items 1-3 and the code snippets: per-token FP32 global
+ *     scale, E4M3 block scales over 16-element blocks, E2M1 codes; online
+ *     NVFP4 weight conversion; in-place scale refresh after a weight reload
+ *     that keeps every captured address valid and fails loudly when scale
+ *     metadata changed; deterministic inference forces the non-fused
+ *     (fixed-order) finalize.
+ *   - "size CuteDSL MoE allgather buffers for the worst-case forward",
+ *     Motivation and Implementation: buffers are sized once from the
+ *     worst-case token count of one forward; a larger forward is an error.
+ *   - "SM10X Command-A-Plus decode 2.3x faster, BCG capture memory -78%",
+ *     Motivation and Implementation item 2: routing, expandInputRows,
+ *     activation and finalize fused around the expert GEMMs; the routed
+ *     output must not alias its input.
+ *
+ * Numeric rules (the pages print no formula; these are the library's stated
+ * readings):
+ *   gs   = fl32(2688 / amax) per token (activations), per expanded row (the
+ *          intermediate) or per expert (weights); 1 when amax == 0.
+ *   sf   = E4M3_rne_satfinite(fl32(fl32(amax_16 * gs) / 6)).
+ *   code = E2M1_rne_satfinite(fl32(x * fl32(gs / dec(sf)))), +0 if dec(sf)==0.
+ *   Router logits are FP32 in a canonical order (8-element chunks, partial
+ *   p sums chunks p, p+32, ... with fused multiply-adds, then a pairwise tree
+ *   over the 32 partials); top-k by logit (ties to the lower expert id);
+ *   weights = softmax over all experts, chosen ones renormalised.
+ *   Requires hidden % 256 == 0, inter % 128 == 0, num_experts % 8 == 0,
+ *   num_experts <= 256, 1 <= top_k <= min(num_experts, 16).
+ *
+ * Memory and ownership: every pointer argument is a device pointer on the
+ * handle's device unless stated otherwise.  Inputs are borrowed and read in
+ * stream order; the caller keeps them alive until the stream reaches the
+ * work.  The handle owns the quantized weights and all workspace.
+ *
+ * Errors: every entry point returns a moe_status and never aborts; the text
+ * of the last error on a handle is available from moe_get_last_error.
+ * Kernel-side waits are bounded: a wait that runs out records
+ * MOE_ERR_DEVICE_TIMEOUT in a host-visible status word, which the next
+ * moe_forward and moe_get_status report.
+ */
+#ifndef MOE_NVFP4_H
+#define MOE_NVFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct moe_handle moe_handle; /* opaque; owns all device memory */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,       /* bad pointer, size, shape or dtype */
+  MOE_ERR_TOO_MANY_TOKENS = 2,   /* num_tokens > max_num_tokens */
+  MOE_ERR_NOT_LOADED = 3,        /* forward / refresh before moe_load_weights */
+  MOE_ERR_METADATA_CHANGED = 4,  /* refresh with a different shape/dtype/device */
+  MOE_ERR_ALIAS = 5,             /* out overlaps x */
+  MOE_ERR_CUDA = 6,              /* a CUDA runtime call failed */
+  MOE_ERR_DEVICE_TIMEOUT = 7,    /* a bounded device-side wait ran out */
+  MOE_ERR_UNSUPPORTED = 8        /* shape outside the supported set, or no sm_103a device */
+} moe_status;
+
+/* Deterministic mode: the top-k weighted reduction runs in a fixed order
+ * (slot 0, 1, ..., K-1 per token) with no floating-point atomics, so the
+ * output is bitwise identical across runs.  Without it, expert rows are
+ * accumulated with FP32 atomic adds (the fused finalize). */
+#define MOE_FLAG_DETERMINISTIC 1u
+
+typedef struct {
+  int hidden;          /* H: model width (K dim of w13, N dim of w2) */
+  int inter;           /* I: expert intermediate width */
+  int num_experts;     /* E */
+  int top_k;           /* K: experts per token */
+  int max_num_tokens;  /* worst-case tokens of one forward; fixes all buffer sizes */
+  int device;          /* CUDA device ordinal */
+  unsigned flags;      /* MOE_FLAG_* */
+} moe_config;
+
+typedef enum { MOE_DTYPE_BF16 = 1 } moe_dtype;
+
+/* Shape of an expert weight tensor as the caller holds it: a contiguous,
+ * row-major [dims[0], dims[1], dims[2]] array of dtype on device `device`. */
+typedef struct {
+  int64_t dims[3];
+  int dtype;           /* moe_dtype */
+  int device;          /* CUDA ordinal the data lives on */
+} moe_weight_desc;
+
+/* Create a handle and allocate every device buffer for the worst-case forward
+ * (max_num_tokens tokens).  Nothing is allocated afterwards.  *out is set to
+ * NULL on failure. */
+MOE_API moe_status moe_create(const moe_config* cfg, moe_handle** out);
+
+/* Release all device memory of the handle.  Waits for the device.  NULL is
+ * accepted. */
+MOE_API moe_status moe_destroy(moe_handle* h);
+
+/* Online NVFP4 conversion of bf16 expert weights.
+ *   w13: [E, 2I, H] bf16; rows [0, I) of expert e are the gate projection,
+ *        rows [I, 2I) the up projection.
+ *   w2:  [E, H, I] bf16.
+ * One FP32 global scale per expert and tensor (2688 / amax over the expert's
+ * whole matrix), E4M3 block scales along the reduction dimension.  Enqueued
+ * on `stream` (a cudaStream_t; NULL = legacy default stream).  The bf16
+ * inputs may be freed once the stream has passed this call. */
+MOE_API moe_status moe_load_weights(moe_handle* h, const void* w13, const moe_weight_desc* w13_desc,
+                            const void* w2, const moe_weight_desc* w2_desc, void* stream);
+
+/* Weight reload: re-quantize new bf16 weights into the SAME device buffers
+ * (codes, block scales, global scales), so a CUDA graph captured around
+ * moe_forward stays valid and replays with the new weights.  Fails with
+ * MOE_ERR_NOT_LOADED before the first load and with MOE_ERR_METADATA_CHANGED
+ * if any shape, dtype or device differs from the loaded weights (a captured
+ * graph would then need to be recaptured).  Never reallocates. */
+MOE_API moe_status moe_refresh_scales_inplace(moe_handle* h, const void* w13, const moe_weight_desc* w13_desc,
+                                      const void* w2, const moe_weight_desc* w2_desc, void* stream);
+
+/* One forward of the routed MoE layer.
+ *   x:      [num_tokens, H] bf16 activations (read only).
+ *   gate_w: [H, E] bf16 router weight.
+ *   out:    [num_tokens, H] bf16, written; must not overlap x.
+ * 0 <= num_tokens <= max_num_tokens (0 is a no-op).  Enqueued on `stream`
+ * with no host synchronisation, no allocation and no host read of device
+ * results, so the call may be captured into a CUDA graph. */
+MOE_API moe_status moe_forward(moe_handle* h, const void* x, const void* gate_w, void* out,
+                       int num_tokens, void* stream);
+
+/* moe_forward with an optional FP32 [E] bias added to the router logits
+ * (NULL = none).  The bias moves both the top-k choice and the softmax. */
+MOE_API moe_status moe_forward_ex(moe_handle* h, const void* x, const void* gate_w, const float* gate_bias,
+                          void* out, int num_tokens, void* stream);
+
+/* Same forward, but x, gate_w, gate_bias and out are HOST pointers: the call
+ * copies the inputs into handle-owned device staging buffers, runs the
+ * forward and copies the result back, all on `stream`, and returns after the
+ * stream has finished (so it is not capturable). */
+MOE_API moe_status moe_forward_host(moe_handle* h, const void* x_host, const void* gate_w_host,
+                            const float* gate_bias_host, void* out_host, int num_tokens,
+                            void* stream);
+
+/* Device bytes owned by the handle (weights + workspace + staging). */
+MOE_API size_t moe_get_workspace_bytes(const moe_handle* h);
+
+/* Text of the last error on this handle ("" if none).  The pointer stays
+ * valid until the next call on the handle. */
+MOE_API const char* moe_get_last_error(const moe_handle* h);
+
+/* Human-readable name of a status code. */
+MOE_API const char* moe_status_string(moe_status s);
+
+/* Reads the host-visible device status word without synchronising: MOE_OK,
+ * or MOE_ERR_DEVICE_TIMEOUT if a kernel of this handle gave up a bounded
+ * wait.  Call after synchronising the stream to see the latest state. */
+MOE_API moe_status moe_get_status(const moe_handle* h);
+
+/* ---------------------------------------------------------------------------
+ * Parity exports.  Each copies state left by the LAST moe_forward on the
+ * handle (or by the last load/refresh for the weights) into caller device
+ * buffers, in canonical row-major layouts, on `stream`.  T below is that
+ * forward's num_tokens, R = T*K.
+ * ------------------------------------------------------------------------ */
+
+/* topk_ids int32 [T,K] (slot order), topk_w f32 [T,K], src_of_row int32 [R]
+ * (row r of the expert-grouped order is slot src%K of token src/K),
+ * expert_offsets int32 [E+1] (unpadded exclusive prefix sum). Any pointer may
+ * be NULL to skip it. */
+MOE_API moe_status moe_debug_routing(moe_handle* h, int32_t* topk_ids, float* topk_w, int32_t* src_of_row,
+                             int32_t* expert_offsets, void* stream);
+
+/* Router logits f32 [T,E] (bias included). */
+MOE_API moe_status moe_debug_logits(moe_handle* h, float* logits, void* stream);
+
+/* Per-token activation quantization: codes uint8 [T, H/2] (element 2i in the
+ * low nibble), block scales uint8 [T, H/16] (E4M3), gs f32 [T]. */
+MOE_API moe_status moe_debug_act_quant(moe_handle* h, uint8_t* codes, uint8_t* sf, float* gs, void* stream);
+
+/* Quantized weights. which = 0: w13 -> codes [E, 2I, H/2], sf [E, 2I, H/16];
+ * which = 1: w2 -> codes [E, H, I/2], sf [E, H, I/16]; gs f32 [E]. Rows in the
+ * caller's order (gate rows first for w13). */
+MOE_API moe_status moe_debug_weight_quant(moe_handle* h, int which, uint8_t* codes, uint8_t* sf, float* gs,
+                                  void* stream);
+
+/* Requantized intermediate of the last forward: h_codes uint8 [R, I/2],
+ * h_sf uint8 [R, I/16], h_gs f32 [R], indexed by src = t*K + j. */
+MOE_API moe_status moe_debug_intermediate(moe_handle* h, uint8_t* h_codes, uint8_t* h_sf, float* h_gs,
+                                  void* stream);
+
+/* Addresses of every device buffer the handle owns (weights, scales,
+ * workspace), for checking that load/refresh never moves them.  On entry *n
+ * is the capacity of ptrs; on return it is the number of buffers. */
+MOE_API moe_status moe_debug_buffer_ptrs(const moe_handle* h, const void** ptrs, int* n);
+
+/* Hardware conversion check: for n FP32 inputs, e2m1[i] = E2M1 code of in[i]
+ * (round to nearest even, satfinite) and e4m3[i] = E4M3 byte of in[i], using
+ * the same conversion instructions as the quantizer. Inputs must be finite. */
+MOE_API moe_status moe_debug_convert(const float* in, uint8_t* e2m1, uint8_t* e4m3, int64_t n, void* stream);
+
+/* Block-scaled FP4 GEMM through the same tcgen05 main loop as the expert
+ * GEMMs: d[m][n] = sum_k dec(a)*dec(sfa)*dec(b)*dec(sfb) in FP32, for
+ * a_codes [M, K/2], a_sf [M, K/16], b_codes [N, K/2], b_sf [N, K/16]
+ * (canonical layouts), d f32 [M, N].  M % 128 == 0, N % 256 == 0,
+ * K % 256 == 0.  Allocates and frees temporary buffers and synchronises the
+ * stream; for tests only. */
+MOE_API moe_status moe_debug_block_scaled_gemm(const uint8_t* a_codes, const uint8_t* a_sf,
+                                       const uint8_t* b_codes, const uint8_t* b_sf,
+                                       float* d, int M, int N, int K, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_NVFP4_H */

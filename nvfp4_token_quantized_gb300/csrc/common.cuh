@@ -1,0 +1,344 @@
+// common.cuh - device helpers shared by the sm_103a kernels of the routed-MoE
+// forward: inline PTX for mbarrier / TMA / tcgen05, bounded waits, and the
+// NVFP4 block quantizer.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// Layout constants
+// ---------------------------------------------------------------------------
+constexpr int SF_VEC = 16;          // elements per E4M3 block scale
+constexpr int MMA_K = 64;           // FP4 elements per tcgen05.mma (kind::mxf4nvf4)
+constexpr int STAGE_K = 256;        // FP4 elements per pipeline stage (128 bytes per row)
+constexpr int TILE_M = 128;         // rows per expert tile
+constexpr int TILE_N = 256;         // output columns per tile
+constexpr int SF_ATOM_BYTES = 512;  // block scales of 128 rows x 64 K-elements
+
+// Device status word bits (mapped host memory, read by the host without sync).
+constexpr int DEV_ERR_TIMEOUT = 1;
+constexpr int DEV_ERR_BAD_STATE = 2;
+
+// Byte offset of the block scale of (row, k16) in the "128x4 atom" layout the
+// tensor cores read: atoms of 128 rows x 4 block scales (64 K-elements), 512
+// bytes each; row r of an atom at (r%32)*16 + (r/32)*4, block j at +j.
+// Atoms are ordered [row / 128][k16 / 4].
+__host__ __device__ __forceinline__ size_t sf_atom_offset(int row, int k16, int k16_per_row) {
+  const int atoms_per_rowblock = k16_per_row / 4;
+  return ((size_t)(row >> 7) * atoms_per_rowblock + (k16 >> 2)) * SF_ATOM_BYTES +
+         (size_t)((row & 31) * 16 + ((row >> 5) & 3) * 4 + (k16 & 3));
+}
+
+// ---------------------------------------------------------------------------
+// Generic helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void report_device_error(int* status_word, int bits) {
+  if (status_word) atomicOr(status_word, bits);
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbarrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of `parity` to complete, for at most ~timeout_ns.  When
+// `abort` is given, gives up early once another thread of the CTA raised it.
+// Returns false on timeout or abort; the caller then records the error and
+// unwinds.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                  uint64_t timeout_ns = 2000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (abort != nullptr && *abort) return false;
+      if (global_timer_ns() - t0 > timeout_ns) return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// TMA and bulk copies (global -> shared, completion on an mbarrier)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x,
+                                            int y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 (5th-generation tensor cores, accumulators in tensor memory)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* smem_result, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(smem_result)),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Arrive on `bar` when every tcgen05 operation issued so far by this thread
+// (MMAs and copies) has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+// Copy 32 rows x 16 bytes of block scales from shared memory into tensor
+// memory, replicated to the four 32-lane quarters (4 columns).
+__device__ __forceinline__ void tc_copy_sf(uint32_t taddr, uint64_t src_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src_desc) : "memory");
+}
+
+// D[tmem] (+)= A[smem] x B[smem]^T with E2M1 operands and UE4M3 scales per 16
+// elements (scale_vec::4X), M=128, N from the instruction descriptor, K=64.
+__device__ __forceinline__ void tc_mma_fp4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "setp.ne.b32 p, %6, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n"
+      "}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// 16 consecutive FP32 columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, K-major, 128-byte swizzle: rows of 128
+// bytes, 8-row groups 1024 bytes apart.  The tile base must be 1024-byte
+// aligned; a K offset inside the swizzle atom is added to the start address.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);          // start address
+  d |= (uint64_t)(16u >> 4) << 16;                    // leading byte offset (unused here)
+  d |= (uint64_t)(1024u >> 4) << 32;                  // stride byte offset: 8 rows x 128 B
+  d |= (uint64_t)1 << 46;                             // descriptor version
+  d |= (uint64_t)2 << 61;                             // 128-byte swizzle
+  return d;
+}
+
+// Descriptor of a contiguous 32-row x 16-byte block-scale chunk (no swizzle,
+// 8-row core matrices 128 bytes apart).
+__device__ __forceinline__ uint64_t smem_desc_sf(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(128u >> 4) << 32;                   // stride byte offset
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::mxf4nvf4: E2M1 x E2M1, UE4M3
+// block scales, both operands K-major, dense, M x N.
+__host__ __device__ constexpr uint32_t idesc_fp4(int M, int N) {
+  return (1u << 7)                         // A format: E2M1
+         | (1u << 10)                      // B format: E2M1
+         | ((uint32_t)(N >> 3) << 17)      // N / 8
+         | (0u << 23)                      // scale format: UE4M3
+         | ((uint32_t)(M >> 4) << 24);     // M / 16
+}
+
+// ---------------------------------------------------------------------------
+// Cluster helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float ld_shared_cluster_f32(const void* local_smem, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local_smem)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// NVFP4 conversions and the block quantizer
+// ---------------------------------------------------------------------------
+
+// E4M3 byte of v: round to nearest even, saturating at +-448.
+__device__ __forceinline__ uint32_t cvt_e4m3(float v) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(v));
+  return (uint32_t)(r & 0xFFu);
+}
+
+// Two E2M1 codes packed in a byte: `lo` in bits 0-3, `hi` in bits 4-7; round
+// to nearest even, saturating at +-6.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n"
+      ".reg .b8 t;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n"
+      "cvt.u32.u8 %0, t;\n"
+      "}\n"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r & 0xFFu;
+}
+
+// Exact value of a non-negative E4M3 byte (sign ignored; NaN never produced).
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+  const uint32_t e = (b >> 3) & 0xFu, m = b & 7u;
+  if (e == 0) return (float)m * 0.001953125f;                    // m * 2^-9
+  return __uint_as_float(((e + 120u) << 23) | (m << 20));        // (1 + m/8) * 2^(e-7)
+}
+
+// Global scale 2688 / amax (amax >= 0): 1 for amax == 0, FLT_MAX when the
+// quotient overflows.
+__device__ __forceinline__ float nvfp4_global_scale(float amax) {
+  if (!(amax > 0.0f)) return 1.0f;
+  const float g = __fdiv_rn(2688.0f, amax);
+  return isinf(g) ? 3.402823466e38f : g;
+}
+
+// Quantize one 16-element block given the global scale: returns the E4M3
+// scale byte and writes 8 packed code bytes (element 2i low nibble).
+__device__ __forceinline__ uint32_t nvfp4_quant_block16(const float (&v)[16], float gs, uint2& packed) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const float sf32 = __fdiv_rn(__fmul_rn(amax, gs), 6.0f);
+  const uint32_t sf = cvt_e4m3(sf32);
+  const float sfv = e4m3_value(sf);
+  uint32_t w0 = 0, w1 = 0;
+  if (sfv > 0.0f) {
+    const float q = __fdiv_rn(gs, sfv);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w0 |= cvt_e2m1x2(__fmul_rn(v[2 * i], q), __fmul_rn(v[2 * i + 1], q)) << (8 * i);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      w1 |= cvt_e2m1x2(__fmul_rn(v[8 + 2 * i], q), __fmul_rn(v[8 + 2 * i + 1], q)) << (8 * i);
+  }
+  packed = make_uint2(w0, w1);
+  return sf;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// 16 bf16 values (two 16-byte words) widened to float.
+__device__ __forceinline__ void bf16x16_to_f32(const uint4& a, const uint4& b, float (&v)[16]) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[2 * i] = bf16_lo(w[i]);
+    v[2 * i + 1] = bf16_hi(w[i]);
+  }
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+}  // namespace moe

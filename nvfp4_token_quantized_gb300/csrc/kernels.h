@@ -1,0 +1,86 @@
+// kernels.h - host-side launchers of the sm_103a kernels (internal interface
+// between the C ABI in moe_host.cu and the kernel translation units).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// ---- routing (kernels_route.cu) ----
+cudaError_t launch_router_logits(const void* x, const void* gate_w, const float* bias, float* logits, int T,
+                                 int H, int E, cudaStream_t s);
+cudaError_t launch_topk(const float* logits, int T, int E, int K, int32_t* topk_ids, float* topk_w,
+                        int32_t* counts, cudaStream_t s);
+struct PermuteOut {
+  int32_t* expert_offsets;  // [E+1]
+  int32_t* src_of_row;      // [R]
+  int32_t* row_of_src;      // [R]
+  int32_t* pad_row_of_src;  // [R]
+  int32_t* src_of_padrow;   // [Rpad]
+  int4* tiles;              // [tile bound] {expert, first padded row, valid rows, 0}
+  int32_t* num_tiles;       // [1]
+};
+cudaError_t launch_permute(const int32_t* topk_ids, const int32_t* counts, int T, int K, int E,
+                           const PermuteOut& o, cudaStream_t s);
+
+// ---- quantization (kernels_quant.cu) ----
+cudaError_t launch_act_quant(const void* x, int T, int H, int K, const int32_t* pad_row_of_src,
+                             uint8_t* a_codes, uint8_t* a_sf, float* gs_rows, float* out_acc, cudaStream_t s);
+cudaError_t launch_weight_amax(const void* w, int E, int N, int Kd, uint32_t* amax_bits, cudaStream_t s);
+// interleave: 0 = rows in caller order; 1 = w13 gate/up chunks of 128 rows
+// interleaved so that chunk f of the internal layout is [gate f, up f].
+cudaError_t launch_weight_quant(const void* w, int E, int N, int Kd, int Kpad, int interleave,
+                                const uint32_t* amax_bits, uint8_t* codes, uint8_t* sf, float* gs,
+                                cudaStream_t s);
+cudaError_t launch_export_rows(const uint8_t* codes, const uint8_t* sf, const float* gs_rows, int n_rows,
+                               int Kd, int Kpad, const int32_t* row_map, int map_stride, int row_map_mode,
+                               int E_rows, uint8_t* out_codes, uint8_t* out_sf, float* out_gs, cudaStream_t s);
+cudaError_t launch_convert(const float* in, uint8_t* e2m1, uint8_t* e4m3, int64_t n, cudaStream_t s);
+cudaError_t launch_sf_to_atoms(const uint8_t* sf, int rows, int k16, uint8_t* atoms, cudaStream_t s);
+
+// ---- finalize (kernels_quant.cu) ----
+cudaError_t launch_finalize_atomic(const float* out_acc, void* out, int T, int H, cudaStream_t s);
+cudaError_t launch_finalize_ordered(const float* ybuf, const float* topk_w, void* out, int T, int H, int K,
+                                    cudaStream_t s);
+
+// ---- block-scaled FP4 GEMMs (kernels_gemm.cu) ----
+struct GemmArgs {
+  const uint8_t* a_sf;        // A block scales, 128x4 atoms
+  const uint8_t* b_sf;        // B block scales, 128x4 atoms
+  int k_stages;               // Kpad / 256
+  int kblocks;                // Kpad / 64
+  const int4* tiles;          // {expert, first padded row, valid rows, 0}
+  const int32_t* num_tiles;   // device tile count
+  int b_rows_per_expert;      // 2I (w13) or H (w2)
+  const float* gs_rows;       // global scale per padded A row
+  const float* gs_w;          // global scale per expert
+  // w13 epilogue: SwiGLU + requantization into the w2 operand
+  uint8_t* h_codes;
+  uint8_t* h_sf;
+  float* h_gs;
+  int i_pad;                  // K of the w2 GEMM (padded intermediate width)
+  // w2 epilogue: top-k weighted reduction
+  const int32_t* src_of_padrow;
+  const float* topk_w;
+  int top_k;
+  float* out_acc;             // atomic mode
+  float* ybuf;                // ordered mode
+  int hidden;
+  // plain epilogue (tests)
+  float* d;
+  int ldd;
+  int* status;                // device status word
+};
+
+int gemm_smem_bytes();
+cudaError_t gemm_setup_attributes();
+cudaError_t launch_gemm_w13(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int n_chunks,
+                            int tile_bound, cudaStream_t s);
+cudaError_t launch_gemm_w2(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int n_tiles,
+                           int tile_bound, bool ordered, cudaStream_t s);
+cudaError_t launch_gemm_plain(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int n_tiles,
+                              int m_tiles, cudaStream_t s);
+
+}  // namespace moe

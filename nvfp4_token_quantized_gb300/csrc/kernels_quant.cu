@@ -1,0 +1,267 @@
+// kernels_quant.cu - per-token NVFP4 quantization of the activations (fused
+// with the expert expansion), online NVFP4 conversion of the expert weights,
+// the finalize kernels, and the parity exports.
+//
+// Quantization rules ("CuTe DSL backend gets per-token NVFP4 online
+// quantization and reload", Implementation item 2; the stated reading):
+// gs = 2688 / amax per token (or per expert for weights); per 16-element
+// block sf = E4M3(amax_b * gs / 6); code = E2M1(x * (gs / sf)).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+// One warp per token.  Lane L owns the 16-element blocks L, L+32, ...
+// The token's codes, block scales and global scale are written to each of its
+// K expanded rows (the rows of its K experts in the padded expert-grouped
+// layout the w13 GEMM reads).  In atomic-finalize mode the token's FP32
+// output accumulator row is cleared here as well.
+__global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int K,
+                                                       const int32_t* __restrict__ pad_row_of_src,
+                                                       uint8_t* __restrict__ a_codes, uint8_t* __restrict__ a_sf,
+                                                       float* __restrict__ gs_rows, float* __restrict__ out_acc) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const int nblk = H / SF_VEC;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+
+  float amax = 0.0f;
+  for (int b = lane; b < nblk; b += 32) {
+    float v[16];
+    bf16x16_to_f32(__ldg(xr + 2 * b), __ldg(xr + 2 * b + 1), v);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  }
+  amax = warp_max(amax);
+  const float gs = nvfp4_global_scale(amax);
+
+  int prow[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) prow[j] = j < K ? pad_row_of_src[(size_t)t * K + j] : 0;
+
+  const size_t row_bytes = (size_t)H / 2;
+  for (int b = lane; b < nblk; b += 32) {
+    float v[16];
+    bf16x16_to_f32(__ldg(xr + 2 * b), __ldg(xr + 2 * b + 1), v);
+    uint2 packed;
+    const uint32_t sf = nvfp4_quant_block16(v, gs, packed);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (j < K) {
+        *reinterpret_cast<uint2*>(a_codes + (size_t)prow[j] * row_bytes + 8 * b) = packed;
+        a_sf[sf_atom_offset(prow[j], b, nblk)] = (uint8_t)sf;
+      }
+    }
+  }
+  if (lane < K) gs_rows[pad_row_of_src[(size_t)t * K + lane]] = gs;
+  if (out_acc) {
+    float4* o = reinterpret_cast<float4*>(out_acc + (size_t)t * H);
+    for (int i = lane; i < H / 4; i += 32) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// amax over each expert's whole matrix: grid (chunks, E).
+__global__ void __launch_bounds__(256) weight_amax_kernel(const __nv_bfloat16* __restrict__ w, size_t per_expert,
+                                                         uint32_t* __restrict__ amax_bits) {
+  const int e = blockIdx.y;
+  const uint4* src = reinterpret_cast<const uint4*>(w + (size_t)e * per_expert);
+  const size_t n16 = per_expert / 8;
+  float m = 0.0f;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x) {
+    const uint4 q = __ldg(src + i);
+    const uint32_t ww[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) m = fmaxf(m, fmaxf(fabsf(bf16_lo(ww[k])), fabsf(bf16_hi(ww[k]))));
+  }
+  m = warp_max(m);
+  __shared__ float red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float mm = 0.0f;
+    for (int i = 0; i < 8; ++i) mm = fmaxf(mm, red[i]);
+    atomicMax(&amax_bits[e], __float_as_uint(mm));  // non-negative floats order like their bits
+  }
+}
+
+__device__ __forceinline__ int w13_internal_row(int n, int N) {
+  // caller row n of [gate (I rows); up (I rows)] -> internal row where chunk f
+  // of 256 rows is [gate rows 128f..128f+127, up rows 128f..128f+127]
+  const int I = N / 2;
+  if (n < I) return (n >> 7) * 256 + (n & 127);
+  const int u = n - I;
+  return (u >> 7) * 256 + 128 + (u & 127);
+}
+
+// One warp per (expert, row): block scales and codes of the row with the
+// expert's global scale, written into the internal operand layout.
+__global__ void __launch_bounds__(256) weight_quant_kernel(const __nv_bfloat16* __restrict__ w, int E, int N,
+                                                          int Kd, int Kpad, int interleave,
+                                                          const uint32_t* __restrict__ amax_bits,
+                                                          uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                                                          float* __restrict__ gs_out) {
+  const size_t gw = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (gw >= (size_t)E * N) return;
+  const int e = (int)(gw / N), n = (int)(gw % N);
+  const float gs = nvfp4_global_scale(__uint_as_float(amax_bits[e]));
+  const int irow = e * N + (interleave ? w13_internal_row(n, N) : n);
+  const uint4* src = reinterpret_cast<const uint4*>(w + ((size_t)e * N + n) * Kd);
+  const int nblk = Kd / SF_VEC;
+  for (int b = lane; b < nblk; b += 32) {
+    float v[16];
+    bf16x16_to_f32(__ldg(src + 2 * b), __ldg(src + 2 * b + 1), v);
+    uint2 packed;
+    const uint32_t s = nvfp4_quant_block16(v, gs, packed);
+    *reinterpret_cast<uint2*>(codes + (size_t)irow * (Kpad / 2) + 8 * b) = packed;
+    sf[sf_atom_offset(irow, b, Kpad / SF_VEC)] = (uint8_t)s;
+  }
+  if (n == 0 && lane == 0) gs_out[e] = gs;
+}
+
+// Copy rows from an internal operand layout to canonical row-major arrays.
+// mode 0: internal row = row_map[i * map_stride] (expanded activations /
+//         intermediate);
+// mode 1: internal row = i (weights in caller order);
+// mode 2: internal row = w13 interleave of i within its expert (E_rows rows per expert).
+__global__ void __launch_bounds__(256) export_rows_kernel(const uint8_t* __restrict__ codes,
+                                                         const uint8_t* __restrict__ sf,
+                                                         const float* __restrict__ gs_rows, int n_rows, int Kd,
+                                                         int Kpad, const int32_t* __restrict__ row_map,
+                                                         int map_stride, int mode, int E_rows, uint8_t* __restrict__ out_codes,
+                                                         uint8_t* __restrict__ out_sf, float* __restrict__ out_gs) {
+  const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (i >= n_rows) return;
+  int r;
+  if (mode == 0) r = row_map[(size_t)i * map_stride];
+  else if (mode == 1) r = i;
+  else r = (i / E_rows) * E_rows + w13_internal_row(i % E_rows, E_rows);
+  if (out_codes)
+    for (int b = lane; b < Kd / 2; b += 32) out_codes[(size_t)i * (Kd / 2) + b] = codes[(size_t)r * (Kpad / 2) + b];
+  if (out_sf)
+    for (int b = lane; b < Kd / SF_VEC; b += 32)
+      out_sf[(size_t)i * (Kd / SF_VEC) + b] = sf[sf_atom_offset(r, b, Kpad / SF_VEC)];
+  if (out_gs && gs_rows && lane == 0) out_gs[i] = gs_rows[r];
+}
+
+__global__ void convert_kernel(const float* __restrict__ in, uint8_t* __restrict__ e2m1,
+                               uint8_t* __restrict__ e4m3, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const float v = in[i];
+    if (e2m1) e2m1[i] = (uint8_t)(cvt_e2m1x2(v, 0.0f) & 0xF);
+    if (e4m3) e4m3[i] = (uint8_t)cvt_e4m3(v);
+  }
+}
+
+__global__ void sf_to_atoms_kernel(const uint8_t* __restrict__ sf, int rows, int k16, uint8_t* __restrict__ atoms) {
+  const int64_t n = (int64_t)rows * k16;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int r = (int)(i / k16), b = (int)(i % k16);
+    atoms[sf_atom_offset(r, b, k16)] = sf[i];
+  }
+}
+
+// out = bf16_rn(acc), 8 elements per thread.
+__global__ void __launch_bounds__(256) finalize_atomic_kernel(const float* __restrict__ acc,
+                                                             __nv_bfloat16* __restrict__ out, size_t n8) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+    const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
+    const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+    __nv_bfloat162 o[4] = {__floats2bfloat162_rn(a.x, a.y), __floats2bfloat162_rn(a.z, a.w),
+                           __floats2bfloat162_rn(b.x, b.y), __floats2bfloat162_rn(b.z, b.w)};
+    reinterpret_cast<uint4*>(out)[i] = *reinterpret_cast<const uint4*>(o);
+  }
+}
+
+// out[t][n] = bf16_rn(sum over j ascending of fl32(w[t][j] * y[t*K+j][n])),
+// FP32 partial sums, the first term taken as is.  4 columns per thread.
+__global__ void __launch_bounds__(256) finalize_ordered_kernel(const float* __restrict__ ybuf,
+                                                              const float* __restrict__ topk_w,
+                                                              __nv_bfloat16* __restrict__ out, int T, int H, int K) {
+  const size_t n4 = (size_t)T * H / 4;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t flat = 4 * i;
+    const int t = (int)(flat / H), n = (int)(flat % H);
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < K; ++j) {
+      const float w = topk_w[(size_t)t * K + j];
+      const float4 y = *reinterpret_cast<const float4*>(ybuf + ((size_t)t * K + j) * H + n);
+      const float4 p = make_float4(__fmul_rn(w, y.x), __fmul_rn(w, y.y), __fmul_rn(w, y.z), __fmul_rn(w, y.w));
+      if (j == 0) s = p;
+      else s = make_float4(__fadd_rn(s.x, p.x), __fadd_rn(s.y, p.y), __fadd_rn(s.z, p.z), __fadd_rn(s.w, p.w));
+    }
+    __nv_bfloat162 o[2] = {__floats2bfloat162_rn(s.x, s.y), __floats2bfloat162_rn(s.z, s.w)};
+    *reinterpret_cast<uint2*>(out + flat) = *reinterpret_cast<const uint2*>(o);
+  }
+}
+
+int grid_for(size_t n, int per_block, int cap = 152 * 16) {
+  size_t g = (n + per_block - 1) / per_block;
+  if (g < 1) g = 1;
+  if (g > (size_t)cap) g = cap;
+  return (int)g;
+}
+
+}  // namespace
+
+cudaError_t launch_act_quant(const void* x, int T, int H, int K, const int32_t* pad_row_of_src, uint8_t* a_codes,
+                             uint8_t* a_sf, float* gs_rows, float* out_acc, cudaStream_t s) {
+  act_quant_kernel<<<(T + 7) / 8, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(x), T, H, K, pad_row_of_src,
+                                               a_codes, a_sf, gs_rows, out_acc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_weight_amax(const void* w, int E, int N, int Kd, uint32_t* amax_bits, cudaStream_t s) {
+  const size_t per = (size_t)N * Kd;
+  dim3 grid(grid_for(per / 8, 256 * 8, 64), E);
+  weight_amax_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(w), per, amax_bits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_weight_quant(const void* w, int E, int N, int Kd, int Kpad, int interleave,
+                                const uint32_t* amax_bits, uint8_t* codes, uint8_t* sf, float* gs, cudaStream_t s) {
+  const size_t warps = (size_t)E * N;
+  weight_quant_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(w), E, N, Kd,
+                                                                  Kpad, interleave, amax_bits, codes, sf, gs);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_export_rows(const uint8_t* codes, const uint8_t* sf, const float* gs_rows, int n_rows, int Kd,
+                               int Kpad, const int32_t* row_map, int map_stride, int row_map_mode, int E_rows,
+                               uint8_t* out_codes, uint8_t* out_sf, float* out_gs, cudaStream_t s) {
+  if (n_rows <= 0) return cudaSuccess;
+  export_rows_kernel<<<(n_rows + 7) / 8, 256, 0, s>>>(codes, sf, gs_rows, n_rows, Kd, Kpad, row_map, map_stride,
+                                                      row_map_mode, E_rows, out_codes, out_sf, out_gs);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_convert(const float* in, uint8_t* e2m1, uint8_t* e4m3, int64_t n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  convert_kernel<<<grid_for((size_t)n, 256), 256, 0, s>>>(in, e2m1, e4m3, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sf_to_atoms(const uint8_t* sf, int rows, int k16, uint8_t* atoms, cudaStream_t s) {
+  sf_to_atoms_kernel<<<grid_for((size_t)rows * k16, 256), 256, 0, s>>>(sf, rows, k16, atoms);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize_atomic(const float* out_acc, void* out, int T, int H, cudaStream_t s) {
+  const size_t n8 = (size_t)T * H / 8;
+  finalize_atomic_kernel<<<grid_for(n8, 256), 256, 0, s>>>(out_acc, reinterpret_cast<__nv_bfloat16*>(out), n8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize_ordered(const float* ybuf, const float* topk_w, void* out, int T, int H, int K,
+                                    cudaStream_t s) {
+  const size_t n4 = (size_t)T * H / 4;
+  finalize_ordered_kernel<<<grid_for(n4, 256), 256, 0, s>>>(ybuf, topk_w, reinterpret_cast<__nv_bfloat16*>(out), T,
+                                                            H, K);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,650 @@
+// moe_host.cu - the C ABI (include/moe_nvfp4.h): handle lifetime, worst-case
+// buffer planning, online weight conversion, in-place refresh, and the
+// stream-ordered launch sequence of one forward.
+//
+// Buffers are sized once at moe_create from max_num_tokens ("size CuteDSL MoE
+// allgather buffers for the worst-case forward", Implementation items 1-3);
+// a larger forward is refused with MOE_ERR_TOO_MANY_TOKENS.  Weight reload
+// rewrites the same buffers ("CuTe DSL backend gets per-token NVFP4 online
+// quantization and reload", Implementation item 3 and the refresh snippet).
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/moe_nvfp4.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace moe;
+
+struct moe_handle {
+  moe_config cfg{};
+  int H = 0, I = 0, E = 0, K = 0, Tmax = 0;
+  int Ipad = 0;         // intermediate width padded to a multiple of 256 (w2 GEMM K)
+  int Rmax = 0;         // Tmax * K
+  int Rpad = 0;         // padded expert-grouped rows, worst case
+  int tile_cap = 0;     // worst-case number of 128-row tiles
+  bool deterministic = false;
+  bool loaded = false;
+  moe_weight_desc w13_desc{}, w2_desc{};
+  int last_T = -1;
+  std::string err;
+  size_t bytes = 0;
+  std::vector<void*> allocs;
+
+  // weights (internal operand layouts)
+  uint8_t *w13_codes = nullptr, *w13_sf = nullptr, *w2_codes = nullptr, *w2_sf = nullptr;
+  float *gs_w13 = nullptr, *gs_w2 = nullptr;
+  uint32_t* amax_bits = nullptr;  // [2E]
+
+  // routing workspace
+  float* logits = nullptr;
+  int32_t *topk_ids = nullptr, *counts = nullptr, *expert_offsets = nullptr;
+  float* topk_w = nullptr;
+  int32_t *src_of_row = nullptr, *row_of_src = nullptr, *pad_row_of_src = nullptr, *src_of_padrow = nullptr;
+  int4* tiles = nullptr;
+  int32_t* num_tiles = nullptr;
+
+  // operands of the two GEMMs
+  uint8_t *a_codes = nullptr, *a_sf = nullptr, *h_codes = nullptr, *h_sf = nullptr;
+  float *gs_rows = nullptr, *h_gs = nullptr;
+  float *out_acc = nullptr, *ybuf = nullptr;
+
+  // staging for moe_forward_host
+  void *stage_x = nullptr, *stage_gate = nullptr, *stage_out = nullptr;
+  float* stage_bias = nullptr;
+
+  // host-visible device status word (mapped pinned memory)
+  int* status_host = nullptr;
+  int* status_dev = nullptr;
+
+  CUtensorMap tm_a1{}, tm_b1{}, tm_a2{}, tm_b2{};
+};
+
+namespace {
+
+void set_err(moe_handle* h, const char* fmt, ...) {
+  if (!h) return;
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  h->err = buf;
+}
+
+moe_status cuda_fail(moe_handle* h, cudaError_t e, const char* what) {
+  set_err(h, "%s: %s", what, cudaGetErrorString(e));
+  return MOE_ERR_CUDA;
+}
+
+#define CK(h, call)                                             \
+  do {                                                          \
+    cudaError_t e_ = (call);                                    \
+    if (e_ != cudaSuccess) return cuda_fail((h), e_, #call);    \
+  } while (0)
+
+template <typename T>
+moe_status dalloc(moe_handle* h, T** p, size_t bytes) {
+  bytes = (bytes + 255) & ~size_t(255);
+  if (bytes == 0) bytes = 256;
+  void* q = nullptr;
+  cudaError_t e = cudaMalloc(&q, bytes);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaMalloc");
+  e = cudaMemset(q, 0, bytes);
+  if (e != cudaSuccess) {
+    cudaFree(q);
+    return cuda_fail(h, e, "cudaMemset");
+  }
+  h->allocs.push_back(q);
+  h->bytes += bytes;
+  *p = reinterpret_cast<T*>(q);
+  return MOE_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2D byte tensor [rows, row_bytes] with a 128-byte-wide box of box_rows rows,
+// 128-byte swizzle (the K-major operand layout of the FP4 MMAs).
+moe_status make_operand_map(moe_handle* h, CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows,
+                            uint32_t box_rows) {
+  auto fn = get_encode_fn();
+  if (!fn) {
+    set_err(h, "cuTensorMapEncodeTiled is not available from the driver");
+    return MOE_ERR_CUDA;
+  }
+  cuuint64_t dims[2] = {row_bytes, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_err(h, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+#define TRY(x)                         \
+  do {                                 \
+    moe_status s_ = (x);               \
+    if (s_ != MOE_OK) return s_;       \
+  } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+int device_of(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) return -1;
+  return at.device;
+}
+
+// Worst-case number of 128-row tiles when T tokens each pick K of E experts.
+int tile_bound(int T, int K, int E) {
+  const long R = (long)T * K;
+  const long busy = std::min<long>(E, R);
+  const long a = (R + 127L * busy) / 128;
+  const long b = busy * ((T + 127L) / 128);
+  return (int)std::max<long>(1, std::min(a, b));
+}
+
+moe_status check_weight_desc(moe_handle* h, const moe_weight_desc* d, const void* ptr, int64_t d0, int64_t d1,
+                             int64_t d2, const char* name) {
+  if (!d || !ptr) {
+    set_err(h, "%s: NULL pointer or descriptor", name);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (d->dtype != MOE_DTYPE_BF16) {
+    set_err(h, "%s: dtype must be MOE_DTYPE_BF16", name);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (d->dims[0] != d0 || d->dims[1] != d1 || d->dims[2] != d2) {
+    set_err(h, "%s: shape [%lld, %lld, %lld] does not match the configuration [%lld, %lld, %lld]", name,
+            (long long)d->dims[0], (long long)d->dims[1], (long long)d->dims[2], (long long)d0, (long long)d1,
+            (long long)d2);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (d->device != h->cfg.device || device_of(ptr) != h->cfg.device) {
+    set_err(h, "%s: data is not on device %d", name, h->cfg.device);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (!aligned16(ptr)) {
+    set_err(h, "%s: pointer must be 16-byte aligned", name);
+    return MOE_ERR_INVALID_ARG;
+  }
+  return MOE_OK;
+}
+
+bool same_desc(const moe_weight_desc& a, const moe_weight_desc& b) {
+  return a.dims[0] == b.dims[0] && a.dims[1] == b.dims[1] && a.dims[2] == b.dims[2] && a.dtype == b.dtype &&
+         a.device == b.device;
+}
+
+moe_status quantize_weights(moe_handle* h, const void* w13, const void* w2, cudaStream_t s) {
+  CK(h, cudaMemsetAsync(h->amax_bits, 0, sizeof(uint32_t) * 2 * h->E, s));
+  CK(h, launch_weight_amax(w13, h->E, 2 * h->I, h->H, h->amax_bits, s));
+  CK(h, launch_weight_amax(w2, h->E, h->H, h->I, h->amax_bits + h->E, s));
+  CK(h, launch_weight_quant(w13, h->E, 2 * h->I, h->H, h->H, 1, h->amax_bits, h->w13_codes, h->w13_sf, h->gs_w13,
+                            s));
+  CK(h, launch_weight_quant(w2, h->E, h->H, h->I, h->Ipad, 0, h->amax_bits + h->E, h->w2_codes, h->w2_sf, h->gs_w2,
+                            s));
+  return MOE_OK;
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    int cur;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const float* bias, void* out, int T,
+                        cudaStream_t s) {
+  const int H = h->H, E = h->E, K = h->K;
+  if (T > 0) {
+    CK(h, cudaMemsetAsync(h->counts, 0, sizeof(int32_t) * E, s));
+    CK(h, launch_router_logits(x, gate_w, bias, h->logits, T, H, E, s));
+    CK(h, launch_topk(h->logits, T, E, K, h->topk_ids, h->topk_w, h->counts, s));
+    PermuteOut po{h->expert_offsets, h->src_of_row, h->row_of_src, h->pad_row_of_src,
+                  h->src_of_padrow,  h->tiles,      h->num_tiles};
+    CK(h, launch_permute(h->topk_ids, h->counts, T, K, E, po, s));
+    CK(h, launch_act_quant(x, T, H, K, h->pad_row_of_src, h->a_codes, h->a_sf, h->gs_rows,
+                           h->deterministic ? nullptr : h->out_acc, s));
+    const int tb = tile_bound(T, K, E);
+    GemmArgs g{};
+    g.status = h->status_dev;
+    g.tiles = h->tiles;
+    g.num_tiles = h->num_tiles;
+    // w13: A = expanded activations [Rpad, H], B = w13 [E*2I, H]
+    g.a_sf = h->a_sf;
+    g.b_sf = h->w13_sf;
+    g.k_stages = H / STAGE_K;
+    g.kblocks = H / MMA_K;
+    g.b_rows_per_expert = 2 * h->I;
+    g.gs_rows = h->gs_rows;
+    g.gs_w = h->gs_w13;
+    g.h_codes = h->h_codes;
+    g.h_sf = h->h_sf;
+    g.h_gs = h->h_gs;
+    g.i_pad = h->Ipad;
+    CK(h, launch_gemm_w13(h->tm_a1, h->tm_b1, g, h->I / 128, tb, s));
+    // w2: A = requantized intermediate [Rpad, Ipad], B = w2 [E*H, Ipad]
+    GemmArgs g2{};
+    g2.status = h->status_dev;
+    g2.tiles = h->tiles;
+    g2.num_tiles = h->num_tiles;
+    g2.a_sf = h->h_sf;
+    g2.b_sf = h->w2_sf;
+    g2.k_stages = h->Ipad / STAGE_K;
+    g2.kblocks = h->Ipad / MMA_K;
+    g2.b_rows_per_expert = H;
+    g2.gs_rows = h->h_gs;
+    g2.gs_w = h->gs_w2;
+    g2.src_of_padrow = h->src_of_padrow;
+    g2.topk_w = h->topk_w;
+    g2.top_k = K;
+    g2.out_acc = h->out_acc;
+    g2.ybuf = h->ybuf;
+    g2.hidden = H;
+    CK(h, launch_gemm_w2(h->tm_a2, h->tm_b2, g2, H / TILE_N, tb, h->deterministic, s));
+    if (h->deterministic) CK(h, launch_finalize_ordered(h->ybuf, h->topk_w, out, T, H, K, s));
+    else CK(h, launch_finalize_atomic(h->out_acc, out, T, H, s));
+  }
+  h->last_T = T;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_TOO_MANY_TOKENS: return "MOE_ERR_TOO_MANY_TOKENS";
+    case MOE_ERR_NOT_LOADED: return "MOE_ERR_NOT_LOADED";
+    case MOE_ERR_METADATA_CHANGED: return "MOE_ERR_METADATA_CHANGED";
+    case MOE_ERR_ALIAS: return "MOE_ERR_ALIAS";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+moe_status moe_create(const moe_config* cfg, moe_handle** out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg) return MOE_ERR_INVALID_ARG;
+  const int H = cfg->hidden, I = cfg->inter, E = cfg->num_experts, K = cfg->top_k, T = cfg->max_num_tokens;
+  if (H <= 0 || I <= 0 || E <= 0 || K <= 0 || T <= 0) return MOE_ERR_INVALID_ARG;
+  if (H % 256 || I % 128 || E % 8 || E > 256 || K > E || K > 16 || I / 128 > 16) return MOE_ERR_UNSUPPORTED;
+  if ((long)T * K > (1L << 30)) return MOE_ERR_UNSUPPORTED;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || cfg->device < 0 || cfg->device >= ndev) {
+    cudaGetLastError();
+    return MOE_ERR_UNSUPPORTED;
+  }
+  cudaDeviceProp prop{};
+  if (cudaGetDeviceProperties(&prop, cfg->device) != cudaSuccess || prop.major != 10 || prop.minor != 3) {
+    cudaGetLastError();
+    return MOE_ERR_UNSUPPORTED;
+  }
+  DeviceGuard dg(cfg->device);
+  moe_handle* h = new moe_handle();
+  h->cfg = *cfg;
+  h->H = H;
+  h->I = I;
+  h->E = E;
+  h->K = K;
+  h->Tmax = T;
+  h->Ipad = (I + 255) / 256 * 256;
+  h->Rmax = T * K;
+  h->Rpad = (h->Rmax + 127 * std::min(E, h->Rmax) + 127) / 128 * 128;
+  h->tile_cap = tile_bound(T, K, E);
+  h->deterministic = (cfg->flags & MOE_FLAG_DETERMINISTIC) != 0;
+
+  auto fail = [&](moe_status s) {
+    moe_destroy(h);
+    return s;
+  };
+#define A(ptr, bytes)                                \
+  do {                                               \
+    moe_status s_ = dalloc(h, &(ptr), (bytes));      \
+    if (s_ != MOE_OK) return fail(s_);               \
+  } while (0)
+  const size_t Rp = h->Rpad;
+  A(h->w13_codes, (size_t)E * 2 * I * (H / 2));
+  A(h->w13_sf, (size_t)E * 2 * I * (H / 16));
+  A(h->w2_codes, (size_t)E * H * (h->Ipad / 2));
+  A(h->w2_sf, (size_t)E * H * (h->Ipad / 16));
+  A(h->gs_w13, sizeof(float) * E);
+  A(h->gs_w2, sizeof(float) * E);
+  A(h->amax_bits, sizeof(uint32_t) * 2 * E);
+  A(h->logits, sizeof(float) * (size_t)T * E);
+  A(h->topk_ids, sizeof(int32_t) * (size_t)T * K);
+  A(h->topk_w, sizeof(float) * (size_t)T * K);
+  A(h->counts, sizeof(int32_t) * E);
+  A(h->expert_offsets, sizeof(int32_t) * (E + 1));
+  A(h->src_of_row, sizeof(int32_t) * (size_t)h->Rmax);
+  A(h->row_of_src, sizeof(int32_t) * (size_t)h->Rmax);
+  A(h->pad_row_of_src, sizeof(int32_t) * (size_t)h->Rmax);
+  A(h->src_of_padrow, sizeof(int32_t) * Rp);
+  A(h->tiles, sizeof(int4) * (size_t)h->tile_cap);
+  A(h->num_tiles, sizeof(int32_t) * 4);
+  A(h->a_codes, Rp * (H / 2));
+  A(h->a_sf, Rp * (H / 16));
+  A(h->gs_rows, sizeof(float) * Rp);
+  A(h->h_codes, Rp * (h->Ipad / 2));
+  A(h->h_sf, Rp * (h->Ipad / 16));
+  A(h->h_gs, sizeof(float) * Rp);
+  if (h->deterministic) A(h->ybuf, sizeof(float) * (size_t)h->Rmax * H);
+  else A(h->out_acc, sizeof(float) * (size_t)T * H);
+  A(h->stage_x, sizeof(uint16_t) * (size_t)T * H);
+  A(h->stage_gate, sizeof(uint16_t) * (size_t)H * E);
+  A(h->stage_bias, sizeof(float) * E);
+  A(h->stage_out, sizeof(uint16_t) * (size_t)T * H);
+#undef A
+  {
+    cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&h->status_host), sizeof(int), cudaHostAllocMapped);
+    if (e != cudaSuccess) return fail(cuda_fail(h, e, "cudaHostAlloc"));
+    *h->status_host = 0;
+    e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&h->status_dev), h->status_host, 0);
+    if (e != cudaSuccess) return fail(cuda_fail(h, e, "cudaHostGetDevicePointer"));
+  }
+  moe_status st;
+  if ((st = make_operand_map(h, &h->tm_a1, h->a_codes, H / 2, Rp, 32)) != MOE_OK) return fail(st);
+  if ((st = make_operand_map(h, &h->tm_b1, h->w13_codes, H / 2, (uint64_t)E * 2 * I, 256)) != MOE_OK)
+    return fail(st);
+  if ((st = make_operand_map(h, &h->tm_a2, h->h_codes, h->Ipad / 2, Rp, 32)) != MOE_OK) return fail(st);
+  if ((st = make_operand_map(h, &h->tm_b2, h->w2_codes, h->Ipad / 2, (uint64_t)E * H, 256)) != MOE_OK)
+    return fail(st);
+  {
+    cudaError_t e = gemm_setup_attributes();
+    if (e != cudaSuccess) return fail(cuda_fail(h, e, "cudaFuncSetAttribute"));
+  }
+  *out = h;
+  return MOE_OK;
+}
+
+moe_status moe_destroy(moe_handle* h) {
+  if (!h) return MOE_OK;
+  DeviceGuard dg(h->cfg.device);
+  cudaDeviceSynchronize();
+  for (void* p : h->allocs) cudaFree(p);
+  if (h->status_host) cudaFreeHost(h->status_host);
+  cudaGetLastError();
+  delete h;
+  return MOE_OK;
+}
+
+moe_status moe_load_weights(moe_handle* h, const void* w13, const moe_weight_desc* w13_desc, const void* w2,
+                            const moe_weight_desc* w2_desc, void* stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  DeviceGuard dg(h->cfg.device);
+  TRY(check_weight_desc(h, w13_desc, w13, h->E, 2 * h->I, h->H, "w13"));
+  TRY(check_weight_desc(h, w2_desc, w2, h->E, h->H, h->I, "w2"));
+  TRY(quantize_weights(h, w13, w2, reinterpret_cast<cudaStream_t>(stream)));
+  h->w13_desc = *w13_desc;
+  h->w2_desc = *w2_desc;
+  h->loaded = true;
+  h->err.clear();
+  return MOE_OK;
+}
+
+moe_status moe_refresh_scales_inplace(moe_handle* h, const void* w13, const moe_weight_desc* w13_desc,
+                                      const void* w2, const moe_weight_desc* w2_desc, void* stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  DeviceGuard dg(h->cfg.device);
+  if (!h->loaded) {
+    set_err(h, "refresh before the first moe_load_weights");
+    return MOE_ERR_NOT_LOADED;
+  }
+  if (!w13_desc || !w2_desc || !same_desc(*w13_desc, h->w13_desc) || !same_desc(*w2_desc, h->w2_desc)) {
+    set_err(h, "weight metadata changed during reload; CUDA graph recapture is required");
+    return MOE_ERR_METADATA_CHANGED;
+  }
+  TRY(check_weight_desc(h, w13_desc, w13, h->E, 2 * h->I, h->H, "w13"));
+  TRY(check_weight_desc(h, w2_desc, w2, h->E, h->H, h->I, "w2"));
+  TRY(quantize_weights(h, w13, w2, reinterpret_cast<cudaStream_t>(stream)));
+  h->err.clear();
+  return MOE_OK;
+}
+
+moe_status moe_forward_ex(moe_handle* h, const void* x, const void* gate_w, const float* gate_bias, void* out,
+                          int num_tokens, void* stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  if (h->status_host && *(volatile int*)h->status_host) {
+    set_err(h, "a kernel of this handle gave up a bounded wait (device status 0x%x)", *(volatile int*)h->status_host);
+    return MOE_ERR_DEVICE_TIMEOUT;
+  }
+  if (!h->loaded) {
+    set_err(h, "moe_forward before moe_load_weights");
+    return MOE_ERR_NOT_LOADED;
+  }
+  if (num_tokens < 0) {
+    set_err(h, "num_tokens (%d) is negative", num_tokens);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (num_tokens > h->Tmax) {
+    set_err(h, "num_tokens (%d) exceeds max_num_tokens (%d)", num_tokens, h->Tmax);
+    return MOE_ERR_TOO_MANY_TOKENS;
+  }
+  if (num_tokens == 0) {
+    h->last_T = 0;
+    return MOE_OK;
+  }
+  if (!x || !gate_w || !out) {
+    set_err(h, "NULL x, gate_w or out");
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (!aligned16(x) || !aligned16(gate_w) || !aligned16(out) || (gate_bias && !aligned16(gate_bias))) {
+    set_err(h, "x, gate_w, out and gate_bias must be 16-byte aligned");
+    return MOE_ERR_INVALID_ARG;
+  }
+  const size_t act_bytes = (size_t)num_tokens * h->H * 2;
+  if (ranges_overlap(x, act_bytes, out, act_bytes)) {
+    set_err(h, "out must not overlap x (the routed output never aliases its input)");
+    return MOE_ERR_ALIAS;
+  }
+  DeviceGuard dg(h->cfg.device);
+  return forward_impl(h, x, gate_w, gate_bias, out, num_tokens, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_forward(moe_handle* h, const void* x, const void* gate_w, void* out, int num_tokens, void* stream) {
+  return moe_forward_ex(h, x, gate_w, nullptr, out, num_tokens, stream);
+}
+
+moe_status moe_forward_host(moe_handle* h, const void* x_host, const void* gate_w_host, const float* gate_bias_host,
+                            void* out_host, int num_tokens, void* stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  if (num_tokens < 0 || num_tokens > h->Tmax) {
+    set_err(h, "num_tokens (%d) outside [0, %d]", num_tokens, h->Tmax);
+    return num_tokens < 0 ? MOE_ERR_INVALID_ARG : MOE_ERR_TOO_MANY_TOKENS;
+  }
+  if (num_tokens > 0 && (!x_host || !gate_w_host || !out_host)) {
+    set_err(h, "NULL host pointer");
+    return MOE_ERR_INVALID_ARG;
+  }
+  DeviceGuard dg(h->cfg.device);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (num_tokens == 0) return moe_forward_ex(h, nullptr, nullptr, nullptr, nullptr, 0, stream);
+  const size_t xb = (size_t)num_tokens * h->H * 2;
+  CK(h, cudaMemcpyAsync(h->stage_x, x_host, xb, cudaMemcpyHostToDevice, s));
+  CK(h, cudaMemcpyAsync(h->stage_gate, gate_w_host, (size_t)h->H * h->E * 2, cudaMemcpyHostToDevice, s));
+  if (gate_bias_host) CK(h, cudaMemcpyAsync(h->stage_bias, gate_bias_host, sizeof(float) * h->E, cudaMemcpyHostToDevice, s));
+  TRY(moe_forward_ex(h, h->stage_x, h->stage_gate, gate_bias_host ? h->stage_bias : nullptr, h->stage_out,
+                     num_tokens, stream));
+  CK(h, cudaMemcpyAsync(out_host, h->stage_out, xb, cudaMemcpyDeviceToHost, s));
+  CK(h, cudaStreamSynchronize(s));
+  return moe_get_status(h);
+}
+
+size_t moe_get_workspace_bytes(const moe_handle* h) { return h ? h->bytes : 0; }
+
+const char* moe_get_last_error(const moe_handle* h) { return h ? h->err.c_str() : "NULL handle"; }
+
+moe_status moe_get_status(const moe_handle* h) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  return (h->status_host && *(volatile int*)h->status_host) ? MOE_ERR_DEVICE_TIMEOUT : MOE_OK;
+}
+
+moe_status moe_debug_routing(moe_handle* h, int32_t* topk_ids, float* topk_w, int32_t* src_of_row,
+                             int32_t* expert_offsets, void* stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  if (h->last_T < 0) {
+    set_err(h, "no forward has run on this handle");
+    return MOE_ERR_NOT_LOADED;
+  }
+  DeviceGuard dg(h->cfg.device);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t tk = (size_t)h->last_T * h->K;
+  if (topk_ids && tk) CK(h, cudaMemcpyAsync(topk_ids, h->topk_ids, tk * 4, cudaMemcpyDeviceToDevice, s));
+  if (topk_w && tk) CK(h, cudaMemcpyAsync(topk_w, h->topk_w, tk * 4, cudaMemcpyDeviceToDevice, s));
+  if (src_of_row && tk) CK(h, cudaMemcpyAsync(src_of_row, h->src_of_row, tk * 4, cudaMemcpyDeviceToDevice, s));
+  if (expert_offsets) {
+    if (h->last_T == 0) CK(h, cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (h->E + 1), s));
+    else CK(h, cudaMemcpyAsync(expert_offsets, h->expert_offsets, sizeof(int32_t) * (h->E + 1),
+                               cudaMemcpyDeviceToDevice, s));
+  }
+  return MOE_OK;
+}
+
+moe_status moe_debug_logits(moe_handle* h, float* logits, void* stream) {
+  if (!h || !logits) return MOE_ERR_INVALID_ARG;
+  if (h->last_T < 0) return MOE_ERR_NOT_LOADED;
+  DeviceGuard dg(h->cfg.device);
+  if (h->last_T)
+    CK(h, cudaMemcpyAsync(logits, h->logits, sizeof(float) * (size_t)h->last_T * h->E, cudaMemcpyDeviceToDevice,
+                          reinterpret_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+moe_status moe_debug_act_quant(moe_handle* h, uint8_t* codes, uint8_t* sf, float* gs, void* stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  if (h->last_T < 0) return MOE_ERR_NOT_LOADED;
+  DeviceGuard dg(h->cfg.device);
+  // token t's quantization is the one written to its slot-0 expanded row,
+  // pad_row_of_src[t*K].
+  if (h->last_T == 0) return MOE_OK;
+  CK(h, launch_export_rows(h->a_codes, h->a_sf, h->gs_rows, h->last_T, h->H, h->H, h->pad_row_of_src, h->K, 0, 0,
+                           codes, sf, gs, reinterpret_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+moe_status moe_debug_weight_quant(moe_handle* h, int which, uint8_t* codes, uint8_t* sf, float* gs, void* stream) {
+  if (!h || (which != 0 && which != 1)) return MOE_ERR_INVALID_ARG;
+  if (!h->loaded) return MOE_ERR_NOT_LOADED;
+  DeviceGuard dg(h->cfg.device);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (which == 0) {
+    CK(h, launch_export_rows(h->w13_codes, h->w13_sf, nullptr, h->E * 2 * h->I, h->H, h->H, nullptr, 0, 2,
+                             2 * h->I, codes, sf, nullptr, s));
+    if (gs) CK(h, cudaMemcpyAsync(gs, h->gs_w13, sizeof(float) * h->E, cudaMemcpyDeviceToDevice, s));
+  } else {
+    CK(h, launch_export_rows(h->w2_codes, h->w2_sf, nullptr, h->E * h->H, h->I, h->Ipad, nullptr, 0, 1, 0, codes,
+                             sf, nullptr, s));
+    if (gs) CK(h, cudaMemcpyAsync(gs, h->gs_w2, sizeof(float) * h->E, cudaMemcpyDeviceToDevice, s));
+  }
+  return MOE_OK;
+}
+
+moe_status moe_debug_intermediate(moe_handle* h, uint8_t* h_codes, uint8_t* h_sf, float* h_gs, void* stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  if (h->last_T < 0) return MOE_ERR_NOT_LOADED;
+  DeviceGuard dg(h->cfg.device);
+  if (h->last_T == 0) return MOE_OK;
+  CK(h, launch_export_rows(h->h_codes, h->h_sf, h->h_gs, h->last_T * h->K, h->I, h->Ipad, h->pad_row_of_src, 1, 0,
+                           0, h_codes, h_sf, h_gs, reinterpret_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+moe_status moe_debug_buffer_ptrs(const moe_handle* h, const void** ptrs, int* n) {
+  if (!h || !n) return MOE_ERR_INVALID_ARG;
+  const int have = (int)h->allocs.size();
+  if (ptrs) {
+    for (int i = 0; i < std::min(*n, have); ++i) ptrs[i] = h->allocs[i];
+  }
+  *n = have;
+  return MOE_OK;
+}
+
+moe_status moe_debug_convert(const float* in, uint8_t* e2m1, uint8_t* e4m3, int64_t n, void* stream) {
+  if (n < 0 || (n > 0 && !in)) return MOE_ERR_INVALID_ARG;
+  cudaError_t e = launch_convert(in, e2m1, e4m3, n, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_debug_block_scaled_gemm(const uint8_t* a_codes, const uint8_t* a_sf, const uint8_t* b_codes,
+                                       const uint8_t* b_sf, float* d, int M, int N, int K, void* stream) {
+  if (!a_codes || !a_sf || !b_codes || !b_sf || !d) return MOE_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || K <= 0 || M % 128 || N % 256 || K % 256) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(a_codes) || !aligned16(b_codes) || !aligned16(d)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t *sfa = nullptr, *sfb = nullptr;
+  moe_handle tmp;  // error sink only
+  if (cudaMalloc(&sfa, (size_t)M * K / 16) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMalloc(&sfb, (size_t)N * K / 16) != cudaSuccess) {
+    cudaFree(sfa);
+    return MOE_ERR_CUDA;
+  }
+  moe_status st = MOE_OK;
+  CUtensorMap ta, tb;
+  if (launch_sf_to_atoms(a_sf, M, K / 16, sfa, s) != cudaSuccess ||
+      launch_sf_to_atoms(b_sf, N, K / 16, sfb, s) != cudaSuccess)
+    st = MOE_ERR_CUDA;
+  if (st == MOE_OK) st = make_operand_map(&tmp, &ta, a_codes, K / 2, M, 32);
+  if (st == MOE_OK) st = make_operand_map(&tmp, &tb, b_codes, K / 2, N, 256);
+  if (st == MOE_OK && gemm_setup_attributes() != cudaSuccess) st = MOE_ERR_CUDA;
+  if (st == MOE_OK) {
+    GemmArgs g{};
+    g.a_sf = sfa;
+    g.b_sf = sfb;
+    g.k_stages = K / STAGE_K;
+    g.kblocks = K / MMA_K;
+    g.d = d;
+    g.ldd = N;
+    if (launch_gemm_plain(ta, tb, g, N / TILE_N, M / TILE_M, s) != cudaSuccess) st = MOE_ERR_CUDA;
+  }
+  if (cudaStreamSynchronize(s) != cudaSuccess) st = MOE_ERR_CUDA;
+  cudaFree(sfa);
+  cudaFree(sfb);
+  return st;
+}
+
+}  // extern "C"
