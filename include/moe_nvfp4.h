@@ -173,6 +173,25 @@ MOE_API const char* moe_status_string(moe_status s);
 MOE_API moe_status moe_get_status(const moe_handle* h);
 
 /* ---------------------------------------------------------------------------
+ * Stage timing (tracing).  When enabled, moe_forward records a CUDA event
+ * before its first kernel and after each of its MOE_NUM_STAGES stages; inside
+ * a stream capture the records become event nodes of the graph, so every
+ * replay re-records them.  moe_get_stage_times returns the durations of the
+ * last completed forward or replay (synchronise first).  Enabling allocates
+ * the events; call it before any capture.
+ * ------------------------------------------------------------------------ */
+#define MOE_NUM_STAGES 7  /* router, top-k, permute, quantize, gemm_w13, gemm_w2, finalize */
+
+MOE_API moe_status moe_set_stage_timing(moe_handle* h, int enable);
+
+/* ms[i] = duration of stage i in milliseconds; on entry *n is the capacity of
+ * ms, on return the number of stages written. */
+MOE_API moe_status moe_get_stage_times(const moe_handle* h, float* ms, int* n);
+
+/* Name of stage i ("router", "topk", ...), or NULL. */
+MOE_API const char* moe_stage_name(int i);
+
+/* ---------------------------------------------------------------------------
  * Parity exports.  Each copies state left by the LAST moe_forward on the
  * handle (or by the last load/refresh for the weights) into caller device
  * buffers, in canonical row-major layouts, on `stream`.  T below is that

@@ -33,8 +33,10 @@ EXPORTED = (
     "moe_forward_ex", "moe_forward_host", "moe_get_workspace_bytes", "moe_get_last_error",
     "moe_status_string", "moe_get_status", "moe_debug_routing", "moe_debug_logits",
     "moe_debug_act_quant", "moe_debug_weight_quant", "moe_debug_intermediate", "moe_debug_buffer_ptrs",
-    "moe_debug_convert", "moe_debug_block_scaled_gemm",
+    "moe_debug_convert", "moe_debug_block_scaled_gemm", "moe_set_stage_timing", "moe_get_stage_times",
+    "moe_stage_name",
 )
+MOE_NUM_STAGES = 7
 
 
 class moe_config(ctypes.Structure):
@@ -91,6 +93,9 @@ def load_library() -> ctypes.CDLL:
         "moe_debug_buffer_ptrs": (I, [P, ctypes.POINTER(P), ctypes.POINTER(I)]),
         "moe_debug_convert": (I, [P, P, P, L, P]),
         "moe_debug_block_scaled_gemm": (I, [P, P, P, P, P, I, I, I, P]),
+        "moe_set_stage_timing": (I, [P, I]),
+        "moe_get_stage_times": (I, [P, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(I)]),
+        "moe_stage_name": (ctypes.c_char_p, [I]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -327,6 +332,17 @@ class MoE:
         _raise(self._h, load_library().moe_debug_intermediate(self._h, _ptr(codes), _ptr(sf), _ptr(gs),
                                                               _stream(stream)))
         return codes, sf, gs
+
+    def set_stage_timing(self, enable: bool = True):
+        _raise(self._h, load_library().moe_set_stage_timing(self._h, int(enable)))
+
+    def stage_times(self) -> dict:
+        """Durations (ms) of the stages of the last completed forward / replay."""
+        lib = load_library()
+        arr = (ctypes.c_float * MOE_NUM_STAGES)()
+        n = ctypes.c_int(MOE_NUM_STAGES)
+        _raise(self._h, lib.moe_get_stage_times(self._h, arr, ctypes.byref(n)))
+        return {lib.moe_stage_name(i).decode(): float(arr[i]) for i in range(n.value)}
 
     def debug_buffer_ptrs(self):
         n = ctypes.c_int(0)

@@ -65,6 +65,10 @@ struct moe_handle {
   int* status_dev = nullptr;
 
   CUtensorMap tm_a1{}, tm_b1{}, tm_a2{}, tm_b2{};
+
+  // stage timing: events[0] before the first kernel, events[i+1] after stage i
+  bool timing = false;
+  cudaEvent_t events[MOE_NUM_STAGES + 1] = {};
 };
 
 namespace {
@@ -232,18 +236,34 @@ struct DeviceGuard {
   }
 };
 
+// Stage boundary i.  Inside a stream capture the record becomes an external
+// event node (re-recorded on every replay); outside it is a plain record.
+cudaError_t mark(moe_handle* h, int i, cudaStream_t s) {
+  if (!h->timing) return cudaSuccess;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cs);
+  if (e != cudaSuccess) return e;
+  if (cs == cudaStreamCaptureStatusActive) return cudaEventRecordWithFlags(h->events[i], s, cudaEventRecordExternal);
+  return cudaEventRecord(h->events[i], s);
+}
+
 moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const float* bias, void* out, int T,
                         cudaStream_t s) {
   const int H = h->H, E = h->E, K = h->K;
   if (T > 0) {
+    CK(h, mark(h, 0, s));
     CK(h, cudaMemsetAsync(h->counts, 0, sizeof(int32_t) * E, s));
     CK(h, launch_router_logits(x, gate_w, bias, h->logits, T, H, E, s));
+    CK(h, mark(h, 1, s));
     CK(h, launch_topk(h->logits, T, E, K, h->topk_ids, h->topk_w, h->counts, s));
+    CK(h, mark(h, 2, s));
     PermuteOut po{h->expert_offsets, h->src_of_row, h->row_of_src, h->pad_row_of_src,
                   h->src_of_padrow,  h->tiles,      h->num_tiles};
     CK(h, launch_permute(h->topk_ids, h->counts, T, K, E, po, s));
+    CK(h, mark(h, 3, s));
     CK(h, launch_act_quant(x, T, H, K, h->pad_row_of_src, h->a_codes, h->a_sf, h->gs_rows,
                            h->deterministic ? nullptr : h->out_acc, s));
+    CK(h, mark(h, 4, s));
     const int tb = tile_bound(T, K, E);
     GemmArgs g{};
     g.status = h->status_dev;
@@ -262,6 +282,7 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
     g.h_gs = h->h_gs;
     g.i_pad = h->Ipad;
     CK(h, launch_gemm_w13(h->tm_a1, h->tm_b1, g, h->I / 128, tb, s));
+    CK(h, mark(h, 5, s));
     // w2: A = requantized intermediate [Rpad, Ipad], B = w2 [E*H, Ipad]
     GemmArgs g2{};
     g2.status = h->status_dev;
@@ -281,8 +302,10 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
     g2.ybuf = h->ybuf;
     g2.hidden = H;
     CK(h, launch_gemm_w2(h->tm_a2, h->tm_b2, g2, H / TILE_N, tb, h->deterministic, s));
+    CK(h, mark(h, 6, s));
     if (h->deterministic) CK(h, launch_finalize_ordered(h->ybuf, h->topk_w, out, T, H, K, s));
     else CK(h, launch_finalize_atomic(h->out_acc, out, T, H, s));
+    CK(h, mark(h, 7, s));
   }
   h->last_T = T;
   return MOE_OK;
@@ -408,6 +431,8 @@ moe_status moe_destroy(moe_handle* h) {
   cudaDeviceSynchronize();
   for (void* p : h->allocs) cudaFree(p);
   if (h->status_host) cudaFreeHost(h->status_host);
+  for (cudaEvent_t ev : h->events)
+    if (ev) cudaEventDestroy(ev);
   cudaGetLastError();
   delete h;
   return MOE_OK;
@@ -513,6 +538,37 @@ moe_status moe_forward_host(moe_handle* h, const void* x_host, const void* gate_
   CK(h, cudaMemcpyAsync(out_host, h->stage_out, xb, cudaMemcpyDeviceToHost, s));
   CK(h, cudaStreamSynchronize(s));
   return moe_get_status(h);
+}
+
+moe_status moe_set_stage_timing(moe_handle* h, int enable) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  DeviceGuard dg(h->cfg.device);
+  if (enable && !h->events[0]) {
+    for (cudaEvent_t& ev : h->events) CK(h, cudaEventCreate(&ev));
+  }
+  h->timing = enable != 0;
+  return MOE_OK;
+}
+
+moe_status moe_get_stage_times(const moe_handle* h, float* ms, int* n) {
+  if (!h || !n || (*n > 0 && !ms)) return MOE_ERR_INVALID_ARG;
+  if (!h->events[0]) return MOE_ERR_NOT_LOADED;
+  DeviceGuard dg(h->cfg.device);
+  const int m = std::min(*n, MOE_NUM_STAGES);
+  for (int i = 0; i < m; ++i) {
+    if (cudaEventElapsedTime(&ms[i], h->events[i], h->events[i + 1]) != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+  }
+  *n = m;
+  return MOE_OK;
+}
+
+const char* moe_stage_name(int i) {
+  static const char* names[MOE_NUM_STAGES] = {"router", "topk", "permute", "quantize", "gemm_w13", "gemm_w2",
+                                              "finalize"};
+  return (i >= 0 && i < MOE_NUM_STAGES) ? names[i] : nullptr;
 }
 
 size_t moe_get_workspace_bytes(const moe_handle* h) { return h ? h->bytes : 0; }
