@@ -38,7 +38,7 @@ KERNELS_PER_FORWARD = 7
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--config", default="c1_decode")
@@ -111,14 +111,77 @@ def run_oracle(args, steps, warmup):
 # --------------------------------------------------------------------------
 
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock and clock-event reasons sampled while the timed loop runs.
+
+    Reads NVML directly (libnvidia-ml through ctypes, read-only queries) every
+    ~2 ms so that even a short timed region gets samples; falls back to
+    nvidia-smi when NVML cannot be loaded.
+    """
+
+    NVML_CLOCK_SM = 1
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid=None, index=0, interval=0.002):
+        import ctypes
+
+        self.samples, self.reason_bits, self.max_mhz = [], 0, None
+        self.stop_flag = threading.Event()
+        self.lib = None
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            ok = uuid and lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) == 0
+            if not ok and lib.nvmlDeviceGetHandleByIndex_v2(int(index), ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle")
+            self.lib, self.h = lib, h
+            mx = ctypes.c_uint(0)
+            if lib.nvmlDeviceGetMaxClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self.reason_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.thread = threading.Thread(target=self._loop, args=(interval,), daemon=True)
+            self.thread.start()
+        except (OSError, AttributeError):
+            self.lib = None
+            self.smi = _SmiSampler(uuid)
+
+    def _loop(self, interval):
+        import ctypes
+
+        clk = ctypes.c_uint(0)
+        rs = ctypes.c_ulonglong(0)
+        while not self.stop_flag.is_set():
+            if self.lib.nvmlDeviceGetClockInfo(self.h, self.NVML_CLOCK_SM, ctypes.byref(clk)) == 0:
+                self.samples.append(float(clk.value))
+            if self.reason_fn(self.h, ctypes.byref(rs)) == 0:
+                self.reason_bits |= int(rs.value)
+            time.sleep(interval)
+
+    def stop(self):
+        if self.lib is None:
+            return self.smi.stop()
+        self.stop_flag.set()
+        self.thread.join(timeout=5)
+        self.lib.nvmlShutdown()
+        if not self.samples:
+            return None
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(n for b, n in self.REASONS.items() if self.reason_bits & b),
+                "samples": len(self.samples), "source": "nvml"}
+
+
+class _SmiSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, uuid=None):
         self.rows = []
         self.proc = None
-        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
         if uuid:
             cmd += ["-i", uuid]
         try:
@@ -131,7 +194,7 @@ class ClockSampler:
     def _read(self):
         for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 8:
+            if len(parts) >= 6:
                 self.rows.append(parts)
 
     def stop(self):
@@ -149,11 +212,11 @@ class ClockSampler:
         reasons = set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         for r in self.rows:
-            for name, v in zip(names, r[4:8]):
+            for name, v in zip(names, r[2:6]):
                 if v.strip().lower() == "active":
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(self.rows)}
+                "reasons": sorted(reasons), "samples": len(self.rows), "source": "nvidia-smi"}
 
 
 # --------------------------------------------------------------------------
@@ -236,17 +299,24 @@ def run_ours(args, rank, world, local_rank):
     gate_w = wl.gate_w.to(dev)
     bias = None if wl.bias is None else wl.bias.to(dev)
     out = torch.empty_like(x)
-    layer.set_stage_timing(True)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
-    # capture one forward into a CUDA graph (the decode path's serving mode)
+    # Two CUDA graphs of one forward (the decode path's serving mode): the
+    # headline graph has no instrumentation; the second records an event at
+    # every kernel boundary for the per-stage breakdown and the roofline of the
+    # dominant kernel (the events serialise the kernels they separate).
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
-        layer.forward(x, gate_w, out=out, bias=bias)          # load lazy state, warm caches
+        layer.forward(x, gate_w, out=out, bias=bias)          # warm caches and lazy state
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         layer.forward(x, gate_w, out=out, bias=bias)
+    layer.set_stage_timing(True)
+    graph_staged = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_staged, stream=stream):
+        layer.forward(x, gate_w, out=out, bias=bias)
+    layer.set_stage_timing(False)
     torch.cuda.synchronize()
 
     start = torch.cuda.Event(enable_timing=True)
@@ -254,6 +324,8 @@ def run_ours(args, rank, world, local_rank):
     for _ in range(args.warmup):
         flush.fill_(1)
         graph.replay()
+        flush.fill_(2)
+        graph_staged.replay()
     torch.cuda.synchronize()
 
     uuid = None
@@ -265,8 +337,8 @@ def run_ours(args, rank, world, local_rank):
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
-    clocks = ClockSampler(uuid)
-    step_ms, stages = [], {k: [] for k in STAGES}
+    clocks = ClockSampler(uuid, index=local_rank)
+    step_ms = []
     with torch.cuda.stream(stream):
         for i in range(args.steps):
             flush.fill_(i & 0xFF)
@@ -275,13 +347,22 @@ def run_ours(args, rank, world, local_rank):
             end.record(stream)
             end.synchronize()
             step_ms.append(start.elapsed_time(end))
-            for k, v in layer.stage_times().items():
-                stages[k].append(v)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
     total_ms = sum(step_ms)
+
+    # per-stage breakdown (same inputs, instrumented graph)
+    stages = {k: [] for k in STAGES}
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            graph_staged.replay()
+            stream.synchronize()
+            for k, v in layer.stage_times().items():
+                stages[k].append(v)
+    torch.cuda.synchronize()
 
     routing = layer.debug_routing()
     counts = torch.diff(routing["expert_offsets"]).cpu()
@@ -347,6 +428,7 @@ def run_ours(args, rank, world, local_rank):
         "layer_roofline": {"bound": "hbm", "alg_bytes": layer_bytes, "achieved_gbs": layer_gbs,
                            "frac": layer_gbs / peak, "touched_experts": touched},
         "stages_ms": mean_stage,
+        "stages_note": "per-kernel times from an instrumented replay whose boundary events serialise the kernels",
         "e2e": {"value": T * world / (e2e_total / args.steps), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "path": "moe_forward_host (pinned host buffers, eager launches)"},

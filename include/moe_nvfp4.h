@@ -236,7 +236,7 @@ MOE_API moe_status moe_debug_convert(const float* in, uint8_t* e2m1, uint8_t* e4
 /* Block-scaled FP4 GEMM through the same tcgen05 main loop as the expert
  * GEMMs: d[m][n] = sum_k dec(a)*dec(sfa)*dec(b)*dec(sfb) in FP32, for
  * a_codes [M, K/2], a_sf [M, K/16], b_codes [N, K/2], b_sf [N, K/16]
- * (canonical layouts), d f32 [M, N].  M % 128 == 0, N % 256 == 0,
+ * (canonical layouts), d f32 [M, N].  M % 128 == 0, N % 128 == 0,
  * K % 256 == 0.  Allocates and frees temporary buffers and synchronises the
  * stream; for tests only. */
 MOE_API moe_status moe_debug_block_scaled_gemm(const uint8_t* a_codes, const uint8_t* a_sf,

@@ -9,8 +9,10 @@
 namespace moe {
 
 // ---- routing (kernels_route.cu) ----
+cudaError_t router_setup(int H, int E);  // shared-memory attribute of the router kernel
+// Also clears counts[E] for the top-k kernel.
 cudaError_t launch_router_logits(const void* x, const void* gate_w, const float* bias, float* logits, int T,
-                                 int H, int E, cudaStream_t s);
+                                 int H, int E, int32_t* counts, cudaStream_t s);
 cudaError_t launch_topk(const float* logits, int T, int E, int K, int32_t* topk_ids, float* topk_w,
                         int32_t* counts, cudaStream_t s);
 struct PermuteOut {
@@ -29,8 +31,8 @@ cudaError_t launch_permute(const int32_t* topk_ids, const int32_t* counts, int T
 cudaError_t launch_act_quant(const void* x, int T, int H, int K, const int32_t* pad_row_of_src,
                              uint8_t* a_codes, uint8_t* a_sf, float* gs_rows, float* out_acc, cudaStream_t s);
 cudaError_t launch_weight_amax(const void* w, int E, int N, int Kd, uint32_t* amax_bits, cudaStream_t s);
-// interleave: 0 = rows in caller order; 1 = w13 gate/up chunks of 128 rows
-// interleaved so that chunk f of the internal layout is [gate f, up f].
+// interleave: 0 = rows in caller order; 1 = w13 gate/up rows interleaved in
+// chunks of 64 so that internal chunk f (128 rows) is [gate f, up f].
 cudaError_t launch_weight_quant(const void* w, int E, int N, int Kd, int Kpad, int interleave,
                                 const uint32_t* amax_bits, uint8_t* codes, uint8_t* sf, float* gs,
                                 cudaStream_t s);
@@ -71,16 +73,23 @@ struct GemmArgs {
   // plain epilogue (tests)
   float* d;
   int ldd;
+  int n_tiles;                // 128-column tiles per row tile (w2 / plain)
+  int m_tiles;                // row tiles (plain)
   int* status;                // device status word
 };
 
 int gemm_smem_bytes();
-cudaError_t gemm_setup_attributes();
+cudaError_t gemm_setup_attributes(int w13_chunks);
+// Thread-block clusters of the w13 kernel (w13_chunks CTAs each) that fit on
+// the device at once; 0 if none.
+int gemm_w13_max_clusters(int w13_chunks);
+// Persistent launches: the w13 kernel runs n_clusters clusters of n_chunks
+// CTAs; the w2 / plain kernels run n_ctas CTAs.  Each walks a static tile list.
 cudaError_t launch_gemm_w13(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int n_chunks,
-                            int tile_bound, cudaStream_t s);
-cudaError_t launch_gemm_w2(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int n_tiles,
-                           int tile_bound, bool ordered, cudaStream_t s);
-cudaError_t launch_gemm_plain(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int n_tiles,
-                              int m_tiles, cudaStream_t s);
+                            int n_clusters, cudaStream_t s);
+cudaError_t launch_gemm_w2(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int n_ctas,
+                           bool ordered, cudaStream_t s);
+cudaError_t launch_gemm_plain(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int n_ctas,
+                              cudaStream_t s);
 
 }  // namespace moe

@@ -2,33 +2,44 @@
 // on the sm_103a tensor cores (tcgen05.mma kind::mxf4nvf4, E2M1 operands with
 // UE4M3 scales per 16 elements, FP32 accumulators in tensor memory).
 //
-// One CTA computes one 128-row x 256-column tile of one expert:
-//   warp 0      TMA producer: A rows (only the tile's valid rows), B rows,
-//               and both block-scale tiles into a 4-stage shared-memory ring;
+// Persistent kernels.  A work unit is one 128-row x 128-column MMA tile of
+// one expert; each CTA (w2, plain) or cluster (w13) walks a static list.
+//   warp 0      TMA producer: A rows (only a unit's valid rows), B rows and
+//               both block-scale tiles into a STAGES-deep shared-memory ring,
+//               running ahead across unit boundaries;
 //   warp 1      tensor-memory allocation and the single MMA-issuing thread:
 //               block scales shared -> tensor memory (tcgen05.cp), then four
-//               K=64 MMAs per 256-element stage;
-//   warps 2-5   epilogue: one accumulator row (tensor-memory lane) per thread.
+//               K=64 MMAs per 256-element stage, into one of two accumulator
+//               buffers (tensor-memory columns [0,128) and [128,256));
+//   warps 2-5   epilogue, one accumulator row (tensor-memory lane) per thread.
+// With two accumulator buffers the epilogue drains unit u while the tensor
+// cores compute unit u+1, so weight streaming never waits for an epilogue.
 //
 // Epilogues:
-//   w13  the 256 columns are 128 gate and the matching 128 up features
-//        (the weights are stored interleaved in chunks of 128), so each
-//        thread forms SwiGLU for its row locally.  The row's absolute maximum
-//        over all I features is combined across the I/128 CTAs of a thread
-//        block cluster through distributed shared memory, and each CTA then
-//        requantizes its 128 features with the row's global scale - the
-//        per-row NVFP4 input of the w2 GEMM, written without a round trip of
-//        the FP32 intermediate through global memory.
-//   w2   y = acc / (gs_h * gs_w2), scaled by the token's top-k weight and
+//   w13  a unit's 128 columns are 64 gate features and the matching 64 up
+//        features (weights stored interleaved in chunks of 64), so a thread
+//        forms SwiGLU for its row locally.  A CTA owns 128 features (two
+//        units) of an m-tile and keeps their SwiGLU values in registers.
+//        The row's absolute maximum over all I features is combined across
+//        the I/128 CTAs of a thread-block cluster: every CTA stores its partial
+//        maximum, tagged with the m-tile's sequence number in the same 64-bit
+//        word, into every peer's shared memory, and each thread polls its own
+//        row's slots until all tags match - no barrier or fence on the path.
+//        Each CTA then requantizes its 128 features with the row's global
+//        scale: the per-row NVFP4 input of the w2 GEMM, written without a
+//        round trip of the FP32 intermediate through HBM.
+//   w2   y = acc / (gs_h * gs_w2) scaled by the token's top-k weight and
 //        added into the FP32 output accumulator (atomic mode), or stored per
 //        (token, slot) for the fixed-order finalize (ordered mode).
 //   plain FP32 store (tests).
 //
-// The activation (routing, expandInputRows, activation, finalize) fusion
-// around the expert GEMMs follows "SM10X Command-A-Plus decode 2.3x faster,
-// BCG capture memory -78%" (Motivation); the per-token scales follow "CuTe
-// DSL backend gets per-token NVFP4 online quantization and reload"
-// (Implementation item 2).
+// The fusion of routing, expandInputRows, activation and finalize around the
+// expert GEMMs follows "SM10X Command-A-Plus decode 2.3x faster, BCG capture
+// memory -78%" (Motivation); the per-token scales follow "CuTe DSL backend
+// gets per-token NVFP4 online quantization and reload" (Implementation
+// item 2).
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -36,39 +47,43 @@ namespace moe {
 
 namespace {
 
-constexpr int STAGES = 4;
 constexpr int A_STAGE = TILE_M * 128;        // 16 KB: 128 rows x 128 bytes
-constexpr int B_STAGE = TILE_N * 128;        // 32 KB: 256 rows x 128 bytes
+constexpr int B_STAGE = TILE_N * 128;        // 16 KB: 128 rows x 128 bytes
 constexpr int SFA_STAGE = 4 * SF_ATOM_BYTES; // 2 KB: 128 rows x 16 scales
-constexpr int SFB_STAGE = 8 * SF_ATOM_BYTES; // 4 KB: 256 rows x 16 scales
+constexpr int SFB_STAGE = 4 * SF_ATOM_BYTES; // 2 KB: 128 rows x 16 scales
+constexpr int STAGE_BYTES = A_STAGE + B_STAGE + SFA_STAGE + SFB_STAGE;
+constexpr int MAX_STAGES = 6;
 constexpr int A_BOX_ROWS = 32;
 constexpr int TMEM_COLS = 512;
-constexpr int TMEM_SF_BASE = 256;            // accumulator in columns [0, 256)
-constexpr int TMEM_SF_STAGE = 48;            // 16 columns SFA + 32 columns SFB per stage
+constexpr int TMEM_SF_BASE = 2 * TILE_N;     // two accumulator buffers in columns [0, 256)
+constexpr int TMEM_SF_STAGE = 32;            // 16 columns SFA + 16 columns SFB per stage
 constexpr uint32_t IDESC = idesc_fp4(TILE_M, TILE_N);
 constexpr int THREADS = 192;
+constexpr int EPI_WARPS = 4;
+constexpr int CTRL_BYTES = 256;
+constexpr int MAX_SMEM = 232448;
+static_assert(TMEM_SF_BASE + MAX_STAGES * TMEM_SF_STAGE <= TMEM_COLS, "tensor memory overflow");
 
 enum Mode { MODE_W13 = 0, MODE_W2_ATOMIC = 1, MODE_W2_ORDERED = 2, MODE_PLAIN = 3 };
 
-struct Smem {
-  uint8_t a[STAGES][A_STAGE];
-  uint8_t b[STAGES][B_STAGE];
-  uint8_t sfa[STAGES][SFA_STAGE];
-  uint8_t sfb[STAGES][SFB_STAGE];
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
-  uint64_t acc_full;
+struct Ctrl {
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
   uint32_t tmem_base;
   int abort_flag;
-  float part_amax[TILE_M];
 };
+static_assert(sizeof(Ctrl) <= CTRL_BYTES, "control block too large");
 
-constexpr int SMEM_BYTES = (int)sizeof(Smem) + 1024;  // + alignment slack
+__host__ __device__ constexpr int smem_bytes_for(int stages, int nch) {
+  return stages * STAGE_BYTES + CTRL_BYTES + 2 * nch * TILE_M * 8 + 1024;
+}
 
 __device__ __forceinline__ float swiglu(float g_acc, float u_acc, float alpha) {
   const float g = __fmul_rn(g_acc, alpha);
   const float u = __fmul_rn(u_acc, alpha);
-  return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+  return __fdividef(__fmul_rn(g, u), __fadd_rn(1.0f, __expf(-g)));
 }
 
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
@@ -76,233 +91,332 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
                : "memory");
 }
 
-template <int MODE>
+struct Unit {
+  int e, row0, valid, col;  // expert, first padded row, valid rows, 128-column block of B
+};
+
+template <int MODE, int STAGES>
 __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA,
                                                              const __grid_constant__ CUtensorMap tmB, GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = base;
+  uint8_t* sB = sA + STAGES * A_STAGE;
+  uint8_t* sSFA = sB + STAGES * B_STAGE;
+  uint8_t* sSFB = sSFA + STAGES * SFA_STAGE;
+  Ctrl& c = *reinterpret_cast<Ctrl*>(sSFB + STAGES * SFB_STAGE);
+  // [2][nch][128] words of (tile tag << 32 | partial row maximum bits)
+  uint64_t* part = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(&c) + CTRL_BYTES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mt = blockIdx.y;
-  int4 tile;
-  if (MODE == MODE_PLAIN) {
-    tile = make_int4(0, mt * TILE_M, TILE_M, 0);
+
+  // ---- static schedule, identical in every role ----
+  // w13: cluster blockIdx.y takes m-tiles blockIdx.y, +gridDim.y, ...; CTA
+  //      rank r of the cluster takes units (m-tile, B column blocks 2r, 2r+1).
+  // w2 / plain: CTA b takes units b, b + gridDim.x, ... of (m-tile, n-tile).
+  const int nch = (MODE == MODE_W13) ? (int)gridDim.x : 1;
+  const uint32_t rank = (MODE == MODE_W13) ? blockIdx.x : 0;
+  pdl_trigger();
+  int first, stride;
+  if constexpr (MODE == MODE_W13) {
+    first = 2 * blockIdx.y;
+    stride = 2 * gridDim.y;
   } else {
-    if (mt >= *p.num_tiles) return;  // same decision for every CTA of a cluster
-    tile = p.tiles[mt];
+    first = blockIdx.x;
+    stride = gridDim.x;
   }
-  const int e = tile.x, row0 = tile.y, valid = tile.z;
-  const int nb = blockIdx.x;  // w13: feature chunk (= cluster rank); w2 / plain: 256-column tile
-  const int brow0 = (MODE == MODE_PLAIN) ? nb * TILE_N : e * p.b_rows_per_expert + nb * TILE_N;
+  // w13 units come in pairs (2 per m-tile); `next` skips to the next pair.
+  auto next = [&](int u) -> int {
+    if constexpr (MODE == MODE_W13) return (u & 1) ? u - 1 + stride : u + 1;
+    else return u + stride;
+  };
+  auto unit_at = [&](int u) -> Unit {
+    Unit r;
+    if constexpr (MODE == MODE_W13) {
+      const int4 ti = p.tiles[u >> 1];
+      r.e = ti.x; r.row0 = ti.y; r.valid = ti.z; r.col = 2 * (int)rank + (u & 1);
+    } else if constexpr (MODE == MODE_PLAIN) {
+      r.e = 0; r.row0 = (u / p.n_tiles) * TILE_M; r.valid = TILE_M; r.col = u % p.n_tiles;
+    } else {
+      const int4 ti = p.tiles[u / p.n_tiles];
+      r.e = ti.x; r.row0 = ti.y; r.valid = ti.z; r.col = u % p.n_tiles;
+    }
+    return r;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], 1);
+      mbar_init(&c.full[s], 1);
+      mbar_init(&c.empty[s], 1);
     }
-    mbar_init(&sm.acc_full, 1);
-    sm.abort_flag = 0;
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&c.acc_full[b], 1);
+      mbar_init(&c.acc_empty[b], EPI_WARPS);
+    }
+    c.abort_flag = 0;
+    if (MODE == MODE_W13)
+      for (int i = 0; i < 2 * nch * TILE_M; ++i) part[i] = 0;  // tag 0 is never a live tile
     fence_mbarrier_init();
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(&sm.tmem_base, TMEM_COLS);
+    tmem_alloc(&c.tmem_base, TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (MODE == MODE_W13) cluster_sync_all();  // peers' exchange slots are cleared before any remote store
   tc_fence_after();
-  const uint32_t tmem = sm.tmem_base;
+  const uint32_t tmem = c.tmem_base;
   const int KS = p.k_stages;
+  // Everything above overlaps the previous kernel's tail; its outputs (the
+  // tile list, operands, scales) are read only from here on.
+  pdl_wait();
+  int nunits;
+  if constexpr (MODE == MODE_W13) nunits = 2 * (*p.num_tiles);
+  else nunits = (MODE == MODE_PLAIN ? p.m_tiles : *p.num_tiles) * p.n_tiles;
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer ----------------
-      const int a_boxes = (valid + A_BOX_ROWS - 1) / A_BOX_ROWS;
-      const uint32_t bytes = a_boxes * A_BOX_ROWS * 128 + B_STAGE + SFA_STAGE + SFB_STAGE;
-      const uint64_t pol = policy_evict_first();
+      const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_a = policy_evict_last();
-      const uint8_t* sfa_src = p.a_sf + ((size_t)(row0 >> 7) * p.kblocks) * SF_ATOM_BYTES;
-      const uint8_t* sfb_src0 = p.b_sf + ((size_t)(brow0 >> 7) * p.kblocks) * SF_ATOM_BYTES;
-      const uint8_t* sfb_src1 = sfb_src0 + (size_t)p.kblocks * SF_ATOM_BYTES;
-      int issued = 0;
-      for (int ks = 0; ks < KS; ++ks) {
-        const int s = ks % STAGES;
-        const uint32_t round = ks / STAGES;
-        if (!mbar_wait_bounded(&sm.empty[s], (round & 1) ^ 1, &sm.abort_flag)) {
-          sm.abort_flag = 1;
-          report_device_error(p.status, DEV_ERR_TIMEOUT);
-          break;
+      uint32_t g = 0;  // stages issued so far (ring position)
+      for (int u = first; u < nunits && !c.abort_flag; u = next(u)) {
+        const Unit un = unit_at(u);
+        const int brow0 = (MODE == MODE_PLAIN ? 0 : un.e * p.b_rows_per_expert) + un.col * TILE_N;
+        const int a_boxes = (un.valid + A_BOX_ROWS - 1) / A_BOX_ROWS;
+        const uint32_t bytes = a_boxes * A_BOX_ROWS * 128 + B_STAGE + SFA_STAGE + SFB_STAGE;
+        const uint8_t* sfa_src = p.a_sf + ((size_t)(un.row0 >> 7) * p.kblocks) * SF_ATOM_BYTES;
+        const uint8_t* sfb_src = p.b_sf + ((size_t)(brow0 >> 7) * p.kblocks) * SF_ATOM_BYTES;
+        for (int ks = 0; ks < KS; ++ks, ++g) {
+          const int s = g % STAGES;
+          if (!mbar_wait_bounded(&c.empty[s], ((g / STAGES) & 1) ^ 1, &c.abort_flag)) {
+            c.abort_flag = 1;
+            report_device_error(p.status, DEV_ERR_TIMEOUT);
+            break;
+          }
+          mbar_arrive_expect_tx(&c.full[s], bytes);
+          for (int i = 0; i < a_boxes; ++i)
+            tma_load_2d(sA + s * A_STAGE + i * A_BOX_ROWS * 128, &tmA, &c.full[s], ks * 128,
+                        un.row0 + i * A_BOX_ROWS, pol_a);
+          tma_load_2d(sB + s * B_STAGE, &tmB, &c.full[s], ks * 128, brow0, pol_w);
+          bulk_load(sSFA + s * SFA_STAGE, sfa_src + (size_t)ks * SFA_STAGE, SFA_STAGE, &c.full[s]);
+          bulk_load(sSFB + s * SFB_STAGE, sfb_src + (size_t)ks * SFB_STAGE, SFB_STAGE, &c.full[s]);
         }
-        issued = ks + 1;
-        mbar_arrive_expect_tx(&sm.full[s], bytes);
-        for (int i = 0; i < a_boxes; ++i)
-          tma_load_2d(&sm.a[s][i * A_BOX_ROWS * 128], &tmA, &sm.full[s], ks * 128, row0 + i * A_BOX_ROWS, pol_a);
-        tma_load_2d(&sm.b[s][0], &tmB, &sm.full[s], ks * 128, brow0, pol);
-        bulk_load(&sm.sfa[s][0], sfa_src + (size_t)ks * SFA_STAGE, SFA_STAGE, &sm.full[s]);
-        bulk_load(&sm.sfb[s][0], sfb_src0 + (size_t)ks * SFA_STAGE, SFA_STAGE, &sm.full[s]);
-        bulk_load(&sm.sfb[s][SFA_STAGE], sfb_src1 + (size_t)ks * SFA_STAGE, SFA_STAGE, &sm.full[s]);
       }
-      if (sm.abort_flag) {
+      if (c.abort_flag) {
         // Unwinding: let the copies already issued land before the CTA's
         // shared memory is released (bounded, no early exit).
-        for (int ks = issued - STAGES < 0 ? 0 : issued - STAGES; ks < issued; ++ks)
-          mbar_wait_bounded(&sm.full[ks % STAGES], (ks / STAGES) & 1, nullptr, 1000000000ull);
+        for (uint32_t k = g > STAGES ? g - STAGES : 0; k < g; ++k)
+          mbar_wait_bounded(&c.full[k % STAGES], (k / STAGES) & 1, nullptr, 1000000000ull);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      bool ok = true;
-      for (int ks = 0; ks < KS; ++ks) {
-        const int s = ks % STAGES;
-        const uint32_t round = ks / STAGES;
-        if (!mbar_wait_bounded(&sm.full[s], round & 1, &sm.abort_flag)) {
-          sm.abort_flag = 1;
+      uint32_t g = 0;
+      int n = 0;  // units processed by this CTA
+      for (int u = first; u < nunits; u = next(u), ++n) {
+        if (c.abort_flag) break;
+        const int buf = n & 1;
+        if (!mbar_wait_bounded(&c.acc_empty[buf], ((n >> 1) & 1) ^ 1, &c.abort_flag)) {
+          c.abort_flag = 1;
           report_device_error(p.status, DEV_ERR_TIMEOUT);
-          ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t sfa_t = tmem + TMEM_SF_BASE + s * TMEM_SF_STAGE;
-        const uint32_t sfb_t = sfa_t + 16;
+        const uint32_t d_tmem = tmem + buf * TILE_N;
+        for (int ks = 0; ks < KS; ++ks, ++g) {
+          const int s = g % STAGES;
+          if (!mbar_wait_bounded(&c.full[s], (g / STAGES) & 1, &c.abort_flag)) {
+            c.abort_flag = 1;
+            report_device_error(p.status, DEV_ERR_TIMEOUT);
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sfa_t = tmem + TMEM_SF_BASE + s * TMEM_SF_STAGE;
+          const uint32_t sfb_t = sfa_t + 16;
 #pragma unroll
-        for (int kb = 0; kb < 4; ++kb) {
-          tc_copy_sf(sfa_t + kb * 4, smem_desc_sf(smem_u32(&sm.sfa[s][kb * SF_ATOM_BYTES])));
-          tc_copy_sf(sfb_t + kb * 8, smem_desc_sf(smem_u32(&sm.sfb[s][kb * SF_ATOM_BYTES])));
-          tc_copy_sf(sfb_t + kb * 8 + 4, smem_desc_sf(smem_u32(&sm.sfb[s][SFA_STAGE + kb * SF_ATOM_BYTES])));
-        }
-        const uint32_t a_base = smem_u32(&sm.a[s][0]);
-        const uint32_t b_base = smem_u32(&sm.b[s][0]);
+          for (int kb = 0; kb < 4; ++kb) {
+            tc_copy_sf(sfa_t + kb * 4, smem_desc_sf(smem_u32(sSFA + s * SFA_STAGE + kb * SF_ATOM_BYTES)));
+            tc_copy_sf(sfb_t + kb * 4, smem_desc_sf(smem_u32(sSFB + s * SFB_STAGE + kb * SF_ATOM_BYTES)));
+          }
+          const uint32_t a_base = smem_u32(sA + s * A_STAGE);
+          const uint32_t b_base = smem_u32(sB + s * B_STAGE);
 #pragma unroll
-        for (int kb = 0; kb < 4; ++kb) {
-          tc_mma_fp4(tmem, smem_desc_sw128(a_base + kb * 32), smem_desc_sw128(b_base + kb * 32), IDESC,
-                     sfa_t + kb * 4, sfb_t + kb * 8, (ks | kb) != 0);
+          for (int kb = 0; kb < 4; ++kb)
+            tc_mma_fp4(d_tmem, smem_desc_sw128(a_base + kb * 32), smem_desc_sw128(b_base + kb * 32), IDESC,
+                       sfa_t + kb * 4, sfb_t + kb * 4, (ks | kb) != 0);
+          tc_commit(&c.empty[s]);
         }
-        tc_commit(&sm.empty[s]);
+        // Always signal, even after an abort: the epilogue waits for the
+        // MMAs already issued before it lets tensor memory go.
+        tc_commit(&c.acc_full[buf]);
       }
-      // Signal the epilogue even after an abort so that it does not wait for
-      // the full timeout; it checks the abort flag.
-      tc_commit(&sm.acc_full);
-      (void)ok;
     }
     __syncwarp();
-  }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int quarter = warp & 3;          // tensor-memory lanes [32q, 32q+32)
+    const int m = quarter * 32 + lane;     // accumulator row of this thread
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    int n = 0;  // units drained by this CTA
 
-  // ---------------- epilogue (warps 2..5) ----------------
-  const bool epi = warp >= 2;
-  const int quarter = warp & 3;                 // tensor-memory lanes [32q, 32q+32)
-  const int m = quarter * 32 + lane;            // accumulator row of this thread
-  const bool row_ok = m < valid;
-  const int prow = row0 + m;
-  const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
-  bool acc_ready = false;
-  if (epi) {
-    // No early exit here: the MMA thread always commits acc_full, and tensor
-    // memory must not be released before the MMAs already issued are done.
-    acc_ready = mbar_wait_bounded(&sm.acc_full, 0, nullptr);
-    if (!acc_ready) report_device_error(p.status, DEV_ERR_TIMEOUT);
-    acc_ready = acc_ready && !sm.abort_flag;
-    tc_fence_after();
-  }
-
-  if constexpr (MODE == MODE_W13) {
-    const float alpha = row_ok ? __fdiv_rn(1.0f, __fmul_rn(p.gs_rows[prow], p.gs_w[e])) : 0.0f;
-    if (epi) {
-      float amax = 0.0f;
-      if (acc_ready) {
-#pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          float g[16], u[16];
-          tmem_ld16(trow + 16 * c, g);
-          tmem_ld16(trow + 128 + 16 * c, u);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(swiglu(g[i], u[i], alpha)));
-        }
+    // Wait for the accumulator of unit n; false if the device state is bad.
+    auto wait_acc = [&](int buf, int nn) -> bool {
+      bool ok = mbar_wait_bounded(&c.acc_full[buf], (nn >> 1) & 1, nullptr);
+      if (!ok) {
+        c.abort_flag = 1;
+        report_device_error(p.status, DEV_ERR_TIMEOUT);
       }
-      sm.part_amax[m] = row_ok ? amax : 0.0f;
-    }
-    __syncwarp();
-    cluster_sync_all();  // every CTA's partial row maxima are visible
-    if (epi) {
-      const uint32_t nranks = gridDim.x;
-      float amax_row = 0.0f;
-      for (uint32_t r = 0; r < nranks; ++r) amax_row = fmaxf(amax_row, ld_shared_cluster_f32(&sm.part_amax[m], r));
-      const float gs_h = nvfp4_global_scale(amax_row);
-      if (acc_ready) {
-        const int k16_row = p.i_pad / SF_VEC;
-#pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          float g[16], u[16], h[16];
-          tmem_ld16(trow + 16 * c, g);
-          tmem_ld16(trow + 128 + 16 * c, u);
-          tmem_ld_wait();
+      tc_fence_after();
+      return ok && !c.abort_flag;
+    };
+    auto release_acc = [&](int buf) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.acc_empty[buf]);
+    };
+
+    if constexpr (MODE == MODE_W13) {
+      int i = 0;  // m-tiles processed
+      for (int u = first; u < nunits; u = next(next(u)), ++i) {
+        const Unit un = unit_at(u);
+        const bool warp_rows = quarter * 32 < un.valid;  // warp-uniform
+        const bool row_ok = m < un.valid;
+        const int prow = un.row0 + m;
+        const float alpha = row_ok ? __fdiv_rn(1.0f, __fmul_rn(p.gs_rows[prow], p.gs_w[un.e])) : 0.0f;
+        float h[128];
+        float amax = 0.0f;
+        bool ready = true;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) h[i] = swiglu(g[i], u[i], alpha);
-          uint2 packed;
-          const uint32_t sf = nvfp4_quant_block16(h, gs_h, packed);
-          const int k = nb * 128 + 16 * c;  // feature index of this block
-          if (row_ok) {
+        for (int j = 0; j < 2; ++j, ++n) {
+          const int buf = n & 1;
+          ready = wait_acc(buf, n) && ready;
+          if (ready && warp_rows) {
+            const uint32_t t = lane_base + buf * TILE_N;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              float gv[32], uv[32];
+              tmem_ld32(t + 32 * half, gv);        // gate features 32*half ..
+              tmem_ld32(t + 64 + 32 * half, uv);   // matching up features
+              tmem_ld_wait();
+#pragma unroll
+              for (int q = 0; q < 32; ++q) {
+                const float hv = swiglu(gv[q], uv[q], alpha);
+                h[64 * j + 32 * half + q] = hv;
+                amax = fmaxf(amax, fabsf(hv));
+              }
+            }
+          }
+          release_acc(buf);  // the tensor cores may refill this buffer now
+        }
+        if (!row_ok) amax = 0.0f;
+        // Exchange the row maxima across the cluster.  Slot buffer i & 1;
+        // a peer can be at most one m-tile ahead (it needs this CTA's value
+        // of its next m-tile first), so two buffers never overwrite a value
+        // that has not been read.
+        const int b = i & 1;
+        const uint64_t tag = (uint64_t)(i + 1) << 32;
+        const uint64_t* slots = part + (size_t)b * nch * TILE_M + m;
+        for (int r = 0; r < nch; ++r)
+          st_shared_cluster_u64(slots + (size_t)rank * TILE_M, (uint32_t)r, tag | __float_as_uint(amax));
+        float amax_row = 0.0f;
+        for (int r = 0; r < nch; ++r) {
+          const uint64_t* slot = slots + (size_t)r * TILE_M;
+          uint64_t v = ld_shared_relaxed_u64(slot);
+          if ((v >> 32) != (tag >> 32)) {
+            const uint64_t t0 = global_timer_ns();
+            for (uint32_t it = 1; (v >> 32) != (tag >> 32); ++it) {
+              v = ld_shared_relaxed_u64(slot);
+              if ((it & 255u) == 0 && global_timer_ns() - t0 > 2000000000ull) {
+                c.abort_flag = 1;
+                report_device_error(p.status, DEV_ERR_TIMEOUT);
+                ready = false;
+                break;
+              }
+            }
+          }
+          amax_row = fmaxf(amax_row, __uint_as_float((uint32_t)v));
+        }
+        const float gs_h = nvfp4_global_scale(amax_row);
+        if (ready && row_ok) {
+          const int k16_row = p.i_pad / SF_VEC;
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) {
+            float v[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) v[q] = h[16 * cc + q];
+            uint2 packed;
+            const uint32_t sf = nvfp4_quant_block16(v, gs_h, packed);
+            const int k = (int)rank * 128 + 16 * cc;  // feature index of this block
             *reinterpret_cast<uint2*>(p.h_codes + (size_t)prow * (p.i_pad / 2) + k / 2) = packed;
             p.h_sf[sf_atom_offset(prow, k / SF_VEC, k16_row)] = (uint8_t)sf;
           }
+          if (rank == 0) p.h_gs[prow] = gs_h;
         }
       }
-      if (row_ok && nb == 0) p.h_gs[prow] = gs_h;
-    }
-    __syncwarp();
-    cluster_sync_all();  // peers are done reading this CTA's shared memory
-  } else if constexpr (MODE == MODE_W2_ATOMIC || MODE == MODE_W2_ORDERED) {
-    if (epi && acc_ready) {
-      int src = 0;
-      float alpha = 0.0f, wj = 0.0f;
-      if (row_ok) {
-        src = p.src_of_padrow[prow];
-        alpha = __fdiv_rn(1.0f, __fmul_rn(p.gs_rows[prow], p.gs_w[e]));
-        wj = p.topk_w[src];
-      }
-      const int t = src / p.top_k;
-      const int n0 = nb * TILE_N;
-#pragma unroll 1
-      for (int c = 0; c < 16; ++c) {
-        float a[16];
-        tmem_ld16(trow + 16 * c, a);
-        tmem_ld_wait();
-        if (row_ok) {
-          if constexpr (MODE == MODE_W2_ATOMIC) {
-            float* dst = p.out_acc + (size_t)t * p.hidden + n0 + 16 * c;
-#pragma unroll
-            for (int i = 0; i < 16; i += 4)
-              red_add_v4(dst + i, __fmul_rn(wj, __fmul_rn(a[i], alpha)), __fmul_rn(wj, __fmul_rn(a[i + 1], alpha)),
-                         __fmul_rn(wj, __fmul_rn(a[i + 2], alpha)), __fmul_rn(wj, __fmul_rn(a[i + 3], alpha)));
-          } else {
-            float4* dst = reinterpret_cast<float4*>(p.ybuf + (size_t)src * p.hidden + n0 + 16 * c);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_float4(__fmul_rn(a[4 * i], alpha), __fmul_rn(a[4 * i + 1], alpha),
-                                   __fmul_rn(a[4 * i + 2], alpha), __fmul_rn(a[4 * i + 3], alpha));
+    } else {
+      for (int u = first; u < nunits; u = next(u), ++n) {
+        const Unit un = unit_at(u);
+        const bool warp_rows = quarter * 32 < un.valid;
+        const bool row_ok = m < un.valid;
+        const int prow = un.row0 + m;
+        const int buf = n & 1;
+        const bool ready = wait_acc(buf, n);
+        if (ready && warp_rows) {
+          int src = 0;
+          float alpha = 0.0f, wj = 0.0f;
+          if (MODE != MODE_PLAIN && row_ok) {
+            src = p.src_of_padrow[prow];
+            alpha = __fdiv_rn(1.0f, __fmul_rn(p.gs_rows[prow], p.gs_w[un.e]));
+            wj = p.topk_w[src];
           }
-        }
-      }
-    }
-  } else {  // MODE_PLAIN
-    if (epi && acc_ready) {
-#pragma unroll 1
-      for (int c = 0; c < 16; ++c) {
-        float a[16];
-        tmem_ld16(trow + 16 * c, a);
-        tmem_ld_wait();
-        float4* dst = reinterpret_cast<float4*>(p.d + (size_t)prow * p.ldd + nb * TILE_N + 16 * c);
+          const int tok = src / (p.top_k > 0 ? p.top_k : 1);
+          const int n0 = un.col * TILE_N;
+          const uint32_t t = lane_base + buf * TILE_N;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) dst[i] = make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
+          for (int half = 0; half < 2; ++half) {
+            float a[64];
+            tmem_ld32(t + 64 * half, a);
+            tmem_ld32(t + 64 * half + 32, a + 32);
+            tmem_ld_wait();
+            if (half == 1) release_acc(buf);  // everything is in registers now
+            if (row_ok) {
+              const int col = n0 + 64 * half;
+              if constexpr (MODE == MODE_W2_ATOMIC) {
+                float* dst = p.out_acc + (size_t)tok * p.hidden + col;
+#pragma unroll
+                for (int q = 0; q < 64; q += 4)
+                  red_add_v4(dst + q, __fmul_rn(wj, __fmul_rn(a[q], alpha)),
+                             __fmul_rn(wj, __fmul_rn(a[q + 1], alpha)), __fmul_rn(wj, __fmul_rn(a[q + 2], alpha)),
+                             __fmul_rn(wj, __fmul_rn(a[q + 3], alpha)));
+              } else if constexpr (MODE == MODE_W2_ORDERED) {
+                float4* dst = reinterpret_cast<float4*>(p.ybuf + (size_t)src * p.hidden + col);
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                  dst[q] = make_float4(__fmul_rn(a[4 * q], alpha), __fmul_rn(a[4 * q + 1], alpha),
+                                       __fmul_rn(a[4 * q + 2], alpha), __fmul_rn(a[4 * q + 3], alpha));
+              } else {
+                float4* dst = reinterpret_cast<float4*>(p.d + (size_t)prow * p.ldd + col);
+#pragma unroll
+                for (int q = 0; q < 16; ++q) dst[q] = make_float4(a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
+              }
+            }
+          }
+        } else {
+          release_acc(buf);
+        }
       }
     }
   }
 
   __syncwarp();
+  // No CTA of a cluster leaves while a peer may still write its shared memory.
+  if constexpr (MODE == MODE_W13) cluster_sync_all();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -311,63 +425,112 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
   }
 }
 
-template <int MODE>
-cudaError_t set_attrs() {
-  cudaError_t err = cudaFuncSetAttribute(gemm_fp4_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SMEM_BYTES);
+int stages_for(int nch) {
+  for (int s = MAX_STAGES; s >= 3; --s)
+    if (smem_bytes_for(s, nch) <= MAX_SMEM) return s;
+  return 0;
+}
+
+template <int MODE, int STAGES>
+cudaError_t set_attrs(int nch) {
+  cudaError_t err = cudaFuncSetAttribute(gemm_fp4_kernel<MODE, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         smem_bytes_for(STAGES, nch));
   if (err != cudaSuccess) return err;
-  if (MODE == MODE_W13) {
-    err = cudaFuncSetAttribute(gemm_fp4_kernel<MODE>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  }
+  if (MODE == MODE_W13)
+    err = cudaFuncSetAttribute(gemm_fp4_kernel<MODE, STAGES>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   return err;
 }
 
-template <int MODE>
-cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, dim3 grid, int cluster_x,
-                   cudaStream_t s) {
+template <int MODE, int STAGES>
+cudaLaunchConfig_t make_cfg(dim3 grid, int nch, cudaStream_t s, cudaLaunchAttribute* attr, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = smem_bytes_for(STAGES, MODE == MODE_W13 ? nch : 0);
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  if (cluster_x > 0) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cluster_x;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+  int n = 0;
+  if (MODE == MODE_W13) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = nch;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
   }
-  return cudaLaunchKernelEx(&cfg, gemm_fp4_kernel<MODE>, tmA, tmB, a);
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = n ? attr : nullptr;
+  cfg.numAttrs = n;
+  return cfg;
+}
+
+template <int MODE, int STAGES>
+cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, dim3 grid, int nch,
+                   cudaStream_t s) {
+  cudaLaunchAttribute attr[2];
+  // The expert GEMMs always follow another kernel of the same forward.
+  cudaLaunchConfig_t cfg = make_cfg<MODE, STAGES>(grid, nch, s, attr, MODE != MODE_PLAIN);
+  return cudaLaunchKernelEx(&cfg, gemm_fp4_kernel<MODE, STAGES>, tmA, tmB, a);
+}
+
+// Dispatch on the ring depth that fits the w13 kernel's shared memory.
+template <typename F>
+cudaError_t with_w13_stages(int nch, F&& f) {
+  switch (stages_for(nch)) {
+    case 6: return f(std::integral_constant<int, 6>{});
+    case 5: return f(std::integral_constant<int, 5>{});
+    case 4: return f(std::integral_constant<int, 4>{});
+    case 3: return f(std::integral_constant<int, 3>{});
+    default: return cudaErrorInvalidConfiguration;
+  }
 }
 
 }  // namespace
 
-int gemm_smem_bytes() { return SMEM_BYTES; }
+int gemm_smem_bytes() { return smem_bytes_for(MAX_STAGES, 0); }
 
-cudaError_t gemm_setup_attributes() {
-  cudaError_t e;
-  if ((e = set_attrs<MODE_W13>()) != cudaSuccess) return e;
-  if ((e = set_attrs<MODE_W2_ATOMIC>()) != cudaSuccess) return e;
-  if ((e = set_attrs<MODE_W2_ORDERED>()) != cudaSuccess) return e;
-  return set_attrs<MODE_PLAIN>();
+cudaError_t gemm_setup_attributes(int nch) {
+  cudaError_t e = with_w13_stages(nch, [&](auto st) { return set_attrs<MODE_W13, decltype(st)::value>(nch); });
+  if (e != cudaSuccess) return e;
+  if ((e = set_attrs<MODE_W2_ATOMIC, MAX_STAGES>(0)) != cudaSuccess) return e;
+  if ((e = set_attrs<MODE_W2_ORDERED, MAX_STAGES>(0)) != cudaSuccess) return e;
+  return set_attrs<MODE_PLAIN, MAX_STAGES>(0);
+}
+
+int gemm_w13_max_clusters(int nch) {
+  int n = 0;
+  cudaError_t e = with_w13_stages(nch, [&](auto st) {
+    constexpr int S = decltype(st)::value;
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = make_cfg<MODE_W13, S>(dim3(nch, 1, 1), nch, 0, attr, false);
+    return cudaOccupancyMaxActiveClusters(&n, gemm_fp4_kernel<MODE_W13, S>, &cfg);
+  });
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 cudaError_t launch_gemm_w13(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int n_chunks,
-                            int tile_bound, cudaStream_t s) {
-  return launch<MODE_W13>(tmA, tmB, a, dim3(n_chunks, tile_bound, 1), n_chunks, s);
+                            int n_clusters, cudaStream_t s) {
+  const dim3 grid(n_chunks, n_clusters, 1);
+  return with_w13_stages(n_chunks, [&](auto st) {
+    return launch<MODE_W13, decltype(st)::value>(tmA, tmB, a, grid, n_chunks, s);
+  });
 }
 
-cudaError_t launch_gemm_w2(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int n_tiles,
-                           int tile_bound, bool ordered, cudaStream_t s) {
-  if (ordered) return launch<MODE_W2_ORDERED>(tmA, tmB, a, dim3(n_tiles, tile_bound, 1), 0, s);
-  return launch<MODE_W2_ATOMIC>(tmA, tmB, a, dim3(n_tiles, tile_bound, 1), 0, s);
+cudaError_t launch_gemm_w2(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int n_ctas,
+                           bool ordered, cudaStream_t s) {
+  if (ordered) return launch<MODE_W2_ORDERED, MAX_STAGES>(tmA, tmB, a, dim3(n_ctas, 1, 1), 0, s);
+  return launch<MODE_W2_ATOMIC, MAX_STAGES>(tmA, tmB, a, dim3(n_ctas, 1, 1), 0, s);
 }
 
-cudaError_t launch_gemm_plain(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int n_tiles,
-                              int m_tiles, cudaStream_t s) {
-  return launch<MODE_PLAIN>(tmA, tmB, a, dim3(n_tiles, m_tiles, 1), 0, s);
+cudaError_t launch_gemm_plain(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int n_ctas,
+                              cudaStream_t s) {
+  return launch<MODE_PLAIN, MAX_STAGES>(tmA, tmB, a, dim3(n_ctas, 1, 1), 0, s);
 }
 
 }  // namespace moe

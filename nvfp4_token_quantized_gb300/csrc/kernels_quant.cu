@@ -24,10 +24,16 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __r
                                                        float* __restrict__ gs_rows, float* __restrict__ out_acc) {
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (t >= T) return;
+  pdl_trigger();
+  if (t >= T) {
+    pdl_wait();
+    return;
+  }
   const int nblk = H / SF_VEC;
   const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
 
+  // x is the caller's input: reading it and forming the row maximum may
+  // overlap the permutation kernel; its outputs are read after pdl_wait().
   float amax = 0.0f;
   for (int b = lane; b < nblk; b += 32) {
     float v[16];
@@ -38,6 +44,7 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __r
   amax = warp_max(amax);
   const float gs = nvfp4_global_scale(amax);
 
+  pdl_wait();
   int prow[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) prow[j] = j < K ? pad_row_of_src[(size_t)t * K + j] : 0;
@@ -89,11 +96,12 @@ __global__ void __launch_bounds__(256) weight_amax_kernel(const __nv_bfloat16* _
 
 __device__ __forceinline__ int w13_internal_row(int n, int N) {
   // caller row n of [gate (I rows); up (I rows)] -> internal row where chunk f
-  // of 256 rows is [gate rows 128f..128f+127, up rows 128f..128f+127]
+  // of 128 rows is [gate rows 64f..64f+63, up rows 64f..64f+63], so one
+  // 128-column MMA tile holds matching gate and up features
   const int I = N / 2;
-  if (n < I) return (n >> 7) * 256 + (n & 127);
+  if (n < I) return (n >> 6) * 128 + (n & 63);
   const int u = n - I;
-  return (u >> 7) * 256 + 128 + (u & 127);
+  return (u >> 6) * 128 + 64 + (u & 63);
 }
 
 // One warp per (expert, row): block scales and codes of the row with the
@@ -168,6 +176,8 @@ __global__ void sf_to_atoms_kernel(const uint8_t* __restrict__ sf, int rows, int
 // out = bf16_rn(acc), 8 elements per thread.
 __global__ void __launch_bounds__(256) finalize_atomic_kernel(const float* __restrict__ acc,
                                                              __nv_bfloat16* __restrict__ out, size_t n8) {
+  pdl_trigger();
+  pdl_wait();
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
     const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
     const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
@@ -182,6 +192,8 @@ __global__ void __launch_bounds__(256) finalize_atomic_kernel(const float* __res
 __global__ void __launch_bounds__(256) finalize_ordered_kernel(const float* __restrict__ ybuf,
                                                               const float* __restrict__ topk_w,
                                                               __nv_bfloat16* __restrict__ out, int T, int H, int K) {
+  pdl_trigger();
+  pdl_wait();
   const size_t n4 = (size_t)T * H / 4;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
     const size_t flat = 4 * i;
@@ -210,9 +222,8 @@ int grid_for(size_t n, int per_block, int cap = 152 * 16) {
 
 cudaError_t launch_act_quant(const void* x, int T, int H, int K, const int32_t* pad_row_of_src, uint8_t* a_codes,
                              uint8_t* a_sf, float* gs_rows, float* out_acc, cudaStream_t s) {
-  act_quant_kernel<<<(T + 7) / 8, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(x), T, H, K, pad_row_of_src,
-                                               a_codes, a_sf, gs_rows, out_acc);
-  return cudaGetLastError();
+  return launch_k(act_quant_kernel, dim3((T + 7) / 8), dim3(256), 0, s, true,
+                  reinterpret_cast<const __nv_bfloat16*>(x), T, H, K, pad_row_of_src, a_codes, a_sf, gs_rows, out_acc);
 }
 
 cudaError_t launch_weight_amax(const void* w, int E, int N, int Kd, uint32_t* amax_bits, cudaStream_t s) {
@@ -252,16 +263,15 @@ cudaError_t launch_sf_to_atoms(const uint8_t* sf, int rows, int k16, uint8_t* at
 
 cudaError_t launch_finalize_atomic(const float* out_acc, void* out, int T, int H, cudaStream_t s) {
   const size_t n8 = (size_t)T * H / 8;
-  finalize_atomic_kernel<<<grid_for(n8, 256), 256, 0, s>>>(out_acc, reinterpret_cast<__nv_bfloat16*>(out), n8);
-  return cudaGetLastError();
+  return launch_k(finalize_atomic_kernel, dim3(grid_for(n8, 256)), dim3(256), 0, s, true, out_acc,
+                  reinterpret_cast<__nv_bfloat16*>(out), n8);
 }
 
 cudaError_t launch_finalize_ordered(const float* ybuf, const float* topk_w, void* out, int T, int H, int K,
                                     cudaStream_t s) {
   const size_t n4 = (size_t)T * H / 4;
-  finalize_ordered_kernel<<<grid_for(n4, 256), 256, 0, s>>>(ybuf, topk_w, reinterpret_cast<__nv_bfloat16*>(out), T,
-                                                            H, K);
-  return cudaGetLastError();
+  return launch_k(finalize_ordered_kernel, dim3(grid_for(n4, 256)), dim3(256), 0, s, true, ybuf, topk_w,
+                  reinterpret_cast<__nv_bfloat16*>(out), T, H, K);
 }
 
 }  // namespace moe

@@ -26,83 +26,121 @@ __device__ __forceinline__ int router_swz(int p) {
   else return 0;
 }
 
-// grid: (ceil(T / (8*TB)), E / EB); block: 256 threads = 8 warps.
+// d = a * b + c on two FP32 lanes, each rounded once (the same result as two
+// fmaf calls).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)),
+        "l"(*reinterpret_cast<uint64_t*>(&c)));
+  return *reinterpret_cast<float2*>(&d);
+}
+
+// grid: (ceil(T / (8*TB)), E / EB); block: 256 threads = 8 warps; dynamic
+// shared memory H * EB * 2 bytes holding the CTA's whole router-weight slice,
+// laid out [round j][k][partial p][EB] (row h = 256 j + 8 p + k).
 // Warp w handles tokens t0..t0+TB-1; lane p is partial p of every
-// (token, expert) pair of the CTA's expert block.
-template <int TB, int EB>
+// (token, expert) pair of the CTA's expert block: it accumulates chunks
+// c = p, p+32, ... in ascending order with one fused multiply-add per element,
+// then the 32 partials are combined by the pairwise tree.
+//
+// XALL: every round's activations are loaded into registers up front (one
+// memory round trip; H <= 2048), for small token counts where latency rules.
+// The kernel also clears the per-expert row counters the top-k kernel fills.
+template <int TB, int EB, bool XALL>
 __global__ void __launch_bounds__(256) router_logits_kernel(const __nv_bfloat16* __restrict__ x,
                                                            const __nv_bfloat16* __restrict__ wg,
                                                            const float* __restrict__ bias,
-                                                           float* __restrict__ logits, int T, int H, int E) {
+                                                           float* __restrict__ logits, int T, int H, int E,
+                                                           int32_t* __restrict__ counts) {
   constexpr int UNITS = EB / 8;                 // 16-byte units (8 bf16) per staged row
   constexpr int NV = TB * EB;                   // partial sums per lane
   static_assert(NV % 32 == 0, "TB*EB must be a multiple of 32");
-  __shared__ __align__(16) uint4 sw[2][8][32][UNITS];
+  extern __shared__ uint4 sw[];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e0 = blockIdx.y * EB;
   const int t0 = (blockIdx.x * ROUTER_WARPS + warp) * TB;
   const int rounds = H / 256;
+  pdl_trigger();
+  if (blockIdx.x == 0 && blockIdx.y == 0)
+    for (int e = threadIdx.x; e < E; e += blockDim.x) counts[e] = 0;
 
-  auto stage = [&](int j, int buf) {
-    // thread i stages weight row h = 256 j + i: EB bf16 from wg[h][e0..]
-    const int hr = threadIdx.x;
-    const int h = j * 256 + hr;
-    const int k = hr & 7, p = (hr >> 3) & 31;
+  for (int h = threadIdx.x; h < H; h += 256) {
+    const int j = h >> 8, hr = h & 255, k = hr & 7, p = (hr >> 3) & 31;
     const char* src = reinterpret_cast<const char*>(wg + (size_t)h * E + e0);
 #pragma unroll
     for (int u = 0; u < UNITS; ++u) {
-      const uint32_t dst = smem_u32(&sw[buf][k][p][u ^ router_swz<UNITS>(p)]);
+      const uint32_t dst = smem_u32(&sw[((j * 8 + k) * 32 + p) * UNITS + (u ^ router_swz<UNITS>(p))]);
       asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + 16 * u) : "memory");
     }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-  };
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
 
-  float acc[TB][EB];
-#pragma unroll
-  for (int t = 0; t < TB; ++t)
-#pragma unroll
-    for (int e = 0; e < EB; ++e) acc[t][e] = 0.0f;
-
-  stage(0, 0);
-  for (int j = 0; j < rounds; ++j) {
-    const int buf = j & 1;
-    if (j + 1 < rounds) {
-      stage(j + 1, buf ^ 1);
-      asm volatile("cp.async.wait_group 1;" ::: "memory");
-    } else {
-      asm volatile("cp.async.wait_group 0;" ::: "memory");
-    }
-    __syncthreads();
-    const int c = j * 32 + lane;                // this lane's chunk
-    uint4 xv[TB];
+  auto load_x = [&](int j, uint4 (&xv)[TB]) {
+    const int c = j * 32 + lane;                // this lane's chunk in round j
 #pragma unroll
     for (int t = 0; t < TB; ++t) {
       const int tok = t0 + t;
-      xv[t] = tok < T ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok * H + 8 * c))
-                      : make_uint4(0, 0, 0, 0);
+      xv[t] = tok < T ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok * H + 8 * c)) : make_uint4(0, 0, 0, 0);
     }
+  };
+  constexpr int XR = XALL ? 8 : 2;              // rounds of activations held in registers
+  uint4 xb[XR][TB];
+  if constexpr (XALL) {
+#pragma unroll
+    for (int j = 0; j < XR; ++j)
+      if (j < rounds) load_x(j, xb[j]);
+  } else {
+    load_x(0, xb[0]);
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  __syncthreads();
+
+  float2 acc[TB][EB / 2];
+#pragma unroll
+  for (int t = 0; t < TB; ++t)
+#pragma unroll
+    for (int e = 0; e < EB / 2; ++e) acc[t][e] = make_float2(0.0f, 0.0f);
+
+  auto round_fma = [&](int j, const uint4 (&xv)[TB]) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      float xf[TB];
+      float2 x2[TB];
 #pragma unroll
       for (int t = 0; t < TB; ++t) {
         const uint32_t w32 = (k < 2) ? xv[t].x : (k < 4) ? xv[t].y : (k < 6) ? xv[t].z : xv[t].w;
-        xf[t] = (k & 1) ? bf16_hi(w32) : bf16_lo(w32);
+        const float xf = (k & 1) ? bf16_hi(w32) : bf16_lo(w32);
+        x2[t] = make_float2(xf, xf);
       }
 #pragma unroll
       for (int u = 0; u < UNITS; ++u) {
-        const uint4 wv = sw[buf][k][lane][u ^ router_swz<UNITS>(lane)];
+        const uint4 wv = sw[((j * 8 + k) * 32 + lane) * UNITS + (u ^ router_swz<UNITS>(lane))];
         const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float w = (q & 1) ? bf16_hi(ww[q >> 1]) : bf16_lo(ww[q >> 1]);
+        for (int q = 0; q < 4; ++q) {
+          const float2 w2 = make_float2(bf16_lo(ww[q]), bf16_hi(ww[q]));  // experts 8u+2q, 8u+2q+1
 #pragma unroll
-          for (int t = 0; t < TB; ++t) acc[t][u * 8 + q] = __fmaf_rn(xf[t], w, acc[t][u * 8 + q]);
+          for (int t = 0; t < TB; ++t) acc[t][u * 4 + q] = fma2(x2[t], w2, acc[t][u * 4 + q]);
         }
       }
     }
-    __syncthreads();
+  };
+
+  if constexpr (XALL) {
+#pragma unroll
+    for (int j = 0; j < XR; ++j)
+      if (j < rounds) round_fma(j, xb[j]);
+  } else {
+    for (int j = 0; j < rounds; j += 2) {   // two register buffers, fixed indices
+      if (j + 1 < rounds) load_x(j + 1, xb[1]);
+      round_fma(j, xb[0]);
+      if (j + 1 < rounds) {
+        if (j + 2 < rounds) load_x(j + 2, xb[0]);
+        round_fma(j + 1, xb[1]);
+      }
+    }
   }
 
   // Pairwise tree over the 32 partials (lanes), partial p with p^o for
@@ -112,7 +150,10 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const __nv_bfloat16*
 #pragma unroll
   for (int t = 0; t < TB; ++t)
 #pragma unroll
-    for (int e = 0; e < EB; ++e) v[t * EB + e] = acc[t][e];
+    for (int e = 0; e < EB / 2; ++e) {
+      v[t * EB + 2 * e] = acc[t][e].x;
+      v[t * EB + 2 * e + 1] = acc[t][e].y;
+    }
 #pragma unroll
   for (int lvl = 0; lvl < 5; ++lvl) {
     const int o = 16 >> lvl;
@@ -147,6 +188,8 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
                                                   int32_t* __restrict__ counts) {
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  pdl_trigger();
+  pdl_wait();
   if (t >= T) return;
   constexpr int MAXE = 8;  // up to 256 experts
   float l[MAXE], cand[MAXE];
@@ -250,6 +293,8 @@ __global__ void __launch_bounds__(PERM_THREADS) permute_kernel(const int32_t* __
                                                               int E, PermuteOut o) {
   __shared__ int red[PERM_THREADS / 32];
   const int e = blockIdx.x;
+  pdl_trigger();
+  pdl_wait();
   int c_lt = 0, p_lt = 0, n_lt = 0;
   for (int i = threadIdx.x; i < e; i += blockDim.x) {
     const int c = counts[i];
@@ -306,35 +351,71 @@ __global__ void __launch_bounds__(PERM_THREADS) permute_kernel(const int32_t* __
   }
 }
 
-template <int TB, int EB>
+template <int TB, int EB, bool XALL>
 cudaError_t launch_router_t(const void* x, const void* gate_w, const float* bias, float* logits, int T, int H,
-                            int E, cudaStream_t s) {
+                            int E, int32_t* counts, cudaStream_t s) {
   dim3 grid((T + ROUTER_WARPS * TB - 1) / (ROUTER_WARPS * TB), E / EB);
-  router_logits_kernel<TB, EB><<<grid, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(x),
-                                                    reinterpret_cast<const __nv_bfloat16*>(gate_w), bias, logits,
-                                                    T, H, E);
-  return cudaGetLastError();
+  const size_t smem = (size_t)H * EB * 2;
+  // first kernel of a forward: ordinary stream order (it may depend on the caller's work)
+  return launch_k(router_logits_kernel<TB, EB, XALL>, grid, dim3(256), smem, s, false,
+                  reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<const __nv_bfloat16*>(gate_w), bias,
+                  logits, T, H, E, counts);
+}
+
+// Expert block: the widest of 32 / 16 / 8 experts that divides E and keeps
+// the staged slice (H * EB * 2 bytes) within 96 KB, so two CTAs fit an SM.
+int router_eb(int H, int E) {
+  for (int eb : {32, 16, 8})
+    if (E % eb == 0 && (size_t)H * eb * 2 <= 96 * 1024) return eb;
+  return 8;
+}
+
+// Small batches: two tokens per warp with all activations prefetched.
+bool router_small(int T, int H) { return T <= 512 && H <= 2048; }
+
+template <int TB, int EB, bool XALL>
+cudaError_t set_router_attr(int H) {
+  return cudaFuncSetAttribute(router_logits_kernel<TB, EB, XALL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              H * EB * 2);
 }
 
 }  // namespace
 
+cudaError_t router_setup(int H, int E) {
+  const int eb = router_eb(H, E);
+  cudaError_t e;
+  if (eb == 32) {
+    if ((e = set_router_attr<4, 32, false>(H)) != cudaSuccess) return e;
+    return set_router_attr<2, 32, true>(H);
+  }
+  if (eb == 16) {
+    if ((e = set_router_attr<4, 16, false>(H)) != cudaSuccess) return e;
+    return set_router_attr<2, 16, true>(H);
+  }
+  if ((e = set_router_attr<4, 8, false>(H)) != cudaSuccess) return e;
+  return set_router_attr<4, 8, true>(H);
+}
+
 cudaError_t launch_router_logits(const void* x, const void* gate_w, const float* bias, float* logits, int T,
-                                 int H, int E, cudaStream_t s) {
-  if (E % 32 == 0) return launch_router_t<4, 32>(x, gate_w, bias, logits, T, H, E, s);
-  if (E % 16 == 0) return launch_router_t<4, 16>(x, gate_w, bias, logits, T, H, E, s);
-  return launch_router_t<4, 8>(x, gate_w, bias, logits, T, H, E, s);
+                                 int H, int E, int32_t* counts, cudaStream_t s) {
+  const int eb = router_eb(H, E);
+  const bool small = router_small(T, H);
+  if (eb == 32) return small ? launch_router_t<2, 32, true>(x, gate_w, bias, logits, T, H, E, counts, s)
+                             : launch_router_t<4, 32, false>(x, gate_w, bias, logits, T, H, E, counts, s);
+  if (eb == 16) return small ? launch_router_t<2, 16, true>(x, gate_w, bias, logits, T, H, E, counts, s)
+                             : launch_router_t<4, 16, false>(x, gate_w, bias, logits, T, H, E, counts, s);
+  return small ? launch_router_t<4, 8, true>(x, gate_w, bias, logits, T, H, E, counts, s)
+               : launch_router_t<4, 8, false>(x, gate_w, bias, logits, T, H, E, counts, s);
 }
 
 cudaError_t launch_topk(const float* logits, int T, int E, int K, int32_t* topk_ids, float* topk_w,
                         int32_t* counts, cudaStream_t s) {
-  topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits, T, E, K, topk_ids, topk_w, counts);
-  return cudaGetLastError();
+  return launch_k(topk_kernel, dim3((T + 7) / 8), dim3(256), 0, s, true, logits, T, E, K, topk_ids, topk_w, counts);
 }
 
 cudaError_t launch_permute(const int32_t* topk_ids, const int32_t* counts, int T, int K, int E,
                            const PermuteOut& o, cudaStream_t s) {
-  permute_kernel<<<E, PERM_THREADS, 0, s>>>(topk_ids, counts, T, K, E, o);
-  return cudaGetLastError();
+  return launch_k(permute_kernel, dim3(E), dim3(PERM_THREADS), 0, s, true, topk_ids, counts, T, K, E, o);
 }
 
 }  // namespace moe

@@ -30,6 +30,8 @@ struct moe_handle {
   int Rmax = 0;         // Tmax * K
   int Rpad = 0;         // padded expert-grouped rows, worst case
   int tile_cap = 0;     // worst-case number of 128-row tiles
+  int num_sms = 0;      // persistent w2 grid
+  int w13_clusters = 0; // persistent w13 grid (clusters of I/128 CTAs)
   bool deterministic = false;
   bool loaded = false;
   moe_weight_desc w13_desc{}, w2_desc{};
@@ -252,8 +254,7 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
   const int H = h->H, E = h->E, K = h->K;
   if (T > 0) {
     CK(h, mark(h, 0, s));
-    CK(h, cudaMemsetAsync(h->counts, 0, sizeof(int32_t) * E, s));
-    CK(h, launch_router_logits(x, gate_w, bias, h->logits, T, H, E, s));
+    CK(h, launch_router_logits(x, gate_w, bias, h->logits, T, H, E, h->counts, s));
     CK(h, mark(h, 1, s));
     CK(h, launch_topk(h->logits, T, E, K, h->topk_ids, h->topk_w, h->counts, s));
     CK(h, mark(h, 2, s));
@@ -281,7 +282,7 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
     g.h_sf = h->h_sf;
     g.h_gs = h->h_gs;
     g.i_pad = h->Ipad;
-    CK(h, launch_gemm_w13(h->tm_a1, h->tm_b1, g, h->I / 128, tb, s));
+    CK(h, launch_gemm_w13(h->tm_a1, h->tm_b1, g, h->I / 128, std::min(h->w13_clusters, tb), s));
     CK(h, mark(h, 5, s));
     // w2: A = requantized intermediate [Rpad, Ipad], B = w2 [E*H, Ipad]
     GemmArgs g2{};
@@ -301,7 +302,8 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
     g2.out_acc = h->out_acc;
     g2.ybuf = h->ybuf;
     g2.hidden = H;
-    CK(h, launch_gemm_w2(h->tm_a2, h->tm_b2, g2, H / TILE_N, tb, h->deterministic, s));
+    g2.n_tiles = H / TILE_N;
+    CK(h, launch_gemm_w2(h->tm_a2, h->tm_b2, g2, std::min(h->num_sms, tb * g2.n_tiles), h->deterministic, s));
     CK(h, mark(h, 6, s));
     if (h->deterministic) CK(h, launch_finalize_ordered(h->ybuf, h->topk_w, out, T, H, K, s));
     else CK(h, launch_finalize_atomic(h->out_acc, out, T, H, s));
@@ -412,14 +414,22 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
   }
   moe_status st;
   if ((st = make_operand_map(h, &h->tm_a1, h->a_codes, H / 2, Rp, 32)) != MOE_OK) return fail(st);
-  if ((st = make_operand_map(h, &h->tm_b1, h->w13_codes, H / 2, (uint64_t)E * 2 * I, 256)) != MOE_OK)
+  if ((st = make_operand_map(h, &h->tm_b1, h->w13_codes, H / 2, (uint64_t)E * 2 * I, TILE_N)) != MOE_OK)
     return fail(st);
   if ((st = make_operand_map(h, &h->tm_a2, h->h_codes, h->Ipad / 2, Rp, 32)) != MOE_OK) return fail(st);
-  if ((st = make_operand_map(h, &h->tm_b2, h->w2_codes, h->Ipad / 2, (uint64_t)E * H, 256)) != MOE_OK)
+  if ((st = make_operand_map(h, &h->tm_b2, h->w2_codes, h->Ipad / 2, (uint64_t)E * H, TILE_N)) != MOE_OK)
     return fail(st);
   {
-    cudaError_t e = gemm_setup_attributes();
+    cudaError_t e = gemm_setup_attributes(I / 128);
     if (e != cudaSuccess) return fail(cuda_fail(h, e, "cudaFuncSetAttribute"));
+    e = router_setup(H, E);
+    if (e != cudaSuccess) return fail(cuda_fail(h, e, "cudaFuncSetAttribute(router)"));
+    h->num_sms = prop.multiProcessorCount;
+    h->w13_clusters = gemm_w13_max_clusters(I / 128);
+    if (h->w13_clusters <= 0) {
+      set_err(h, "no thread-block cluster of %d CTAs fits on the device", I / 128);
+      return fail(MOE_ERR_UNSUPPORTED);
+    }
   }
   *out = h;
   return MOE_OK;
@@ -669,7 +679,7 @@ moe_status moe_debug_convert(const float* in, uint8_t* e2m1, uint8_t* e4m3, int6
 moe_status moe_debug_block_scaled_gemm(const uint8_t* a_codes, const uint8_t* a_sf, const uint8_t* b_codes,
                                        const uint8_t* b_sf, float* d, int M, int N, int K, void* stream) {
   if (!a_codes || !a_sf || !b_codes || !b_sf || !d) return MOE_ERR_INVALID_ARG;
-  if (M <= 0 || N <= 0 || K <= 0 || M % 128 || N % 256 || K % 256) return MOE_ERR_UNSUPPORTED;
+  if (M <= 0 || N <= 0 || K <= 0 || M % 128 || N % 128 || K % 256) return MOE_ERR_UNSUPPORTED;
   if (!aligned16(a_codes) || !aligned16(b_codes) || !aligned16(d)) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t *sfa = nullptr, *sfb = nullptr;
@@ -685,8 +695,12 @@ moe_status moe_debug_block_scaled_gemm(const uint8_t* a_codes, const uint8_t* a_
       launch_sf_to_atoms(b_sf, N, K / 16, sfb, s) != cudaSuccess)
     st = MOE_ERR_CUDA;
   if (st == MOE_OK) st = make_operand_map(&tmp, &ta, a_codes, K / 2, M, 32);
-  if (st == MOE_OK) st = make_operand_map(&tmp, &tb, b_codes, K / 2, N, 256);
-  if (st == MOE_OK && gemm_setup_attributes() != cudaSuccess) st = MOE_ERR_CUDA;
+  if (st == MOE_OK) st = make_operand_map(&tmp, &tb, b_codes, K / 2, N, TILE_N);
+  if (st == MOE_OK && gemm_setup_attributes(1) != cudaSuccess) st = MOE_ERR_CUDA;
+  int dev = 0, sms = 0;
+  if (st == MOE_OK && (cudaGetDevice(&dev) != cudaSuccess ||
+                       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess))
+    st = MOE_ERR_CUDA;
   if (st == MOE_OK) {
     GemmArgs g{};
     g.a_sf = sfa;
@@ -695,7 +709,9 @@ moe_status moe_debug_block_scaled_gemm(const uint8_t* a_codes, const uint8_t* a_
     g.kblocks = K / MMA_K;
     g.d = d;
     g.ldd = N;
-    if (launch_gemm_plain(ta, tb, g, N / TILE_N, M / TILE_M, s) != cudaSuccess) st = MOE_ERR_CUDA;
+    g.n_tiles = N / TILE_N;
+    g.m_tiles = M / TILE_M;
+    if (launch_gemm_plain(ta, tb, g, std::min(sms, g.n_tiles * g.m_tiles), s) != cudaSuccess) st = MOE_ERR_CUDA;
   }
   if (cudaStreamSynchronize(s) != cudaSuccess) st = MOE_ERR_CUDA;
   cudaFree(sfa);
