@@ -26,6 +26,15 @@ constexpr int SF_ATOM_BYTES = 512;  // block scales of 128 rows x 64 K-elements
 constexpr int DEV_ERR_TIMEOUT = 1;
 constexpr int DEV_ERR_BAD_STATE = 2;
 
+// Byte offset of packed code byte kb (elements 2kb, 2kb+1) of `row` in the
+// tiled operand layout: tiles of 128 rows x 128 bytes (256 elements of K),
+// each one contiguous 16 KB block, ordered [row / 128][kb / 128].  A pipeline
+// stage of a GEMM then reads one contiguous block per operand tile.
+__host__ __device__ __forceinline__ size_t operand_offset(size_t row, int kb, int row_bytes) {
+  const int stages = row_bytes >> 7;
+  return (((row >> 7) * stages + (size_t)(kb >> 7)) * 128 + (row & 127)) * 128 + (kb & 127);
+}
+
 // Byte offset of the block scale of (row, k16) in the "128x4 atom" layout the
 // tensor cores read: atoms of 128 rows x 4 block scales (64 K-elements), 512
 // bytes each; row r of an atom at (r%32)*16 + (r/32)*4, block j at +j.
@@ -309,16 +318,16 @@ __device__ __forceinline__ void st_shared_cluster_f32(const void* local_smem, ui
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_map(local_smem, rank)), "f"(v) : "memory");
 }
 
-// Store a 64-bit word at the same shared-memory offset in CTA `rank` (one
-// single-copy-atomic access: a reader sees both halves of one store).
-__device__ __forceinline__ void st_shared_cluster_u64(const void* local_smem, uint32_t rank, uint64_t v) {
-  asm volatile("st.relaxed.cluster.shared::cluster.u64 [%0], %1;" ::"r"(cluster_map(local_smem, rank)), "l"(v)
+// Store a 32-bit word at the same shared-memory offset in CTA `rank` (one
+// single-copy-atomic access).
+__device__ __forceinline__ void st_shared_cluster_u32(const void* local_smem, uint32_t rank, uint32_t v) {
+  asm volatile("st.relaxed.cluster.shared::cluster.u32 [%0], %1;" ::"r"(cluster_map(local_smem, rank)), "r"(v)
                : "memory");
 }
 
-__device__ __forceinline__ uint64_t ld_shared_relaxed_u64(const void* local_smem) {
-  uint64_t v;
-  asm volatile("ld.relaxed.cluster.shared::cta.u64 %0, [%1];" : "=l"(v) : "r"(smem_u32(local_smem)) : "memory");
+__device__ __forceinline__ uint32_t ld_shared_relaxed_u32(const void* local_smem) {
+  uint32_t v;
+  asm volatile("ld.relaxed.cluster.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(local_smem)) : "memory");
   return v;
 }
 

@@ -24,7 +24,8 @@ struct PermuteOut {
   int4* tiles;              // [tile bound] {expert, first padded row, valid rows, 0}
   int32_t* num_tiles;       // [1]
 };
-cudaError_t launch_permute(const int32_t* topk_ids, const int32_t* counts, int T, int K, int E,
+// tile_rows: 32 (small batches) or 128 rows per GEMM tile.
+cudaError_t launch_permute(const int32_t* topk_ids, const int32_t* counts, int T, int K, int E, int tile_rows,
                            const PermuteOut& o, cudaStream_t s);
 
 // ---- quantization (kernels_quant.cu) ----
@@ -41,6 +42,7 @@ cudaError_t launch_export_rows(const uint8_t* codes, const uint8_t* sf, const fl
                                int E_rows, uint8_t* out_codes, uint8_t* out_sf, float* out_gs, cudaStream_t s);
 cudaError_t launch_convert(const float* in, uint8_t* e2m1, uint8_t* e4m3, int64_t n, cudaStream_t s);
 cudaError_t launch_sf_to_atoms(const uint8_t* sf, int rows, int k16, uint8_t* atoms, cudaStream_t s);
+cudaError_t launch_codes_to_tiled(const uint8_t* codes, int rows, int row_bytes, uint8_t* tiled, cudaStream_t s);
 
 // ---- finalize (kernels_quant.cu) ----
 cudaError_t launch_finalize_atomic(const float* out_acc, void* out, int T, int H, cudaStream_t s);
@@ -82,13 +84,15 @@ int gemm_smem_bytes();
 cudaError_t gemm_setup_attributes(int w13_chunks);
 // Thread-block clusters of the w13 kernel (w13_chunks CTAs each) that fit on
 // the device at once; 0 if none.
-int gemm_w13_max_clusters(int w13_chunks);
+int gemm_w13_max_clusters(int w13_chunks, int a_rows);
 // Persistent launches: the w13 kernel runs n_clusters clusters of n_chunks
 // CTAs; the w2 / plain kernels run n_ctas CTAs.  Each walks a static tile list.
+// a_rows: rows of the activation operand per tile (32 or 128; every tile of
+// the list must have at most that many valid rows).
 cudaError_t launch_gemm_w13(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int n_chunks,
-                            int n_clusters, cudaStream_t s);
+                            int n_clusters, int a_rows, cudaStream_t s);
 cudaError_t launch_gemm_w2(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int n_ctas,
-                           bool ordered, cudaStream_t s);
+                           bool ordered, int a_rows, cudaStream_t s);
 cudaError_t launch_gemm_plain(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int n_ctas,
                               cudaStream_t s);
 

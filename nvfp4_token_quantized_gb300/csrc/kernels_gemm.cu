@@ -47,12 +47,14 @@ namespace moe {
 
 namespace {
 
-constexpr int A_STAGE = TILE_M * 128;        // 16 KB: 128 rows x 128 bytes
 constexpr int B_STAGE = TILE_N * 128;        // 16 KB: 128 rows x 128 bytes
 constexpr int SFA_STAGE = 4 * SF_ATOM_BYTES; // 2 KB: 128 rows x 16 scales
 constexpr int SFB_STAGE = 4 * SF_ATOM_BYTES; // 2 KB: 128 rows x 16 scales
-constexpr int STAGE_BYTES = A_STAGE + B_STAGE + SFA_STAGE + SFB_STAGE;
-constexpr int MAX_STAGES = 6;
+constexpr int MAX_STAGES = 8;
+// Activation rows reserved per stage: 128, or 32 for small batches.  The MMA
+// always reads 128 rows; with 32 reserved, rows 32..127 read the next stages'
+// data (or the tail pad after the last stage) - in bounds, and their results
+// are never used because such tiles have at most 32 valid rows.
 constexpr int A_BOX_ROWS = 32;
 constexpr int TMEM_COLS = 512;
 constexpr int TMEM_SF_BASE = 2 * TILE_N;     // two accumulator buffers in columns [0, 256)
@@ -76,8 +78,13 @@ struct Ctrl {
 };
 static_assert(sizeof(Ctrl) <= CTRL_BYTES, "control block too large");
 
-__host__ __device__ constexpr int smem_bytes_for(int stages, int nch) {
-  return stages * STAGE_BYTES + CTRL_BYTES + 2 * nch * TILE_M * 8 + 1024;
+__host__ __device__ constexpr int a_stage_bytes(int a_rows) { return a_rows * 128; }
+__host__ __device__ constexpr int a_tail_bytes(int a_rows) { return (TILE_M - a_rows) * 128; }
+__host__ __device__ constexpr int stage_bytes(int a_rows) {
+  return a_stage_bytes(a_rows) + B_STAGE + SFA_STAGE + SFB_STAGE;
+}
+__host__ __device__ constexpr int smem_bytes_for(int stages, int nch, int a_rows) {
+  return stages * stage_bytes(a_rows) + a_tail_bytes(a_rows) + CTRL_BYTES + 2 * nch * TILE_M * 4 + 1024;
 }
 
 __device__ __forceinline__ float swiglu(float g_acc, float u_acc, float alpha) {
@@ -95,18 +102,20 @@ struct Unit {
   int e, row0, valid, col;  // expert, first padded row, valid rows, 128-column block of B
 };
 
-template <int MODE, int STAGES>
+template <int MODE, int A_ROWS, int STAGES>
 __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA,
                                                              const __grid_constant__ CUtensorMap tmB, GemmArgs p) {
+  constexpr int A_STAGE = a_stage_bytes(A_ROWS);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = base;
-  uint8_t* sB = sA + STAGES * A_STAGE;
+  uint8_t* sB = sA + STAGES * A_STAGE + a_tail_bytes(A_ROWS);
   uint8_t* sSFA = sB + STAGES * B_STAGE;
   uint8_t* sSFB = sSFA + STAGES * SFA_STAGE;
   Ctrl& c = *reinterpret_cast<Ctrl*>(sSFB + STAGES * SFB_STAGE);
-  // [2][nch][128] words of (tile tag << 32 | partial row maximum bits)
-  uint64_t* part = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(&c) + CTRL_BYTES);
+  // [2][nch][128] words: partial row maximum bits (non-negative, so bit 31
+  // is free) with bit 31 holding the m-tile tag
+  uint32_t* part = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(&c) + CTRL_BYTES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -155,7 +164,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
     }
     c.abort_flag = 0;
     if (MODE == MODE_W13)
-      for (int i = 0; i < 2 * nch * TILE_M; ++i) part[i] = 0;  // tag 0 is never a live tile
+      for (int i = 0; i < 2 * nch * TILE_M; ++i) part[i] = 0x80000000u;  // tag of no first use
     fence_mbarrier_init();
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
@@ -198,10 +207,12 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
             break;
           }
           mbar_arrive_expect_tx(&c.full[s], bytes);
+          // operands are tiled: tile (row block, stage) is rows
+          // ((row / 128) * KS + ks) * 128 + row % 128 of a 128-byte-wide tensor
+          const int ya = ((un.row0 >> 7) * KS + ks) * TILE_M + (un.row0 & 127);
           for (int i = 0; i < a_boxes; ++i)
-            tma_load_2d(sA + s * A_STAGE + i * A_BOX_ROWS * 128, &tmA, &c.full[s], ks * 128,
-                        un.row0 + i * A_BOX_ROWS, pol_a);
-          tma_load_2d(sB + s * B_STAGE, &tmB, &c.full[s], ks * 128, brow0, pol_w);
+            tma_load_2d(sA + s * A_STAGE + i * A_BOX_ROWS * 128, &tmA, &c.full[s], 0, ya + i * A_BOX_ROWS, pol_a);
+          tma_load_2d(sB + s * B_STAGE, &tmB, &c.full[s], 0, ((brow0 >> 7) * KS + ks) * TILE_N, pol_w);
           bulk_load(sSFA + s * SFA_STAGE, sfa_src + (size_t)ks * SFA_STAGE, SFA_STAGE, &c.full[s]);
           bulk_load(sSFB + s * SFB_STAGE, sfb_src + (size_t)ks * SFB_STAGE, SFB_STAGE, &c.full[s]);
         }
@@ -318,20 +329,21 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
         // Exchange the row maxima across the cluster.  Slot buffer i & 1;
         // a peer can be at most one m-tile ahead (it needs this CTA's value
         // of its next m-tile first), so two buffers never overwrite a value
-        // that has not been read.
+        // that has not been read, and the successive uses of a buffer
+        // alternate the tag bit.
         const int b = i & 1;
-        const uint64_t tag = (uint64_t)(i + 1) << 32;
-        const uint64_t* slots = part + (size_t)b * nch * TILE_M + m;
+        const uint32_t tag = ((uint32_t)(i >> 1) & 1u) << 31;
+        const uint32_t* slots = part + (size_t)b * nch * TILE_M + m;
         for (int r = 0; r < nch; ++r)
-          st_shared_cluster_u64(slots + (size_t)rank * TILE_M, (uint32_t)r, tag | __float_as_uint(amax));
+          st_shared_cluster_u32(slots + (size_t)rank * TILE_M, (uint32_t)r, tag | __float_as_uint(amax));
         float amax_row = 0.0f;
         for (int r = 0; r < nch; ++r) {
-          const uint64_t* slot = slots + (size_t)r * TILE_M;
-          uint64_t v = ld_shared_relaxed_u64(slot);
-          if ((v >> 32) != (tag >> 32)) {
+          const uint32_t* slot = slots + (size_t)r * TILE_M;
+          uint32_t v = ld_shared_relaxed_u32(slot);
+          if ((v & 0x80000000u) != tag) {
             const uint64_t t0 = global_timer_ns();
-            for (uint32_t it = 1; (v >> 32) != (tag >> 32); ++it) {
-              v = ld_shared_relaxed_u64(slot);
+            for (uint32_t it = 1; (v & 0x80000000u) != tag; ++it) {
+              v = ld_shared_relaxed_u32(slot);
               if ((it & 255u) == 0 && global_timer_ns() - t0 > 2000000000ull) {
                 c.abort_flag = 1;
                 report_device_error(p.status, DEV_ERR_TIMEOUT);
@@ -340,7 +352,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
               }
             }
           }
-          amax_row = fmaxf(amax_row, __uint_as_float((uint32_t)v));
+          amax_row = fmaxf(amax_row, __uint_as_float(v & 0x7FFFFFFFu));
         }
         const float gs_h = nvfp4_global_scale(amax_row);
         if (ready && row_ok) {
@@ -353,7 +365,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
             uint2 packed;
             const uint32_t sf = nvfp4_quant_block16(v, gs_h, packed);
             const int k = (int)rank * 128 + 16 * cc;  // feature index of this block
-            *reinterpret_cast<uint2*>(p.h_codes + (size_t)prow * (p.i_pad / 2) + k / 2) = packed;
+            *reinterpret_cast<uint2*>(p.h_codes + operand_offset(prow, k / 2, p.i_pad / 2)) = packed;
             p.h_sf[sf_atom_offset(prow, k / SF_VEC, k16_row)] = (uint8_t)sf;
           }
           if (rank == 0) p.h_gs[prow] = gs_h;
@@ -425,28 +437,28 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
   }
 }
 
-int stages_for(int nch) {
+constexpr int stages_for(int nch, int a_rows) {
   for (int s = MAX_STAGES; s >= 3; --s)
-    if (smem_bytes_for(s, nch) <= MAX_SMEM) return s;
+    if (smem_bytes_for(s, nch, a_rows) <= MAX_SMEM) return s;
   return 0;
 }
 
-template <int MODE, int STAGES>
+template <int MODE, int A_ROWS, int STAGES>
 cudaError_t set_attrs(int nch) {
-  cudaError_t err = cudaFuncSetAttribute(gemm_fp4_kernel<MODE, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         smem_bytes_for(STAGES, nch));
+  auto k = gemm_fp4_kernel<MODE, A_ROWS, STAGES>;
+  cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         smem_bytes_for(STAGES, nch, A_ROWS));
   if (err != cudaSuccess) return err;
-  if (MODE == MODE_W13)
-    err = cudaFuncSetAttribute(gemm_fp4_kernel<MODE, STAGES>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (MODE == MODE_W13) err = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   return err;
 }
 
-template <int MODE, int STAGES>
+template <int MODE, int A_ROWS, int STAGES>
 cudaLaunchConfig_t make_cfg(dim3 grid, int nch, cudaStream_t s, cudaLaunchAttribute* attr, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = smem_bytes_for(STAGES, MODE == MODE_W13 ? nch : 0);
+  cfg.dynamicSmemBytes = smem_bytes_for(STAGES, MODE == MODE_W13 ? nch : 0, A_ROWS);
   cfg.stream = s;
   int n = 0;
   if (MODE == MODE_W13) {
@@ -466,46 +478,62 @@ cudaLaunchConfig_t make_cfg(dim3 grid, int nch, cudaStream_t s, cudaLaunchAttrib
   return cfg;
 }
 
-template <int MODE, int STAGES>
+template <int MODE, int A_ROWS, int STAGES>
 cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, dim3 grid, int nch,
                    cudaStream_t s) {
   cudaLaunchAttribute attr[2];
   // The expert GEMMs always follow another kernel of the same forward.
-  cudaLaunchConfig_t cfg = make_cfg<MODE, STAGES>(grid, nch, s, attr, MODE != MODE_PLAIN);
-  return cudaLaunchKernelEx(&cfg, gemm_fp4_kernel<MODE, STAGES>, tmA, tmB, a);
+  cudaLaunchConfig_t cfg = make_cfg<MODE, A_ROWS, STAGES>(grid, nch, s, attr, MODE != MODE_PLAIN);
+  return cudaLaunchKernelEx(&cfg, gemm_fp4_kernel<MODE, A_ROWS, STAGES>, tmA, tmB, a);
 }
 
-// Dispatch on the ring depth that fits the w13 kernel's shared memory.
+// Ring depths that occur: w2 / plain kernels (no exchange slots) and w13
+// kernels with clusters of up to 6 CTAs get the deepest ring that fits; larger
+// clusters one stage less.
+constexpr int W2_STAGES_128 = stages_for(0, 128);
+constexpr int W2_STAGES_32 = stages_for(0, 32);
+constexpr int W13_STAGES_128 = stages_for(6, 128);
+constexpr int W13_STAGES_128_L = stages_for(16, 128);
+constexpr int W13_STAGES_32 = stages_for(6, 32);
+constexpr int W13_STAGES_32_L = stages_for(16, 32);
+static_assert(W2_STAGES_128 >= 4 && W13_STAGES_128_L >= 3 && W13_STAGES_32_L >= 4, "ring too shallow");
+
 template <typename F>
-cudaError_t with_w13_stages(int nch, F&& f) {
-  switch (stages_for(nch)) {
-    case 6: return f(std::integral_constant<int, 6>{});
-    case 5: return f(std::integral_constant<int, 5>{});
-    case 4: return f(std::integral_constant<int, 4>{});
-    case 3: return f(std::integral_constant<int, 3>{});
-    default: return cudaErrorInvalidConfiguration;
+cudaError_t with_w13(int nch, int a_rows, F&& f) {
+  if (a_rows == 32) {
+    if (nch <= 6) return f(std::integral_constant<int, 32>{}, std::integral_constant<int, W13_STAGES_32>{});
+    return f(std::integral_constant<int, 32>{}, std::integral_constant<int, W13_STAGES_32_L>{});
   }
+  if (nch <= 6) return f(std::integral_constant<int, 128>{}, std::integral_constant<int, W13_STAGES_128>{});
+  return f(std::integral_constant<int, 128>{}, std::integral_constant<int, W13_STAGES_128_L>{});
 }
 
 }  // namespace
 
-int gemm_smem_bytes() { return smem_bytes_for(MAX_STAGES, 0); }
+int gemm_smem_bytes() { return smem_bytes_for(W2_STAGES_128, 0, 128); }
 
 cudaError_t gemm_setup_attributes(int nch) {
-  cudaError_t e = with_w13_stages(nch, [&](auto st) { return set_attrs<MODE_W13, decltype(st)::value>(nch); });
-  if (e != cudaSuccess) return e;
-  if ((e = set_attrs<MODE_W2_ATOMIC, MAX_STAGES>(0)) != cudaSuccess) return e;
-  if ((e = set_attrs<MODE_W2_ORDERED, MAX_STAGES>(0)) != cudaSuccess) return e;
-  return set_attrs<MODE_PLAIN, MAX_STAGES>(0);
+  cudaError_t e;
+  for (int a_rows : {32, 128}) {
+    e = with_w13(nch, a_rows, [&](auto ar, auto st) {
+      return set_attrs<MODE_W13, decltype(ar)::value, decltype(st)::value>(nch);
+    });
+    if (e != cudaSuccess) return e;
+  }
+  if ((e = set_attrs<MODE_W2_ATOMIC, 128, W2_STAGES_128>(0)) != cudaSuccess) return e;
+  if ((e = set_attrs<MODE_W2_ATOMIC, 32, W2_STAGES_32>(0)) != cudaSuccess) return e;
+  if ((e = set_attrs<MODE_W2_ORDERED, 128, W2_STAGES_128>(0)) != cudaSuccess) return e;
+  if ((e = set_attrs<MODE_W2_ORDERED, 32, W2_STAGES_32>(0)) != cudaSuccess) return e;
+  return set_attrs<MODE_PLAIN, 128, W2_STAGES_128>(0);
 }
 
-int gemm_w13_max_clusters(int nch) {
+int gemm_w13_max_clusters(int nch, int a_rows) {
   int n = 0;
-  cudaError_t e = with_w13_stages(nch, [&](auto st) {
-    constexpr int S = decltype(st)::value;
+  cudaError_t e = with_w13(nch, a_rows, [&](auto ar, auto st) {
+    constexpr int AR = decltype(ar)::value, S = decltype(st)::value;
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = make_cfg<MODE_W13, S>(dim3(nch, 1, 1), nch, 0, attr, false);
-    return cudaOccupancyMaxActiveClusters(&n, gemm_fp4_kernel<MODE_W13, S>, &cfg);
+    cudaLaunchConfig_t cfg = make_cfg<MODE_W13, AR, S>(dim3(nch, 1, 1), nch, 0, attr, false);
+    return cudaOccupancyMaxActiveClusters(&n, gemm_fp4_kernel<MODE_W13, AR, S>, &cfg);
   });
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -515,22 +543,27 @@ int gemm_w13_max_clusters(int nch) {
 }
 
 cudaError_t launch_gemm_w13(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int n_chunks,
-                            int n_clusters, cudaStream_t s) {
+                            int n_clusters, int a_rows, cudaStream_t s) {
   const dim3 grid(n_chunks, n_clusters, 1);
-  return with_w13_stages(n_chunks, [&](auto st) {
-    return launch<MODE_W13, decltype(st)::value>(tmA, tmB, a, grid, n_chunks, s);
+  return with_w13(n_chunks, a_rows, [&](auto ar, auto st) {
+    return launch<MODE_W13, decltype(ar)::value, decltype(st)::value>(tmA, tmB, a, grid, n_chunks, s);
   });
 }
 
 cudaError_t launch_gemm_w2(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int n_ctas,
-                           bool ordered, cudaStream_t s) {
-  if (ordered) return launch<MODE_W2_ORDERED, MAX_STAGES>(tmA, tmB, a, dim3(n_ctas, 1, 1), 0, s);
-  return launch<MODE_W2_ATOMIC, MAX_STAGES>(tmA, tmB, a, dim3(n_ctas, 1, 1), 0, s);
+                           bool ordered, int a_rows, cudaStream_t s) {
+  const dim3 grid(n_ctas, 1, 1);
+  if (a_rows == 32) {
+    if (ordered) return launch<MODE_W2_ORDERED, 32, W2_STAGES_32>(tmA, tmB, a, grid, 0, s);
+    return launch<MODE_W2_ATOMIC, 32, W2_STAGES_32>(tmA, tmB, a, grid, 0, s);
+  }
+  if (ordered) return launch<MODE_W2_ORDERED, 128, W2_STAGES_128>(tmA, tmB, a, grid, 0, s);
+  return launch<MODE_W2_ATOMIC, 128, W2_STAGES_128>(tmA, tmB, a, grid, 0, s);
 }
 
 cudaError_t launch_gemm_plain(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int n_ctas,
                               cudaStream_t s) {
-  return launch<MODE_PLAIN, MAX_STAGES>(tmA, tmB, a, dim3(n_ctas, 1, 1), 0, s);
+  return launch<MODE_PLAIN, 128, W2_STAGES_128>(tmA, tmB, a, dim3(n_ctas, 1, 1), 0, s);
 }
 
 }  // namespace moe

@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __r
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       if (j < K) {
-        *reinterpret_cast<uint2*>(a_codes + (size_t)prow[j] * row_bytes + 8 * b) = packed;
+        *reinterpret_cast<uint2*>(a_codes + operand_offset(prow[j], 8 * b, (int)row_bytes)) = packed;
         a_sf[sf_atom_offset(prow[j], b, nblk)] = (uint8_t)sf;
       }
     }
@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(256) weight_quant_kernel(const __nv_bfloat16* 
     bf16x16_to_f32(__ldg(src + 2 * b), __ldg(src + 2 * b + 1), v);
     uint2 packed;
     const uint32_t s = nvfp4_quant_block16(v, gs, packed);
-    *reinterpret_cast<uint2*>(codes + (size_t)irow * (Kpad / 2) + 8 * b) = packed;
+    *reinterpret_cast<uint2*>(codes + operand_offset(irow, 8 * b, Kpad / 2)) = packed;
     sf[sf_atom_offset(irow, b, Kpad / SF_VEC)] = (uint8_t)s;
   }
   if (n == 0 && lane == 0) gs_out[e] = gs;
@@ -149,7 +149,8 @@ __global__ void __launch_bounds__(256) export_rows_kernel(const uint8_t* __restr
   else if (mode == 1) r = i;
   else r = (i / E_rows) * E_rows + w13_internal_row(i % E_rows, E_rows);
   if (out_codes)
-    for (int b = lane; b < Kd / 2; b += 32) out_codes[(size_t)i * (Kd / 2) + b] = codes[(size_t)r * (Kpad / 2) + b];
+    for (int b = lane; b < Kd / 2; b += 32)
+      out_codes[(size_t)i * (Kd / 2) + b] = codes[operand_offset(r, b, Kpad / 2)];
   if (out_sf)
     for (int b = lane; b < Kd / SF_VEC; b += 32)
       out_sf[(size_t)i * (Kd / SF_VEC) + b] = sf[sf_atom_offset(r, b, Kpad / SF_VEC)];
@@ -163,6 +164,14 @@ __global__ void convert_kernel(const float* __restrict__ in, uint8_t* __restrict
     if (e2m1) e2m1[i] = (uint8_t)(cvt_e2m1x2(v, 0.0f) & 0xF);
     if (e4m3) e4m3[i] = (uint8_t)cvt_e4m3(v);
   }
+}
+
+// Row-major codes [rows, row_bytes] -> tiled operand layout (tests).
+__global__ void codes_to_tiled_kernel(const uint8_t* __restrict__ codes, int rows, int row_bytes,
+                                      uint8_t* __restrict__ tiled) {
+  const int64_t n = (int64_t)rows * row_bytes;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    tiled[operand_offset(i / row_bytes, (int)(i % row_bytes), row_bytes)] = codes[i];
 }
 
 __global__ void sf_to_atoms_kernel(const uint8_t* __restrict__ sf, int rows, int k16, uint8_t* __restrict__ atoms) {
@@ -253,6 +262,11 @@ cudaError_t launch_export_rows(const uint8_t* codes, const uint8_t* sf, const fl
 cudaError_t launch_convert(const float* in, uint8_t* e2m1, uint8_t* e4m3, int64_t n, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
   convert_kernel<<<grid_for((size_t)n, 256), 256, 0, s>>>(in, e2m1, e4m3, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_codes_to_tiled(const uint8_t* codes, int rows, int row_bytes, uint8_t* tiled, cudaStream_t s) {
+  codes_to_tiled_kernel<<<grid_for((size_t)rows * row_bytes, 256), 256, 0, s>>>(codes, rows, row_bytes, tiled);
   return cudaGetLastError();
 }
 

@@ -6,8 +6,8 @@
 // multiply-adds in ascending order; a pairwise tree over the 32 partials),
 // so expert choices are reproducible bit for bit on any implementation of the
 // same order.  The permutation groups rows by expert and keeps token order
-// inside an expert, and pads each expert to whole 128-row tiles for the
-// tensor-core GEMMs.
+// inside an expert, and pads each GEMM tile of an expert to its own 128-row
+// block for the tensor-core GEMMs.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -287,20 +287,25 @@ constexpr int PERM_THREADS = 512;
 constexpr int PERM_TPT = 8;  // tokens per thread per pass
 
 // One CTA per expert: offsets from the counts, then a stable compaction of
-// the (token, slot) pairs that chose this expert, in token order.
+// the (token, slot) pairs that chose this expert, in token order.  The
+// expert's rows are cut into GEMM tiles of tile_rows (32 or 128) rows; each
+// tile starts its own 128-row block of the padded operand layout, so a tile's
+// rows always sit at the head of one block-scale atom.
 __global__ void __launch_bounds__(PERM_THREADS) permute_kernel(const int32_t* __restrict__ topk_ids,
                                                               const int32_t* __restrict__ counts, int T, int K,
-                                                              int E, PermuteOut o) {
+                                                              int E, int tile_shift, PermuteOut o) {
   __shared__ int red[PERM_THREADS / 32];
   const int e = blockIdx.x;
+  const int tile_rows = 1 << tile_shift;   // 32 or 128 rows per GEMM tile
   pdl_trigger();
   pdl_wait();
   int c_lt = 0, p_lt = 0, n_lt = 0;
   for (int i = threadIdx.x; i < e; i += blockDim.x) {
     const int c = counts[i];
+    const int nt = (c + tile_rows - 1) >> tile_shift;
     c_lt += c;
-    p_lt += (c + 127) & ~127;
-    n_lt += (c + 127) >> 7;
+    p_lt += nt * 128;                      // every tile starts a 128-row block
+    n_lt += nt;
   }
   const int off = block_sum_int(c_lt, red);
   const int poff = block_sum_int(p_lt, red);
@@ -329,7 +334,7 @@ __global__ void __launch_bounds__(PERM_THREADS) permute_kernel(const int32_t* __
       if (slot[i] >= 0) {
         const int src = (tb + i) * K + slot[i];
         const int r = off + pos;
-        const int pr = poff + pos;
+        const int pr = poff + (pos >> tile_shift) * 128 + (pos & (tile_rows - 1));
         o.src_of_row[r] = src;
         o.row_of_src[src] = r;
         o.pad_row_of_src[src] = pr;
@@ -339,9 +344,9 @@ __global__ void __launch_bounds__(PERM_THREADS) permute_kernel(const int32_t* __
     }
     carry += tot;
   }
-  const int ntile = (cnt + 127) >> 7;
+  const int ntile = (cnt + tile_rows - 1) >> tile_shift;
   for (int i = threadIdx.x; i < ntile; i += blockDim.x)
-    o.tiles[tbase + i] = make_int4(e, poff + 128 * i, min(128, cnt - 128 * i), 0);
+    o.tiles[tbase + i] = make_int4(e, poff + 128 * i, min(tile_rows, cnt - tile_rows * i), 0);
   if (threadIdx.x == 0) {
     o.expert_offsets[e] = off;
     if (e == E - 1) {
@@ -413,9 +418,10 @@ cudaError_t launch_topk(const float* logits, int T, int E, int K, int32_t* topk_
   return launch_k(topk_kernel, dim3((T + 7) / 8), dim3(256), 0, s, true, logits, T, E, K, topk_ids, topk_w, counts);
 }
 
-cudaError_t launch_permute(const int32_t* topk_ids, const int32_t* counts, int T, int K, int E,
+cudaError_t launch_permute(const int32_t* topk_ids, const int32_t* counts, int T, int K, int E, int tile_rows,
                            const PermuteOut& o, cudaStream_t s) {
-  return launch_k(permute_kernel, dim3(E), dim3(PERM_THREADS), 0, s, true, topk_ids, counts, T, K, E, o);
+  const int shift = tile_rows == 32 ? 5 : 7;
+  return launch_k(permute_kernel, dim3(E), dim3(PERM_THREADS), 0, s, true, topk_ids, counts, T, K, E, shift, o);
 }
 
 }  // namespace moe

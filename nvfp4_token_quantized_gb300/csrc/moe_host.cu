@@ -29,9 +29,9 @@ struct moe_handle {
   int Ipad = 0;         // intermediate width padded to a multiple of 256 (w2 GEMM K)
   int Rmax = 0;         // Tmax * K
   int Rpad = 0;         // padded expert-grouped rows, worst case
-  int tile_cap = 0;     // worst-case number of 128-row tiles
+  int tile_cap = 0;     // worst-case number of GEMM tiles
   int num_sms = 0;      // persistent w2 grid
-  int w13_clusters = 0; // persistent w13 grid (clusters of I/128 CTAs)
+  int w13_clusters[2] = {0, 0};  // persistent w13 grid (clusters of I/128 CTAs), 32- / 128-row tiles
   bool deterministic = false;
   bool loaded = false;
   moe_weight_desc w13_desc{}, w2_desc{};
@@ -128,8 +128,10 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   return fn;
 }
 
-// 2D byte tensor [rows, row_bytes] with a 128-byte-wide box of box_rows rows,
-// 128-byte swizzle (the K-major operand layout of the FP4 MMAs).
+// Tensor map of an operand in the tiled layout (tiles of 128 rows x 128
+// bytes, contiguous): a 128-byte-wide tensor of rows * row_bytes / 128 rows,
+// boxes of box_rows rows, 128-byte swizzle (the K-major operand layout of the
+// FP4 MMAs).
 moe_status make_operand_map(moe_handle* h, CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows,
                             uint32_t box_rows) {
   auto fn = get_encode_fn();
@@ -137,8 +139,13 @@ moe_status make_operand_map(moe_handle* h, CUtensorMap* map, const void* base, u
     set_err(h, "cuTensorMapEncodeTiled is not available from the driver");
     return MOE_ERR_CUDA;
   }
-  cuuint64_t dims[2] = {row_bytes, rows};
-  cuuint64_t strides[1] = {row_bytes};
+  if (rows % 128 || row_bytes % 128) {
+    set_err(h, "operand of %llu rows x %llu bytes is not whole 128x128 tiles", (unsigned long long)rows,
+            (unsigned long long)row_bytes);
+    return MOE_ERR_INVALID_ARG;
+  }
+  cuuint64_t dims[2] = {128, rows * (row_bytes / 128)};
+  cuuint64_t strides[1] = {128};
   cuuint32_t box[2] = {128, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
@@ -174,12 +181,20 @@ int device_of(const void* p) {
   return at.device;
 }
 
-// Worst-case number of 128-row tiles when T tokens each pick K of E experts.
-int tile_bound(int T, int K, int E) {
+// Forwards of at most this many tokens use 32-row GEMM tiles: their experts
+// get a handful of rows each, and reserving 32 instead of 128 activation rows
+// per pipeline stage leaves room for a deeper weight-streaming ring.
+constexpr int SMALL_BATCH_TOKENS = 64;
+
+int tile_rows_for(int T) { return T <= SMALL_BATCH_TOKENS ? 32 : 128; }
+
+// Worst-case number of GEMM tiles of tile_rows rows when T tokens each pick
+// K of E experts (each tile is padded to its own 128-row block).
+int tile_bound(int T, int K, int E, int tile_rows) {
   const long R = (long)T * K;
   const long busy = std::min<long>(E, R);
-  const long a = (R + 127L * busy) / 128;
-  const long b = busy * ((T + 127L) / 128);
+  const long a = (R + (tile_rows - 1L) * busy) / tile_rows;
+  const long b = busy * ((T + tile_rows - 1L) / tile_rows);
   return (int)std::max<long>(1, std::min(a, b));
 }
 
@@ -258,14 +273,15 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
     CK(h, mark(h, 1, s));
     CK(h, launch_topk(h->logits, T, E, K, h->topk_ids, h->topk_w, h->counts, s));
     CK(h, mark(h, 2, s));
+    const int tile_rows = tile_rows_for(T);
     PermuteOut po{h->expert_offsets, h->src_of_row, h->row_of_src, h->pad_row_of_src,
                   h->src_of_padrow,  h->tiles,      h->num_tiles};
-    CK(h, launch_permute(h->topk_ids, h->counts, T, K, E, po, s));
+    CK(h, launch_permute(h->topk_ids, h->counts, T, K, E, tile_rows, po, s));
     CK(h, mark(h, 3, s));
     CK(h, launch_act_quant(x, T, H, K, h->pad_row_of_src, h->a_codes, h->a_sf, h->gs_rows,
                            h->deterministic ? nullptr : h->out_acc, s));
     CK(h, mark(h, 4, s));
-    const int tb = tile_bound(T, K, E);
+    const int tb = tile_bound(T, K, E, tile_rows);
     GemmArgs g{};
     g.status = h->status_dev;
     g.tiles = h->tiles;
@@ -282,7 +298,8 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
     g.h_sf = h->h_sf;
     g.h_gs = h->h_gs;
     g.i_pad = h->Ipad;
-    CK(h, launch_gemm_w13(h->tm_a1, h->tm_b1, g, h->I / 128, std::min(h->w13_clusters, tb), s));
+    CK(h, launch_gemm_w13(h->tm_a1, h->tm_b1, g, h->I / 128, std::min(h->w13_clusters[tile_rows == 128], tb),
+                          tile_rows, s));
     CK(h, mark(h, 5, s));
     // w2: A = requantized intermediate [Rpad, Ipad], B = w2 [E*H, Ipad]
     GemmArgs g2{};
@@ -303,7 +320,8 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
     g2.ybuf = h->ybuf;
     g2.hidden = H;
     g2.n_tiles = H / TILE_N;
-    CK(h, launch_gemm_w2(h->tm_a2, h->tm_b2, g2, std::min(h->num_sms, tb * g2.n_tiles), h->deterministic, s));
+    CK(h, launch_gemm_w2(h->tm_a2, h->tm_b2, g2, std::min(h->num_sms, tb * g2.n_tiles), h->deterministic, tile_rows,
+                         s));
     CK(h, mark(h, 6, s));
     if (h->deterministic) CK(h, launch_finalize_ordered(h->ybuf, h->topk_w, out, T, H, K, s));
     else CK(h, launch_finalize_atomic(h->out_acc, out, T, H, s));
@@ -360,8 +378,8 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
   h->Tmax = T;
   h->Ipad = (I + 255) / 256 * 256;
   h->Rmax = T * K;
-  h->Rpad = (h->Rmax + 127 * std::min(E, h->Rmax) + 127) / 128 * 128;
-  h->tile_cap = tile_bound(T, K, E);
+  h->tile_cap = std::max(tile_bound(T, K, E, 128), tile_bound(std::min(T, SMALL_BATCH_TOKENS), K, E, 32));
+  h->Rpad = h->tile_cap * 128;
   h->deterministic = (cfg->flags & MOE_FLAG_DETERMINISTIC) != 0;
 
   auto fail = [&](moe_status s) {
@@ -425,8 +443,9 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
     e = router_setup(H, E);
     if (e != cudaSuccess) return fail(cuda_fail(h, e, "cudaFuncSetAttribute(router)"));
     h->num_sms = prop.multiProcessorCount;
-    h->w13_clusters = gemm_w13_max_clusters(I / 128);
-    if (h->w13_clusters <= 0) {
+    h->w13_clusters[0] = gemm_w13_max_clusters(I / 128, 32);
+    h->w13_clusters[1] = gemm_w13_max_clusters(I / 128, 128);
+    if (h->w13_clusters[0] <= 0 || h->w13_clusters[1] <= 0) {
       set_err(h, "no thread-block cluster of %d CTAs fits on the device", I / 128);
       return fail(MOE_ERR_UNSUPPORTED);
     }
@@ -689,13 +708,18 @@ moe_status moe_debug_block_scaled_gemm(const uint8_t* a_codes, const uint8_t* a_
     cudaFree(sfa);
     return MOE_ERR_CUDA;
   }
+  uint8_t *ta_codes = nullptr, *tb_codes = nullptr;
   moe_status st = MOE_OK;
-  CUtensorMap ta, tb;
-  if (launch_sf_to_atoms(a_sf, M, K / 16, sfa, s) != cudaSuccess ||
-      launch_sf_to_atoms(b_sf, N, K / 16, sfb, s) != cudaSuccess)
+  if (cudaMalloc(&ta_codes, (size_t)M * K / 2) != cudaSuccess || cudaMalloc(&tb_codes, (size_t)N * K / 2) != cudaSuccess)
     st = MOE_ERR_CUDA;
-  if (st == MOE_OK) st = make_operand_map(&tmp, &ta, a_codes, K / 2, M, 32);
-  if (st == MOE_OK) st = make_operand_map(&tmp, &tb, b_codes, K / 2, N, TILE_N);
+  CUtensorMap ta, tb;
+  if (st == MOE_OK && (launch_sf_to_atoms(a_sf, M, K / 16, sfa, s) != cudaSuccess ||
+                       launch_sf_to_atoms(b_sf, N, K / 16, sfb, s) != cudaSuccess ||
+                       launch_codes_to_tiled(a_codes, M, K / 2, ta_codes, s) != cudaSuccess ||
+                       launch_codes_to_tiled(b_codes, N, K / 2, tb_codes, s) != cudaSuccess))
+    st = MOE_ERR_CUDA;
+  if (st == MOE_OK) st = make_operand_map(&tmp, &ta, ta_codes, K / 2, M, 32);
+  if (st == MOE_OK) st = make_operand_map(&tmp, &tb, tb_codes, K / 2, N, TILE_N);
   if (st == MOE_OK && gemm_setup_attributes(1) != cudaSuccess) st = MOE_ERR_CUDA;
   int dev = 0, sms = 0;
   if (st == MOE_OK && (cudaGetDevice(&dev) != cudaSuccess ||
@@ -716,6 +740,8 @@ moe_status moe_debug_block_scaled_gemm(const uint8_t* a_codes, const uint8_t* a_
   if (cudaStreamSynchronize(s) != cudaSuccess) st = MOE_ERR_CUDA;
   cudaFree(sfa);
   cudaFree(sfb);
+  cudaFree(ta_codes);
+  cudaFree(tb_codes);
   return st;
 }
 

@@ -62,26 +62,48 @@ def workload(name: str, T=None, seed: int = 0, weight_seed=None):
     return synthetic.make_workload(name, T=T, seed=seed, weight_seed=weight_seed)
 
 
-class LazyQuantWeights:
-    """Oracle weight quantization of only the experts that are asked for."""
+_POOL = None
 
-    def __init__(self, w: torch.Tensor):
-        self.w = w
-        self.cache = {}
 
-    def expert(self, e: int):
-        if e not in self.cache:
-            self.cache[e] = onv.quantize_tensor(omoe.as_f32(self.w[e]))
-        return self.cache[e]
+def _pool():
+    # spawn, never fork: the parent may already hold a CUDA context
+    global _POOL
+    if _POOL is None:
+        import concurrent.futures as cf
+        import multiprocessing as mp
+        import os as _os
 
-    def full(self, experts) -> omoe.QuantWeights:
-        E, N, Kd = self.w.shape
-        codes = np.zeros((E, N, Kd), np.uint8)
-        sf = np.zeros((E, N, Kd // 16), np.uint8)
-        gs = np.ones(E, np.float32)
-        for e in experts:
-            codes[e], sf[e], gs[e] = self.expert(int(e))
-        return omoe.QuantWeights(codes, sf, gs)
+        _POOL = cf.ProcessPoolExecutor(max_workers=max(1, min(16, (_os.cpu_count() or 2) - 1)),
+                                       mp_context=mp.get_context("spawn"))
+    return _POOL
+
+
+def quantize_experts(w: torch.Tensor, experts) -> omoe.QuantWeights:
+    """Oracle quantization of the listed experts of w [E, N, K] (others left
+    zero with gs = 1), one expert per worker process."""
+    E, N, Kd = w.shape
+    codes = np.zeros((E, N, Kd), np.uint8)
+    sf = np.zeros((E, N, Kd // 16), np.uint8)
+    gs = np.ones(E, np.float32)
+    experts = [int(e) for e in experts]
+    arrays = [omoe.as_f32(w[e]) for e in experts]
+    if len(experts) <= 1:
+        results = [onv.quantize_tensor(a) for a in arrays]
+    else:
+        # workers import only the oracle's numpy code
+        results = list(_pool().map(onv.quantize_tensor, arrays))
+    for e, (c, s_, g) in zip(experts, results):
+        codes[e], sf[e], gs[e] = c, s_, g
+    return omoe.QuantWeights(codes, sf, gs)
+
+
+def oracle_route(wl, tokens=None):
+    x = omoe.as_f32(wl.x)
+    tok = np.arange(x.shape[0]) if tokens is None else np.asarray(tokens)
+    bias = None if wl.bias is None else wl.bias.numpy()
+    logits = omoe.router_logits(x[tok], omoe.as_f32(wl.gate_w), bias)
+    ids, w = omoe.topk_route(logits, wl.shape.K)
+    return logits, ids, w
 
 
 def oracle_forward(wl, tokens=None):
@@ -90,13 +112,17 @@ def oracle_forward(wl, tokens=None):
     x = omoe.as_f32(wl.x)
     wg = omoe.as_f32(wl.gate_w)
     bias = None if wl.bias is None else wl.bias.numpy()
-    tok = np.arange(x.shape[0]) if tokens is None else np.asarray(tokens)
-    logits = omoe.router_logits(x[tok], wg, bias)
-    ids, _ = omoe.topk_route(logits, wl.shape.K)
+    _, ids, _ = oracle_route(wl, tokens)
     experts = np.unique(ids)
-    q13 = LazyQuantWeights(wl.w13).full(experts)
-    q2 = LazyQuantWeights(wl.w2).full(experts)
+    q13 = quantize_experts(wl.w13, experts)
+    q2 = quantize_experts(wl.w2, experts)
     return omoe.moe_forward(x, wg, q13, q2, wl.shape.K, bias, tokens=tokens)
+
+
+def sample_tokens(T: int, n: int, extra=()):
+    """n evenly spread token indices (always the first and last) plus extras."""
+    base = np.linspace(0, T - 1, min(n, T)).astype(np.int64)
+    return np.unique(np.concatenate([base, np.asarray(list(extra), dtype=np.int64)]))
 
 
 def to_dev(wl, dev="cuda:0"):

@@ -1,0 +1,211 @@
+"""GPU parity at the full workload sizes, through the C ABI.
+
+* decode (T=64, H=2048, E=128, top-8, I=768) captured in a CUDA graph and
+  replayed;
+* speculative-decode batch (T=256) with Zipf-skewed routing in deterministic
+  mode, bitwise identical over 10 runs;
+* prefill on one instance sized for 4096 tokens, forwards of 1, 17, 2048, 4073
+  and 4096 tokens, and a refused 4097-token forward;
+* per-token-scale stress (T=2048, H=4096, E=64, top-6, I=1536) with an
+  in-place weight reload under a captured graph, compared with a fresh
+  instance.
+
+Bit-exact: router logits and top-k ids (all tokens where the oracle router
+runs on all of them, else the sampled tokens), the permutation and expert
+offsets, activation codes / block scales / global scales, weight codes / block
+scales / global scales (sampled experts).  Outputs of sampled tokens within
+the parity tolerance.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import synthetic
+from oracle import moe as omoe
+from oracle import nvfp4 as onv
+from tests.parity import (assert_close, built, gpu, needs_gpu, oracle_forward, oracle_route, quantize_experts,
+                          sample_tokens, to_dev)
+
+pytestmark = [gpu, needs_gpu]
+
+
+def _layer(shape, **kw):
+    from nvfp4_token_quantized_gb300 import MoE
+
+    built()
+    return MoE.from_shape(shape, device=0, **kw)
+
+
+def _check_routing(layer, wl, tokens=None, full_permutation=False):
+    logits_ref, ids_ref, w_ref = oracle_route(wl, tokens)
+    tok = np.arange(wl.T) if tokens is None else np.asarray(tokens)
+    logits = layer.debug_logits().cpu().numpy()[tok]
+    assert np.array_equal(logits.view(np.uint32), logits_ref.view(np.uint32)), "router logits differ"
+    r = layer.debug_routing()
+    ids = r["topk_ids"].cpu().numpy()
+    assert np.array_equal(ids[tok], ids_ref), "top-k ids differ"
+    np.testing.assert_allclose(r["topk_w"].cpu().numpy()[tok], w_ref, rtol=3e-6, atol=1e-7)
+    if full_permutation:
+        off, src, _ = omoe.permute(ids_ref, wl.shape.E)
+        assert np.array_equal(r["expert_offsets"].cpu().numpy(), off)
+        assert np.array_equal(r["src_of_row"].cpu().numpy(), src)
+    return ids_ref, r
+
+
+def _check_act_quant(layer, wl, tokens):
+    codes, sf, gs = (t.cpu().numpy() for t in layer.debug_act_quant())
+    rc, rs, rg = onv.quantize_rows(omoe.as_f32(wl.x)[tokens])
+    assert np.array_equal(codes[tokens], onv.pack_e2m1(rc))
+    assert np.array_equal(sf[tokens], rs)
+    assert np.array_equal(gs[tokens].view(np.uint32), rg.view(np.uint32))
+
+
+def _check_weight_quant(layer, wl, experts):
+    q13 = quantize_experts(wl.w13, experts)
+    q2 = quantize_experts(wl.w2, experts)
+    for which, q in ((0, q13), (1, q2)):
+        codes, sf, gs = (t.cpu().numpy() for t in layer.debug_weight_quant(which))
+        for e in experts:
+            assert np.array_equal(codes[e], onv.pack_e2m1(q.codes[e])), f"weight codes {which} expert {e}"
+            assert np.array_equal(sf[e], q.sf[e]), f"weight block scales {which} expert {e}"
+            assert gs[e] == q.gs[e], f"weight global scale {which} expert {e}"
+
+
+def _check_output(out, wl, tokens, what):
+    ref = oracle_forward(wl, tokens)
+    got = out.float().cpu().numpy()[tokens]
+    return assert_close(got, ref.out, what=what)
+
+
+def test_decode_graph_replay():
+    wl = synthetic.make_workload("c1_decode")
+    d = to_dev(wl)
+    layer = _layer(wl.shape)
+    layer.load_weights(d["w13"], d["w2"])
+    out = torch.empty_like(d["x"])
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        layer.forward(d["x"], d["gate_w"], out=out)
+    torch.cuda.synchronize()
+    eager = out.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        layer.forward(d["x"], d["gate_w"], out=out)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    replay = out.clone()
+    _check_routing(layer, wl, full_permutation=True)
+    tokens = sample_tokens(wl.T, 8)
+    _check_act_quant(layer, wl, tokens)
+    _check_output(replay, wl, tokens, "graph replay")
+    _check_output(eager, wl, tokens, "eager")
+    _check_weight_quant(layer, wl, [0, 77, 127])
+    layer.close()
+
+
+def test_specdecode_deterministic_zipf():
+    wl = synthetic.make_workload("c2_specdecode")
+    d = to_dev(wl)
+    layer = _layer(wl.shape)
+    assert layer.deterministic
+    layer.load_weights(d["w13"], d["w2"])
+    outs = [layer.forward(d["x"], d["gate_w"], bias=d["bias"]).clone() for _ in range(10)]
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16)), "deterministic mode differs between runs"
+    ids, r = _check_routing(layer, wl, full_permutation=True)
+    counts = np.diff(r["expert_offsets"].cpu().numpy())
+    assert (counts == 0).sum() >= 4, "skewed routing should leave experts without rows"
+    assert counts.max() > 4 * counts.mean()
+    tokens = sample_tokens(wl.T, 8)
+    _check_output(outs[0], wl, tokens, "zipf deterministic")
+
+
+def test_prefill_token_sweep_one_instance():
+    from nvfp4_token_quantized_gb300 import MoEError
+
+    shape = synthetic.CONFIGS["c3_prefill"]
+    wl = synthetic.make_workload(shape, T=1)
+    gate = wl.gate_w.cuda()
+    layer = _layer(shape)
+    layer.load_weights(wl.w13.cuda(), wl.w2.cuda())
+    ptrs = layer.debug_buffer_ptrs()
+    for T in (1, 17, 2048, 4073, 4096):
+        # new activations for every token count, the instance's weights
+        xT = synthetic.make_activations(shape, T=T, seed=T)
+        wlT = synthetic.Workload(shape=shape, x=xT, gate_w=wl.gate_w, w13=wl.w13, w2=wl.w2, bias=None)
+        out = layer.forward(xT.cuda(), gate)
+        torch.cuda.synchronize()
+        assert torch.isfinite(out.float()).all()
+        tokens = sample_tokens(T, 3)
+        if T == 4096:  # the whole batch: every token's route and the full permutation
+            _check_routing(layer, wlT, None, full_permutation=True)
+        else:
+            _check_routing(layer, wlT, tokens)
+        _check_output(out, wlT, tokens, f"T={T}")
+    assert layer.debug_buffer_ptrs() == ptrs, "a forward moved a device buffer"
+    with pytest.raises(MoEError) as ei:
+        layer.forward(torch.zeros(4097, shape.H, dtype=torch.bfloat16, device="cuda"), gate)
+    assert ei.value.status == 2  # MOE_ERR_TOO_MANY_TOKENS
+    layer.close()
+
+
+def test_stress_refresh_replay_equals_fresh():
+    from nvfp4_token_quantized_gb300 import MoEError
+
+    shape = synthetic.CONFIGS["c4_stress"]
+    wl = synthetic.make_workload(shape)
+    w13_b, w2_b = synthetic.make_weights(shape, seed=shape.refresh_seed)
+    x, gate = wl.x.cuda(), wl.gate_w.cuda()
+    layer = _layer(shape)
+    assert layer.deterministic
+    layer.load_weights(wl.w13.cuda(), wl.w2.cuda())
+    out = torch.empty_like(x)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        layer.forward(x, gate, out=out)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        layer.forward(x, gate, out=out)
+    g.replay()
+    torch.cuda.synchronize()
+    before = out.clone()
+    ptrs = layer.debug_buffer_ptrs()
+
+    w13_b_dev, w2_b_dev = w13_b.cuda(), w2_b.cuda()
+    layer.refresh_scales_inplace(w13_b_dev, w2_b_dev)
+    g.replay()
+    torch.cuda.synchronize()
+    refreshed = out.clone()
+    assert layer.debug_buffer_ptrs() == ptrs, "refresh moved a device buffer"
+    assert not torch.equal(refreshed, before)
+
+    fresh = _layer(shape)
+    fresh.load_weights(w13_b_dev, w2_b_dev)
+    expect = fresh.forward(x, gate)
+    torch.cuda.synchronize()
+    assert torch.equal(refreshed.view(torch.int16), expect.view(torch.int16)), "replay after refresh != fresh load"
+    fresh.close()
+
+    # changed metadata is refused and leaves the loaded weights in place
+    with pytest.raises(MoEError) as ei:
+        layer.refresh_scales_inplace(w13_b_dev[:, :-128].contiguous(), w2_b_dev)
+    assert ei.value.status == 4  # MOE_ERR_METADATA_CHANGED
+
+    # zero rows stay exactly zero; sampled rows (zero, smallest and largest
+    # norms, and a spread) match the oracle with the reloaded weights
+    xf = wl.x.float()
+    norms = xf.norm(dim=1)
+    zero = torch.nonzero(norms == 0).flatten()
+    assert zero.numel() == synthetic.workloads.expected_zero_rows(shape, wl.T)
+    assert torch.count_nonzero(refreshed[zero.cuda()]) == 0
+    nz = torch.nonzero(norms > 0).flatten()
+    extra = [int(zero[0]), int(nz[norms[nz].argmin()]), int(nz[norms[nz].argmax()])]
+    tokens = sample_tokens(wl.T, 4, extra)
+    wl_b = synthetic.Workload(shape=shape, x=wl.x, gate_w=wl.gate_w, w13=w13_b, w2=w2_b, bias=None)
+    _check_output(refreshed, wl_b, tokens, "stress after refresh")
+    _check_weight_quant(layer, wl_b, [0, 63])
+    layer.close()
