@@ -26,22 +26,43 @@ constexpr int SF_ATOM_BYTES = 512;  // block scales of 128 rows x 64 K-elements
 constexpr int DEV_ERR_TIMEOUT = 1;
 constexpr int DEV_ERR_BAD_STATE = 2;
 
-// Byte offset of packed code byte kb (elements 2kb, 2kb+1) of `row` in the
-// tiled operand layout: tiles of 128 rows x 128 bytes (256 elements of K),
-// each one contiguous 16 KB block, ordered [row / 128][kb / 128].  A pipeline
-// stage of a GEMM then reads one contiguous block per operand tile.
-__host__ __device__ __forceinline__ size_t operand_offset(size_t row, int kb, int row_bytes) {
-  const int stages = row_bytes >> 7;
-  return (((row >> 7) * stages + (size_t)(kb >> 7)) * 128 + (row & 127)) * 128 + (kb & 127);
+// Operand layout of every FP4 GEMM operand (activations, intermediate,
+// weights): tiles of 128 rows x 256 elements of K, each one contiguous
+// 18 KB block [2 KB block scales | 16 KB codes], ordered [row / 128][K / 256].
+//  - the block scales of the tile are four "128x4 atoms" of 512 bytes (one
+//    per 64 elements of K): the scale of row r, 16-element block j of the
+//    atom at (r % 32) * 16 + (r / 32) * 4 + j - the layout the tensor cores
+//    read after a 32x128b.warpx4 copy into tensor memory;
+//  - the codes are 128 rows x 128 bytes (two E2M1 codes per byte, element
+//    2i in the low nibble) already in the 128-byte-swizzled order the tensor
+//    cores read from shared memory: 16-byte chunk c of row r at chunk
+//    c ^ (r % 8).
+// A pipeline stage then fetches a whole weight tile, scales included, with
+// one linear bulk copy.  Codes and scales of an operand live in one buffer;
+// both offsets below are relative to its base.
+constexpr int OPERAND_SF_BYTES = 4 * 512;
+constexpr int OPERAND_CODE_BYTES = 128 * 128;
+constexpr int OPERAND_TILE_BYTES = OPERAND_SF_BYTES + OPERAND_CODE_BYTES;
+
+// Bytes of an operand of `rows` rows (a multiple of 128) and row_bytes packed
+// code bytes per row (a multiple of 128).
+__host__ __device__ __forceinline__ size_t operand_bytes(size_t rows, int row_bytes) {
+  return (rows >> 7) * (size_t)(row_bytes >> 7) * OPERAND_TILE_BYTES;
 }
 
-// Byte offset of the block scale of (row, k16) in the "128x4 atom" layout the
-// tensor cores read: atoms of 128 rows x 4 block scales (64 K-elements), 512
-// bytes each; row r of an atom at (r%32)*16 + (r/32)*4, block j at +j.
-// Atoms are ordered [row / 128][k16 / 4].
-__host__ __device__ __forceinline__ size_t sf_atom_offset(int row, int k16, int k16_per_row) {
-  const int atoms_per_rowblock = k16_per_row / 4;
-  return ((size_t)(row >> 7) * atoms_per_rowblock + (k16 >> 2)) * SF_ATOM_BYTES +
+// Offset of packed code byte kb (elements 2kb, 2kb+1) of `row`.
+__host__ __device__ __forceinline__ size_t operand_offset(size_t row, int kb, int row_bytes) {
+  const int stages = row_bytes >> 7;
+  const int r = (int)(row & 127), b = kb & 127;
+  return ((row >> 7) * stages + (size_t)(kb >> 7)) * OPERAND_TILE_BYTES + OPERAND_SF_BYTES + (size_t)r * 128 +
+         ((((b >> 4) ^ r) & 7) << 4) + (b & 15);
+}
+
+// Offset of the E4M3 block scale of (row, 16-element block k16) of an
+// operand with k16_per_row blocks per row, in the layout above.
+__host__ __device__ __forceinline__ size_t sf_atom_offset(size_t row, int k16, int k16_per_row) {
+  const int stages = k16_per_row >> 4;
+  return ((row >> 7) * stages + (size_t)(k16 >> 4)) * OPERAND_TILE_BYTES + (size_t)((k16 >> 2) & 3) * SF_ATOM_BYTES +
          (size_t)((row & 31) * 16 + ((row >> 5) & 3) * 4 + (k16 & 3));
 }
 

@@ -51,16 +51,16 @@ cudaError_t launch_finalize_ordered(const float* ybuf, const float* topk_w, void
 
 // ---- block-scaled FP4 GEMMs (kernels_gemm.cu) ----
 struct GemmArgs {
-  const uint8_t* a_sf;        // A block scales, 128x4 atoms
-  const uint8_t* b_sf;        // B block scales, 128x4 atoms
+  const uint8_t* a_codes;     // A operand (codes and block scales), operand layout
+  const uint8_t* b_codes;     // B operand (codes and block scales), operand layout
   int k_stages;               // Kpad / 256
-  int kblocks;                // Kpad / 64
   const int4* tiles;          // {expert, first padded row, valid rows, 0}
   const int32_t* num_tiles;   // device tile count
   int b_rows_per_expert;      // 2I (w13) or H (w2)
   const float* gs_rows;       // global scale per padded A row
   const float* gs_w;          // global scale per expert
-  // w13 epilogue: SwiGLU + requantization into the w2 operand
+  // w13 epilogue: SwiGLU + requantization into the w2 operand (codes and
+  // block scales share one operand buffer)
   uint8_t* h_codes;
   uint8_t* h_sf;
   float* h_gs;
@@ -89,11 +89,8 @@ int gemm_w13_max_clusters(int w13_chunks, int a_rows);
 // CTAs; the w2 / plain kernels run n_ctas CTAs.  Each walks a static tile list.
 // a_rows: rows of the activation operand per tile (32 or 128; every tile of
 // the list must have at most that many valid rows).
-cudaError_t launch_gemm_w13(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int n_chunks,
-                            int n_clusters, int a_rows, cudaStream_t s);
-cudaError_t launch_gemm_w2(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int n_ctas,
-                           bool ordered, int a_rows, cudaStream_t s);
-cudaError_t launch_gemm_plain(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int n_ctas,
-                              cudaStream_t s);
+cudaError_t launch_gemm_w13(const GemmArgs& a, int n_chunks, int n_clusters, int a_rows, cudaStream_t s);
+cudaError_t launch_gemm_w2(const GemmArgs& a, int n_ctas, bool ordered, int a_rows, cudaStream_t s);
+cudaError_t launch_gemm_plain(const GemmArgs& a, int n_ctas, cudaStream_t s);
 
 }  // namespace moe

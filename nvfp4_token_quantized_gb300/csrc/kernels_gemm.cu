@@ -4,9 +4,11 @@
 //
 // Persistent kernels.  A work unit is one 128-row x 128-column MMA tile of
 // one expert; each CTA (w2, plain) or cluster (w13) walks a static list.
-//   warp 0      TMA producer: A rows (only a unit's valid rows), B rows and
-//               both block-scale tiles into a STAGES-deep shared-memory ring,
-//               running ahead across unit boundaries;
+//   warp 0      producer: per 256-element K stage, two bulk copies into a
+//               STAGES-deep shared-memory ring - the B tile (its 2 KB of
+//               block scales and 16 KB of pre-swizzled codes are one
+//               contiguous 18 KB block) and the A tile's scales plus its
+//               valid rows - running ahead across unit boundaries;
 //   warp 1      tensor-memory allocation and the single MMA-issuing thread:
 //               block scales shared -> tensor memory (tcgen05.cp), then four
 //               K=64 MMAs per 256-element stage, into one of two accumulator
@@ -47,15 +49,12 @@ namespace moe {
 
 namespace {
 
-constexpr int B_STAGE = TILE_N * 128;        // 16 KB: 128 rows x 128 bytes
-constexpr int SFA_STAGE = 4 * SF_ATOM_BYTES; // 2 KB: 128 rows x 16 scales
-constexpr int SFB_STAGE = 4 * SF_ATOM_BYTES; // 2 KB: 128 rows x 16 scales
+constexpr int B_SLOT = OPERAND_TILE_BYTES;   // 18 KB: [scales | 128 rows x 128 bytes]
 constexpr int MAX_STAGES = 8;
 // Activation rows reserved per stage: 128, or 32 for small batches.  The MMA
 // always reads 128 rows; with 32 reserved, rows 32..127 read the next stages'
 // data (or the tail pad after the last stage) - in bounds, and their results
 // are never used because such tiles have at most 32 valid rows.
-constexpr int A_BOX_ROWS = 32;
 constexpr int TMEM_COLS = 512;
 constexpr int TMEM_SF_BASE = 2 * TILE_N;     // two accumulator buffers in columns [0, 256)
 constexpr int TMEM_SF_STAGE = 32;            // 16 columns SFA + 16 columns SFB per stage
@@ -78,11 +77,10 @@ struct Ctrl {
 };
 static_assert(sizeof(Ctrl) <= CTRL_BYTES, "control block too large");
 
-__host__ __device__ constexpr int a_stage_bytes(int a_rows) { return a_rows * 128; }
+// A slot: [2 KB scales | a_rows x 128 bytes of codes]
+__host__ __device__ constexpr int a_slot_bytes(int a_rows) { return OPERAND_SF_BYTES + a_rows * 128; }
 __host__ __device__ constexpr int a_tail_bytes(int a_rows) { return (TILE_M - a_rows) * 128; }
-__host__ __device__ constexpr int stage_bytes(int a_rows) {
-  return a_stage_bytes(a_rows) + B_STAGE + SFA_STAGE + SFB_STAGE;
-}
+__host__ __device__ constexpr int stage_bytes(int a_rows) { return a_slot_bytes(a_rows) + B_SLOT; }
 __host__ __device__ constexpr int smem_bytes_for(int stages, int nch, int a_rows) {
   return stages * stage_bytes(a_rows) + a_tail_bytes(a_rows) + CTRL_BYTES + 2 * nch * TILE_M * 4 + 1024;
 }
@@ -103,16 +101,13 @@ struct Unit {
 };
 
 template <int MODE, int A_ROWS, int STAGES>
-__global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA,
-                                                             const __grid_constant__ CUtensorMap tmB, GemmArgs p) {
-  constexpr int A_STAGE = a_stage_bytes(A_ROWS);
+__global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_constant__ GemmArgs p) {
+  constexpr int A_SLOT = a_slot_bytes(A_ROWS);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = base;
-  uint8_t* sB = sA + STAGES * A_STAGE + a_tail_bytes(A_ROWS);
-  uint8_t* sSFA = sB + STAGES * B_STAGE;
-  uint8_t* sSFB = sSFA + STAGES * SFA_STAGE;
-  Ctrl& c = *reinterpret_cast<Ctrl*>(sSFB + STAGES * SFB_STAGE);
+  uint8_t* sA = base;                                          // [STAGES][A_SLOT] + tail
+  uint8_t* sB = sA + STAGES * A_SLOT + a_tail_bytes(A_ROWS);   // [STAGES][B_SLOT]
+  Ctrl& c = *reinterpret_cast<Ctrl*>(sB + STAGES * B_SLOT);
   // [2][nch][128] words: partial row maximum bits (non-negative, so bit 31
   // is free) with bit 31 holding the m-tile tag
   uint32_t* part = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(&c) + CTRL_BYTES);
@@ -166,8 +161,6 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
     if (MODE == MODE_W13)
       for (int i = 0; i < 2 * nch * TILE_M; ++i) part[i] = 0x80000000u;  // tag of no first use
     fence_mbarrier_init();
-    prefetch_tensormap(&tmA);
-    prefetch_tensormap(&tmB);
   }
   if (warp == 1) {
     tmem_alloc(&c.tmem_base, TMEM_COLS);
@@ -188,17 +181,16 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer ----------------
-      const uint64_t pol_w = policy_evict_first();
-      const uint64_t pol_a = policy_evict_last();
+      // ---------------- producer ----------------
       uint32_t g = 0;  // stages issued so far (ring position)
       for (int u = first; u < nunits && !c.abort_flag; u = next(u)) {
         const Unit un = unit_at(u);
         const int brow0 = (MODE == MODE_PLAIN ? 0 : un.e * p.b_rows_per_expert) + un.col * TILE_N;
-        const int a_boxes = (un.valid + A_BOX_ROWS - 1) / A_BOX_ROWS;
-        const uint32_t bytes = a_boxes * A_BOX_ROWS * 128 + B_STAGE + SFA_STAGE + SFB_STAGE;
-        const uint8_t* sfa_src = p.a_sf + ((size_t)(un.row0 >> 7) * p.kblocks) * SF_ATOM_BYTES;
-        const uint8_t* sfb_src = p.b_sf + ((size_t)(brow0 >> 7) * p.kblocks) * SF_ATOM_BYTES;
+        // scales + valid rows, in whole 8-row swizzle groups
+        const uint32_t a_bytes = OPERAND_SF_BYTES + (uint32_t)((un.valid + 7) & ~7) * 128;
+        const uint32_t bytes = a_bytes + B_SLOT;
+        const uint8_t* a_src = p.a_codes + (size_t)(un.row0 >> 7) * KS * OPERAND_TILE_BYTES;
+        const uint8_t* b_src = p.b_codes + (size_t)(brow0 >> 7) * KS * OPERAND_TILE_BYTES;
         for (int ks = 0; ks < KS; ++ks, ++g) {
           const int s = g % STAGES;
           if (!mbar_wait_bounded(&c.empty[s], ((g / STAGES) & 1) ^ 1, &c.abort_flag)) {
@@ -207,14 +199,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
             break;
           }
           mbar_arrive_expect_tx(&c.full[s], bytes);
-          // operands are tiled: tile (row block, stage) is rows
-          // ((row / 128) * KS + ks) * 128 + row % 128 of a 128-byte-wide tensor
-          const int ya = ((un.row0 >> 7) * KS + ks) * TILE_M + (un.row0 & 127);
-          for (int i = 0; i < a_boxes; ++i)
-            tma_load_2d(sA + s * A_STAGE + i * A_BOX_ROWS * 128, &tmA, &c.full[s], 0, ya + i * A_BOX_ROWS, pol_a);
-          tma_load_2d(sB + s * B_STAGE, &tmB, &c.full[s], 0, ((brow0 >> 7) * KS + ks) * TILE_N, pol_w);
-          bulk_load(sSFA + s * SFA_STAGE, sfa_src + (size_t)ks * SFA_STAGE, SFA_STAGE, &c.full[s]);
-          bulk_load(sSFB + s * SFB_STAGE, sfb_src + (size_t)ks * SFB_STAGE, SFB_STAGE, &c.full[s]);
+          bulk_load(sA + s * A_SLOT, a_src + (size_t)ks * OPERAND_TILE_BYTES, a_bytes, &c.full[s]);
+          bulk_load(sB + s * B_SLOT, b_src + (size_t)ks * OPERAND_TILE_BYTES, B_SLOT, &c.full[s]);
         }
       }
       if (c.abort_flag) {
@@ -250,13 +236,15 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
           tc_fence_after();
           const uint32_t sfa_t = tmem + TMEM_SF_BASE + s * TMEM_SF_STAGE;
           const uint32_t sfb_t = sfa_t + 16;
+          const uint8_t* slot_a = sA + s * A_SLOT;
+          const uint8_t* slot_b = sB + s * B_SLOT;
 #pragma unroll
           for (int kb = 0; kb < 4; ++kb) {
-            tc_copy_sf(sfa_t + kb * 4, smem_desc_sf(smem_u32(sSFA + s * SFA_STAGE + kb * SF_ATOM_BYTES)));
-            tc_copy_sf(sfb_t + kb * 4, smem_desc_sf(smem_u32(sSFB + s * SFB_STAGE + kb * SF_ATOM_BYTES)));
+            tc_copy_sf(sfa_t + kb * 4, smem_desc_sf(smem_u32(slot_a + kb * SF_ATOM_BYTES)));
+            tc_copy_sf(sfb_t + kb * 4, smem_desc_sf(smem_u32(slot_b + kb * SF_ATOM_BYTES)));
           }
-          const uint32_t a_base = smem_u32(sA + s * A_STAGE);
-          const uint32_t b_base = smem_u32(sB + s * B_STAGE);
+          const uint32_t a_base = smem_u32(slot_a + OPERAND_SF_BYTES);
+          const uint32_t b_base = smem_u32(slot_b + OPERAND_SF_BYTES);
 #pragma unroll
           for (int kb = 0; kb < 4; ++kb)
             tc_mma_fp4(d_tmem, smem_desc_sw128(a_base + kb * 32), smem_desc_sw128(b_base + kb * 32), IDESC,
@@ -479,12 +467,11 @@ cudaLaunchConfig_t make_cfg(dim3 grid, int nch, cudaStream_t s, cudaLaunchAttrib
 }
 
 template <int MODE, int A_ROWS, int STAGES>
-cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, dim3 grid, int nch,
-                   cudaStream_t s) {
+cudaError_t launch(const GemmArgs& a, dim3 grid, int nch, cudaStream_t s) {
   cudaLaunchAttribute attr[2];
   // The expert GEMMs always follow another kernel of the same forward.
   cudaLaunchConfig_t cfg = make_cfg<MODE, A_ROWS, STAGES>(grid, nch, s, attr, MODE != MODE_PLAIN);
-  return cudaLaunchKernelEx(&cfg, gemm_fp4_kernel<MODE, A_ROWS, STAGES>, tmA, tmB, a);
+  return cudaLaunchKernelEx(&cfg, gemm_fp4_kernel<MODE, A_ROWS, STAGES>, a);
 }
 
 // Ring depths that occur: w2 / plain kernels (no exchange slots) and w13
@@ -542,28 +529,25 @@ int gemm_w13_max_clusters(int nch, int a_rows) {
   return n;
 }
 
-cudaError_t launch_gemm_w13(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int n_chunks,
-                            int n_clusters, int a_rows, cudaStream_t s) {
+cudaError_t launch_gemm_w13(const GemmArgs& a, int n_chunks, int n_clusters, int a_rows, cudaStream_t s) {
   const dim3 grid(n_chunks, n_clusters, 1);
   return with_w13(n_chunks, a_rows, [&](auto ar, auto st) {
-    return launch<MODE_W13, decltype(ar)::value, decltype(st)::value>(tmA, tmB, a, grid, n_chunks, s);
+    return launch<MODE_W13, decltype(ar)::value, decltype(st)::value>(a, grid, n_chunks, s);
   });
 }
 
-cudaError_t launch_gemm_w2(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int n_ctas,
-                           bool ordered, int a_rows, cudaStream_t s) {
+cudaError_t launch_gemm_w2(const GemmArgs& a, int n_ctas, bool ordered, int a_rows, cudaStream_t s) {
   const dim3 grid(n_ctas, 1, 1);
   if (a_rows == 32) {
-    if (ordered) return launch<MODE_W2_ORDERED, 32, W2_STAGES_32>(tmA, tmB, a, grid, 0, s);
-    return launch<MODE_W2_ATOMIC, 32, W2_STAGES_32>(tmA, tmB, a, grid, 0, s);
+    if (ordered) return launch<MODE_W2_ORDERED, 32, W2_STAGES_32>(a, grid, 0, s);
+    return launch<MODE_W2_ATOMIC, 32, W2_STAGES_32>(a, grid, 0, s);
   }
-  if (ordered) return launch<MODE_W2_ORDERED, 128, W2_STAGES_128>(tmA, tmB, a, grid, 0, s);
-  return launch<MODE_W2_ATOMIC, 128, W2_STAGES_128>(tmA, tmB, a, grid, 0, s);
+  if (ordered) return launch<MODE_W2_ORDERED, 128, W2_STAGES_128>(a, grid, 0, s);
+  return launch<MODE_W2_ATOMIC, 128, W2_STAGES_128>(a, grid, 0, s);
 }
 
-cudaError_t launch_gemm_plain(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int n_ctas,
-                              cudaStream_t s) {
-  return launch<MODE_PLAIN, 128, W2_STAGES_128>(tmA, tmB, a, dim3(n_ctas, 1, 1), 0, s);
+cudaError_t launch_gemm_plain(const GemmArgs& a, int n_ctas, cudaStream_t s) {
+  return launch<MODE_PLAIN, 128, W2_STAGES_128>(a, dim3(n_ctas, 1, 1), 0, s);
 }
 
 }  // namespace moe

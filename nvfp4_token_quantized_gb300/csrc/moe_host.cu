@@ -7,13 +7,10 @@
 // a larger forward is refused with MOE_ERR_TOO_MANY_TOKENS.  Weight reload
 // rewrites the same buffers ("CuTe DSL backend gets per-token NVFP4 online
 // quantization and reload", Implementation item 3 and the refresh snippet).
-#include <cudaTypedefs.h>
-
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
-#include <mutex>
 #include <string>
 #include <vector>
 
@@ -66,7 +63,6 @@ struct moe_handle {
   int* status_host = nullptr;
   int* status_dev = nullptr;
 
-  CUtensorMap tm_a1{}, tm_b1{}, tm_a2{}, tm_b2{};
 
   // stage timing: events[0] before the first kernel, events[i+1] after stage i
   bool timing = false;
@@ -111,50 +107,6 @@ moe_status dalloc(moe_handle* h, T** p, size_t bytes) {
   h->allocs.push_back(q);
   h->bytes += bytes;
   *p = reinterpret_cast<T*>(q);
-  return MOE_OK;
-}
-
-PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-// Tensor map of an operand in the tiled layout (tiles of 128 rows x 128
-// bytes, contiguous): a 128-byte-wide tensor of rows * row_bytes / 128 rows,
-// boxes of box_rows rows, 128-byte swizzle (the K-major operand layout of the
-// FP4 MMAs).
-moe_status make_operand_map(moe_handle* h, CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows,
-                            uint32_t box_rows) {
-  auto fn = get_encode_fn();
-  if (!fn) {
-    set_err(h, "cuTensorMapEncodeTiled is not available from the driver");
-    return MOE_ERR_CUDA;
-  }
-  if (rows % 128 || row_bytes % 128) {
-    set_err(h, "operand of %llu rows x %llu bytes is not whole 128x128 tiles", (unsigned long long)rows,
-            (unsigned long long)row_bytes);
-    return MOE_ERR_INVALID_ARG;
-  }
-  cuuint64_t dims[2] = {128, rows * (row_bytes / 128)};
-  cuuint64_t strides[1] = {128};
-  cuuint32_t box[2] = {128, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    set_err(h, "cuTensorMapEncodeTiled failed (%d)", (int)r);
-    return MOE_ERR_CUDA;
-  }
   return MOE_OK;
 }
 
@@ -287,10 +239,9 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
     g.tiles = h->tiles;
     g.num_tiles = h->num_tiles;
     // w13: A = expanded activations [Rpad, H], B = w13 [E*2I, H]
-    g.a_sf = h->a_sf;
-    g.b_sf = h->w13_sf;
+    g.a_codes = h->a_codes;
+    g.b_codes = h->w13_codes;
     g.k_stages = H / STAGE_K;
-    g.kblocks = H / MMA_K;
     g.b_rows_per_expert = 2 * h->I;
     g.gs_rows = h->gs_rows;
     g.gs_w = h->gs_w13;
@@ -298,18 +249,16 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
     g.h_sf = h->h_sf;
     g.h_gs = h->h_gs;
     g.i_pad = h->Ipad;
-    CK(h, launch_gemm_w13(h->tm_a1, h->tm_b1, g, h->I / 128, std::min(h->w13_clusters[tile_rows == 128], tb),
-                          tile_rows, s));
+    CK(h, launch_gemm_w13(g, h->I / 128, std::min(h->w13_clusters[tile_rows == 128], tb), tile_rows, s));
     CK(h, mark(h, 5, s));
     // w2: A = requantized intermediate [Rpad, Ipad], B = w2 [E*H, Ipad]
     GemmArgs g2{};
     g2.status = h->status_dev;
     g2.tiles = h->tiles;
     g2.num_tiles = h->num_tiles;
-    g2.a_sf = h->h_sf;
-    g2.b_sf = h->w2_sf;
+    g2.a_codes = h->h_codes;
+    g2.b_codes = h->w2_codes;
     g2.k_stages = h->Ipad / STAGE_K;
-    g2.kblocks = h->Ipad / MMA_K;
     g2.b_rows_per_expert = H;
     g2.gs_rows = h->h_gs;
     g2.gs_w = h->gs_w2;
@@ -320,8 +269,7 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
     g2.ybuf = h->ybuf;
     g2.hidden = H;
     g2.n_tiles = H / TILE_N;
-    CK(h, launch_gemm_w2(h->tm_a2, h->tm_b2, g2, std::min(h->num_sms, tb * g2.n_tiles), h->deterministic, tile_rows,
-                         s));
+    CK(h, launch_gemm_w2(g2, std::min(h->num_sms, tb * g2.n_tiles), h->deterministic, tile_rows, s));
     CK(h, mark(h, 6, s));
     if (h->deterministic) CK(h, launch_finalize_ordered(h->ybuf, h->topk_w, out, T, H, K, s));
     else CK(h, launch_finalize_atomic(h->out_acc, out, T, H, s));
@@ -392,10 +340,11 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
     if (s_ != MOE_OK) return fail(s_);               \
   } while (0)
   const size_t Rp = h->Rpad;
-  A(h->w13_codes, (size_t)E * 2 * I * (H / 2));
-  A(h->w13_sf, (size_t)E * 2 * I * (H / 16));
-  A(h->w2_codes, (size_t)E * H * (h->Ipad / 2));
-  A(h->w2_sf, (size_t)E * H * (h->Ipad / 16));
+  // FP4 operands: codes and block scales interleaved per tile in one buffer
+  A(h->w13_codes, operand_bytes((size_t)E * 2 * I, H / 2));
+  h->w13_sf = h->w13_codes;
+  A(h->w2_codes, operand_bytes((size_t)E * H, h->Ipad / 2));
+  h->w2_sf = h->w2_codes;
   A(h->gs_w13, sizeof(float) * E);
   A(h->gs_w2, sizeof(float) * E);
   A(h->amax_bits, sizeof(uint32_t) * 2 * E);
@@ -410,11 +359,11 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
   A(h->src_of_padrow, sizeof(int32_t) * Rp);
   A(h->tiles, sizeof(int4) * (size_t)h->tile_cap);
   A(h->num_tiles, sizeof(int32_t) * 4);
-  A(h->a_codes, Rp * (H / 2));
-  A(h->a_sf, Rp * (H / 16));
+  A(h->a_codes, operand_bytes(Rp, H / 2));
+  h->a_sf = h->a_codes;
   A(h->gs_rows, sizeof(float) * Rp);
-  A(h->h_codes, Rp * (h->Ipad / 2));
-  A(h->h_sf, Rp * (h->Ipad / 16));
+  A(h->h_codes, operand_bytes(Rp, h->Ipad / 2));
+  h->h_sf = h->h_codes;
   A(h->h_gs, sizeof(float) * Rp);
   if (h->deterministic) A(h->ybuf, sizeof(float) * (size_t)h->Rmax * H);
   else A(h->out_acc, sizeof(float) * (size_t)T * H);
@@ -430,13 +379,6 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
     e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&h->status_dev), h->status_host, 0);
     if (e != cudaSuccess) return fail(cuda_fail(h, e, "cudaHostGetDevicePointer"));
   }
-  moe_status st;
-  if ((st = make_operand_map(h, &h->tm_a1, h->a_codes, H / 2, Rp, 32)) != MOE_OK) return fail(st);
-  if ((st = make_operand_map(h, &h->tm_b1, h->w13_codes, H / 2, (uint64_t)E * 2 * I, TILE_N)) != MOE_OK)
-    return fail(st);
-  if ((st = make_operand_map(h, &h->tm_a2, h->h_codes, h->Ipad / 2, Rp, 32)) != MOE_OK) return fail(st);
-  if ((st = make_operand_map(h, &h->tm_b2, h->w2_codes, h->Ipad / 2, (uint64_t)E * H, TILE_N)) != MOE_OK)
-    return fail(st);
   {
     cudaError_t e = gemm_setup_attributes(I / 128);
     if (e != cudaSuccess) return fail(cuda_fail(h, e, "cudaFuncSetAttribute"));
@@ -701,25 +643,16 @@ moe_status moe_debug_block_scaled_gemm(const uint8_t* a_codes, const uint8_t* a_
   if (M <= 0 || N <= 0 || K <= 0 || M % 128 || N % 128 || K % 256) return MOE_ERR_UNSUPPORTED;
   if (!aligned16(a_codes) || !aligned16(b_codes) || !aligned16(d)) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  uint8_t *sfa = nullptr, *sfb = nullptr;
-  moe_handle tmp;  // error sink only
-  if (cudaMalloc(&sfa, (size_t)M * K / 16) != cudaSuccess) return MOE_ERR_CUDA;
-  if (cudaMalloc(&sfb, (size_t)N * K / 16) != cudaSuccess) {
-    cudaFree(sfa);
-    return MOE_ERR_CUDA;
-  }
-  uint8_t *ta_codes = nullptr, *tb_codes = nullptr;
+  // canonical codes / scales -> the interleaved operand layout
+  uint8_t *opa = nullptr, *opb = nullptr;
   moe_status st = MOE_OK;
-  if (cudaMalloc(&ta_codes, (size_t)M * K / 2) != cudaSuccess || cudaMalloc(&tb_codes, (size_t)N * K / 2) != cudaSuccess)
+  if (cudaMalloc(&opa, operand_bytes(M, K / 2)) != cudaSuccess || cudaMalloc(&opb, operand_bytes(N, K / 2)) != cudaSuccess)
     st = MOE_ERR_CUDA;
-  CUtensorMap ta, tb;
-  if (st == MOE_OK && (launch_sf_to_atoms(a_sf, M, K / 16, sfa, s) != cudaSuccess ||
-                       launch_sf_to_atoms(b_sf, N, K / 16, sfb, s) != cudaSuccess ||
-                       launch_codes_to_tiled(a_codes, M, K / 2, ta_codes, s) != cudaSuccess ||
-                       launch_codes_to_tiled(b_codes, N, K / 2, tb_codes, s) != cudaSuccess))
+  if (st == MOE_OK && (launch_sf_to_atoms(a_sf, M, K / 16, opa, s) != cudaSuccess ||
+                       launch_sf_to_atoms(b_sf, N, K / 16, opb, s) != cudaSuccess ||
+                       launch_codes_to_tiled(a_codes, M, K / 2, opa, s) != cudaSuccess ||
+                       launch_codes_to_tiled(b_codes, N, K / 2, opb, s) != cudaSuccess))
     st = MOE_ERR_CUDA;
-  if (st == MOE_OK) st = make_operand_map(&tmp, &ta, ta_codes, K / 2, M, 32);
-  if (st == MOE_OK) st = make_operand_map(&tmp, &tb, tb_codes, K / 2, N, TILE_N);
   if (st == MOE_OK && gemm_setup_attributes(1) != cudaSuccess) st = MOE_ERR_CUDA;
   int dev = 0, sms = 0;
   if (st == MOE_OK && (cudaGetDevice(&dev) != cudaSuccess ||
@@ -727,21 +660,18 @@ moe_status moe_debug_block_scaled_gemm(const uint8_t* a_codes, const uint8_t* a_
     st = MOE_ERR_CUDA;
   if (st == MOE_OK) {
     GemmArgs g{};
-    g.a_sf = sfa;
-    g.b_sf = sfb;
+    g.a_codes = opa;
+    g.b_codes = opb;
     g.k_stages = K / STAGE_K;
-    g.kblocks = K / MMA_K;
     g.d = d;
     g.ldd = N;
     g.n_tiles = N / TILE_N;
     g.m_tiles = M / TILE_M;
-    if (launch_gemm_plain(ta, tb, g, std::min(sms, g.n_tiles * g.m_tiles), s) != cudaSuccess) st = MOE_ERR_CUDA;
+    if (launch_gemm_plain(g, std::min(sms, g.n_tiles * g.m_tiles), s) != cudaSuccess) st = MOE_ERR_CUDA;
   }
   if (cudaStreamSynchronize(s) != cudaSuccess) st = MOE_ERR_CUDA;
-  cudaFree(sfa);
-  cudaFree(sfb);
-  cudaFree(ta_codes);
-  cudaFree(tb_codes);
+  cudaFree(opa);
+  cudaFree(opb);
   return st;
 }
 
