@@ -9,7 +9,9 @@
 namespace moe {
 
 // ---- routing (kernels_route.cu) ----
-cudaError_t router_setup(int H, int E);  // shared-memory attribute of the router kernel
+// Raises the router kernel's dynamic shared-memory cap to what (H, E) needs;
+// never lowers it (the cap is shared by every handle on the device).
+cudaError_t router_setup(int H, int E);
 // Also clears counts[E] for the top-k kernel.
 cudaError_t launch_router_logits(const void* x, const void* gate_w, const float* bias, float* logits, int T,
                                  int H, int E, int32_t* counts, cudaStream_t s);

@@ -40,6 +40,7 @@
 // memory -78%" (Motivation); the per-token scales follow "CuTe DSL backend
 // gets per-token NVFP4 online quantization and reload" (Implementation
 // item 2).
+#include <mutex>
 #include <type_traits>
 
 #include "common.cuh"
@@ -431,11 +432,17 @@ constexpr int stages_for(int nch, int a_rows) {
   return 0;
 }
 
+// The shared-memory cap belongs to the kernel instantiation, which handles of
+// different widths share: it is only ever raised.
 template <int MODE, int A_ROWS, int STAGES>
 cudaError_t set_attrs(int nch) {
   auto k = gemm_fp4_kernel<MODE, A_ROWS, STAGES>;
-  cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         smem_bytes_for(STAGES, nch, A_ROWS));
+  const int bytes = smem_bytes_for(STAGES, nch, A_ROWS);
+  cudaFuncAttributes fa{};
+  cudaError_t err = cudaFuncGetAttributes(&fa, k);
+  if (err != cudaSuccess) return err;
+  if (fa.maxDynamicSharedSizeBytes < bytes)
+    err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (err != cudaSuccess) return err;
   if (MODE == MODE_W13) err = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   return err;
@@ -500,6 +507,8 @@ cudaError_t with_w13(int nch, int a_rows, F&& f) {
 int gemm_smem_bytes() { return smem_bytes_for(W2_STAGES_128, 0, 128); }
 
 cudaError_t gemm_setup_attributes(int nch) {
+  static std::mutex m;
+  std::lock_guard<std::mutex> lock(m);
   cudaError_t e;
   for (int a_rows : {32, 128}) {
     e = with_w13(nch, a_rows, [&](auto ar, auto st) {

@@ -8,6 +8,8 @@
 // same order.  The permutation groups rows by expert and keeps token order
 // inside an expert, and pads each GEMM tile of an expert to its own 128-row
 // block for the tensor-core GEMMs.
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -378,27 +380,37 @@ int router_eb(int H, int E) {
 // Small batches: two tokens per warp with all activations prefetched.
 bool router_small(int T, int H) { return T <= 512 && H <= 2048; }
 
+// Raises (never lowers) the dynamic shared-memory cap of one router
+// instantiation to `bytes`.  The cap belongs to the kernel, not to a handle,
+// so a handle with a narrower hidden size must not shrink it under another.
 template <int TB, int EB, bool XALL>
-cudaError_t set_router_attr(int H) {
+cudaError_t raise_router_attr(int bytes) {
+  cudaFuncAttributes a{};
+  cudaError_t e = cudaFuncGetAttributes(&a, router_logits_kernel<TB, EB, XALL>);
+  if (e != cudaSuccess || a.maxDynamicSharedSizeBytes >= bytes) return e;
   return cudaFuncSetAttribute(router_logits_kernel<TB, EB, XALL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              H * EB * 2);
+                              bytes);
 }
+
+std::mutex router_attr_mutex;
 
 }  // namespace
 
 cudaError_t router_setup(int H, int E) {
   const int eb = router_eb(H, E);
+  const int bytes = H * eb * 2;
+  std::lock_guard<std::mutex> lock(router_attr_mutex);
   cudaError_t e;
   if (eb == 32) {
-    if ((e = set_router_attr<4, 32, false>(H)) != cudaSuccess) return e;
-    return set_router_attr<2, 32, true>(H);
+    if ((e = raise_router_attr<4, 32, false>(bytes)) != cudaSuccess) return e;
+    return raise_router_attr<2, 32, true>(bytes);
   }
   if (eb == 16) {
-    if ((e = set_router_attr<4, 16, false>(H)) != cudaSuccess) return e;
-    return set_router_attr<2, 16, true>(H);
+    if ((e = raise_router_attr<4, 16, false>(bytes)) != cudaSuccess) return e;
+    return raise_router_attr<2, 16, true>(bytes);
   }
-  if ((e = set_router_attr<4, 8, false>(H)) != cudaSuccess) return e;
-  return set_router_attr<4, 8, true>(H);
+  if ((e = raise_router_attr<4, 8, false>(bytes)) != cudaSuccess) return e;
+  return raise_router_attr<4, 8, true>(bytes);
 }
 
 cudaError_t launch_router_logits(const void* x, const void* gate_w, const float* bias, float* logits, int T,

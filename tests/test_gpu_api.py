@@ -96,3 +96,27 @@ def test_hardware_conversion_of_the_worked_examples():
     assert e2.cpu().tolist() == [0x7, 0x5, 0x3, 0x2, 0x0, 0x8, 0xA, 0xC, 0x6, 0x4, 0x2, 0x0, 0xF, 0xD, 0x6, 0x2]
     _, e4 = moe_debug_convert(torch.tensor([448.0, 37.333333, 2.0 ** -10, 0.0013020833], device="cuda"))
     assert e4.cpu().tolist() == [0x7E, 0x61, 0x00, 0x01]
+
+
+def test_narrower_handle_leaves_wider_one_working():
+    # kernel launch limits are per kernel, not per handle: creating a handle
+    # with a smaller hidden and intermediate size must not break the forward
+    # of a wider handle created before it
+    import dataclasses
+
+    from nvfp4_token_quantized_gb300 import MoE
+
+    built()
+    wide = dataclasses.replace(synthetic.CONFIGS["c0_tiny"], name="wide", H=1024, I=512, deterministic=True)
+    wl = synthetic.make_workload(wide)
+    d = to_dev(wl)
+    a = MoE.from_shape(wide, device=0)
+    a.load_weights(d["w13"], d["w2"])
+    before = a.forward(d["x"], d["gate_w"]).clone()
+    narrow = dataclasses.replace(wide, name="narrow", H=256, I=128)
+    b = MoE.from_shape(narrow, device=0)
+    after = a.forward(d["x"], d["gate_w"])
+    torch.cuda.synchronize()
+    assert torch.equal(before.view(torch.int16), after.view(torch.int16))
+    b.close()
+    a.close()
