@@ -192,6 +192,54 @@ MOE_API moe_status moe_get_stage_times(const moe_handle* h, float* ms, int* n);
 MOE_API const char* moe_stage_name(int i);
 
 /* ---------------------------------------------------------------------------
+ * Routing without a handle and without allocation.  The method described on
+ * the pages has no counterpart: this is a library convenience.
+ *
+ * For callers that must not allocate device memory when they route: a
+ * runtime whose memory pool already holds all free device memory (a
+ * cudaMalloc there fails), or a step that cannot afford the device-wide
+ * synchronisation a cudaMalloc/cudaFree implies.  Such callers have no
+ * moe_handle to hold a workspace, so the intermediate router logits and the
+ * per-expert row counters live in one fixed array in the library's device
+ * code: MOE_ROUTE_NOALLOC_MAX_LOGITS floats of logits plus 256 counters
+ * (about 4 MiB per device, reserved when the library's device code is loaded
+ * on that device).  Nothing is allocated by this call, by CUDA or otherwise.
+ *
+ * Computes exactly the routing of moe_forward_ex on the same inputs (the same
+ * kernels): FP32 router logits in the canonical order, plus gate_bias if not
+ * NULL; top-k by logit, ties to the lower expert id; softmax over all
+ * experts, chosen weights renormalised.
+ *   x:         [num_tokens, hidden] bf16, device, 16-byte aligned.
+ *   gate_w:    [hidden, num_experts] bf16, device, 16-byte aligned.
+ *   gate_bias: [num_experts] f32, device, 16-byte aligned, or NULL.
+ *   topk_ids:  [num_tokens, top_k] int32, written (slot order = descending
+ *              logit).
+ *   topk_w:    [num_tokens, top_k] f32, written.
+ * Runs on the calling thread's current device, which must hold every
+ * pointer; enqueued on `stream` (NULL = legacy default stream) with no host
+ * synchronisation.  All buffers are the caller's.
+ *
+ * Limits and errors: hidden % 256 == 0, num_experts % 8 == 0,
+ * num_experts <= 256, 1 <= top_k <= min(num_experts, 16), otherwise
+ * MOE_ERR_UNSUPPORTED; num_tokens * num_experts above
+ * MOE_ROUTE_NOALLOC_MAX_LOGITS returns MOE_ERR_TOO_MANY_TOKENS (split the
+ * batch); NULL or misaligned pointers MOE_ERR_INVALID_ARG; a device other
+ * than sm_103 MOE_ERR_UNSUPPORTED; num_tokens == 0 does nothing.
+ *
+ * The first call on each device does that device's set-up (looks up the
+ * array's device address and raises the router kernel's launch limits), so
+ * make one call on each device before any stream capture.  The array is
+ * shared by every call on the device: calls whose device work overlaps
+ * (different streams, or threads without ordering between them) race on it
+ * and corrupt each other's results; order them on one stream.
+ * ------------------------------------------------------------------------ */
+#define MOE_ROUTE_NOALLOC_MAX_LOGITS (1 << 20) /* num_tokens * num_experts, e.g. 8192 x 128 */
+
+MOE_API moe_status moe_route_noalloc(const void* x, const void* gate_w, const float* gate_bias, int num_tokens,
+                                     int hidden, int num_experts, int top_k, int32_t* topk_ids, float* topk_w,
+                                     void* stream);
+
+/* ---------------------------------------------------------------------------
  * Parity exports.  Each copies state left by the LAST moe_forward on the
  * handle (or by the last load/refresh for the weights) into caller device
  * buffers, in canonical row-major layouts, on `stream`.  T below is that

@@ -25,4 +25,5 @@ from .binding import (  # noqa: F401
     moe_get_workspace_bytes,
     moe_load_weights,
     moe_refresh_scales_inplace,
+    moe_route_noalloc,
 )

@@ -34,8 +34,9 @@ EXPORTED = (
     "moe_status_string", "moe_get_status", "moe_debug_routing", "moe_debug_logits",
     "moe_debug_act_quant", "moe_debug_weight_quant", "moe_debug_intermediate", "moe_debug_buffer_ptrs",
     "moe_debug_convert", "moe_debug_block_scaled_gemm", "moe_set_stage_timing", "moe_get_stage_times",
-    "moe_stage_name",
+    "moe_stage_name", "moe_route_noalloc",
 )
+MOE_ROUTE_NOALLOC_MAX_LOGITS = 1 << 20
 MOE_NUM_STAGES = 7
 
 
@@ -96,6 +97,7 @@ def load_library() -> ctypes.CDLL:
         "moe_set_stage_timing": (I, [P, I]),
         "moe_get_stage_times": (I, [P, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(I)]),
         "moe_stage_name": (ctypes.c_char_p, [I]),
+        "moe_route_noalloc": (I, [P, P, P, I, I, I, I, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -219,6 +221,30 @@ def moe_debug_block_scaled_gemm(a_codes, a_sf, b_codes, b_sf, M: int, N: int, K:
     if st != MOE_OK:
         raise MoEError(st, "moe_debug_block_scaled_gemm")
     return d
+
+
+def moe_route_noalloc(x: torch.Tensor, gate_w: torch.Tensor, top_k: int, bias: Optional[torch.Tensor] = None,
+                      topk_ids: Optional[torch.Tensor] = None, topk_w: Optional[torch.Tensor] = None,
+                      stream=None):
+    """Routing (logits, top-k, renormalised weights) with no handle and no
+    device allocation inside the library call.  ``topk_ids`` (int32 [T, K])
+    and ``topk_w`` (float32 [T, K]) may be passed in to be filled; otherwise
+    they are created here, before the call.  The current CUDA device must be
+    the one holding the tensors."""
+    T, H = x.shape
+    E = gate_w.shape[1]
+    if topk_ids is None:
+        topk_ids = torch.empty(T, top_k, dtype=torch.int32, device=x.device)
+    if topk_w is None:
+        topk_w = torch.empty(T, top_k, dtype=torch.float32, device=x.device)
+    st = load_library().moe_route_noalloc(_ptr(x), _ptr(gate_w), _ptr(bias), T, H, E, top_k, _ptr(topk_ids),
+                                          _ptr(topk_w), _stream(stream))
+    if st != MOE_OK:
+        what = f"moe_route_noalloc(T={T}, H={H}, E={E}, K={top_k})"
+        if st == MOE_ERR_TOO_MANY_TOKENS:
+            what += f": T*E = {T * E} exceeds the fixed scratch of {MOE_ROUTE_NOALLOC_MAX_LOGITS} logits"
+        raise MoEError(st, what)
+    return topk_ids, topk_w
 
 
 class MoE:

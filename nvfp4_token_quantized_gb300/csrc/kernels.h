@@ -12,6 +12,10 @@ namespace moe {
 // Raises the router kernel's dynamic shared-memory cap to what (H, E) needs;
 // never lowers it (the cap is shared by every handle on the device).
 cudaError_t router_setup(int H, int E);
+// Raises the cap of every router instantiation to `bytes` (never lowers it).
+cudaError_t router_setup_max(int bytes);
+// Dynamic shared memory one router launch for (H, E) needs.
+int router_smem_bytes(int H, int E);
 // Also clears counts[E] for the top-k kernel.
 cudaError_t launch_router_logits(const void* x, const void* gate_w, const float* bias, float* logits, int T,
                                  int H, int E, int32_t* counts, cudaStream_t s);

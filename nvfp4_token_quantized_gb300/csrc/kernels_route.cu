@@ -413,6 +413,19 @@ cudaError_t router_setup(int H, int E) {
   return raise_router_attr<4, 8, true>(bytes);
 }
 
+cudaError_t router_setup_max(int bytes) {
+  std::lock_guard<std::mutex> lock(router_attr_mutex);
+  cudaError_t e;
+  if ((e = raise_router_attr<4, 32, false>(bytes)) != cudaSuccess) return e;
+  if ((e = raise_router_attr<2, 32, true>(bytes)) != cudaSuccess) return e;
+  if ((e = raise_router_attr<4, 16, false>(bytes)) != cudaSuccess) return e;
+  if ((e = raise_router_attr<2, 16, true>(bytes)) != cudaSuccess) return e;
+  if ((e = raise_router_attr<4, 8, false>(bytes)) != cudaSuccess) return e;
+  return raise_router_attr<4, 8, true>(bytes);
+}
+
+int router_smem_bytes(int H, int E) { return H * router_eb(H, E) * 2; }
+
 cudaError_t launch_router_logits(const void* x, const void* gate_w, const float* bias, float* logits, int T,
                                  int H, int E, int32_t* counts, cudaStream_t s) {
   const int eb = router_eb(H, E);
