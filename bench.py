@@ -281,6 +281,33 @@ def layer_alg_bytes(s, T, touched):
 # Our implementation
 # --------------------------------------------------------------------------
 
+def workload_config(s, T, world):
+    return {"workload": f"{s.name}: T={T} H={s.H} E={s.E} top-{s.K} I={s.I}, CUDA-graph replay",
+            "T": T, "H": s.H, "E": s.E, "top_k": s.K, "I": s.I,
+            "finalize": "ordered (deterministic)" if s.deterministic else "fp32 atomic",
+            "l2": "flushed before every step (256 MB write, outside the timed events)",
+            "parallelism": f"replicas x{world}"}
+
+
+def max_over_ranks(values, world):
+    """Element-wise maximum of per-rank timings over all replicas (gloo group;
+    no collective touches the data path)."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def replica_throughput(tokens_per_replica, world, ms_per_step):
+    """Whole-job tokens/s: every replica processes its own batch each step, and
+    the step time is the slowest replica's."""
+    return tokens_per_replica * world / (ms_per_step / 1e3)
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -383,18 +410,13 @@ def run_ours(args, rank, world, local_rank):
     h2d = xh.numel() * 2 + gh.numel() * 2 + (0 if bh is None else bh.numel() * 4)
     d2h = oh.numel() * 2
 
-    if world > 1:
-        t = torch.tensor([total_ms, sum(e2e_s)], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, e2e_total = float(t[0]), float(t[1])
-    else:
-        e2e_total = sum(e2e_s)
+    total_ms, e2e_total = max_over_ranks([total_ms, sum(e2e_s)], world)
     if rank != 0:
         layer.close()
         return None
 
     ms_per_step = total_ms / args.steps
-    value = T * world / (ms_per_step / 1e3)
+    value = replica_throughput(T, world, ms_per_step)
     mean_stage = {k: statistics.mean(v) for k, v in stages.items() if v}
     dom = max(mean_stage, key=mean_stage.get)
     alg = stage_alg_bytes(s, T, touched)
@@ -415,12 +437,7 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "nvfp4 (e2m1 x e2m1 with e4m3 block scales, fp32 accumulate)",
         "data": "synthetic (seeded bf16 N(0,1) activations, N(0,0.02) router/expert weights)",
-        "config": {"workload": f"{s.name}: T={T} H={s.H} E={s.E} top-{s.K} I={s.I}, "
-                               "CUDA-graph replay",
-                   "T": T, "H": s.H, "E": s.E, "top_k": s.K, "I": s.I,
-                   "finalize": "ordered (deterministic)" if s.deterministic else "fp32 atomic",
-                   "l2": "flushed before every step (256 MB write, outside the timed events)",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(s, T, world),
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs",
                      "alg_bytes_per_launch": alg[dom], "launch_ms": mean_stage[dom],
@@ -457,7 +474,7 @@ def main():
         line = {"impl": "reference", "metric": METRIC, "value": r["value"], "unit": "tokens/s", "n_gpus": 1,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["seconds_per_step"] * 1e3,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
-                "data": "synthetic", "config": {"workload": f"{s.name} (oracle on a token sample)"},
+                "data": "synthetic", "config": workload_config(s, s.T if args.tokens is None else args.tokens, 1),
                 "cpu_baseline": {k: r[k] for k in ("value", "unit", "cores", "kind", "sample")},
                 "e2e": {"value": r["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))

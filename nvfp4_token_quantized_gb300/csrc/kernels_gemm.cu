@@ -24,9 +24,11 @@
 //        units) of an m-tile and keeps their SwiGLU values in registers.
 //        The row's absolute maximum over all I features is combined across
 //        the I/128 CTAs of a thread-block cluster: every CTA stores its partial
-//        maximum, tagged with the m-tile's sequence number in the same 64-bit
-//        word, into every peer's shared memory, and each thread polls its own
-//        row's slots until all tags match - no barrier or fence on the path.
+//        maximum (a non-negative float, so bit 31 is free) as one 32-bit word
+//        into every peer's shared memory; successive m-tiles alternate
+//        between two slot buffers, and bit 31 flips between successive uses
+//        of a buffer, so each thread polls its own row's slots until every
+//        tag matches - no barrier or fence on the path.
 //        Each CTA then requantizes its 128 features with the row's global
 //        scale: the per-row NVFP4 input of the w2 GEMM, written without a
 //        round trip of the FP32 intermediate through HBM.
