@@ -182,6 +182,12 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint
       : "memory");
 }
 
+// Hint: bring `bytes` (a multiple of 16, 16-byte aligned) of global memory
+// into L2 without a destination or completion.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* gsrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -388,6 +394,17 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_
 }
 
 __device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
+// Arrival on a grid-wide completion counter: an atomic add with
+// acquire-release semantics at GPU scope.  Called by one thread right after a
+// CTA barrier, it publishes everything the CTA wrote before the barrier, and
+// (followed by another barrier) makes everything earlier arrivals published
+// visible to the whole CTA.  Returns the counter's previous value.
+__device__ __forceinline__ uint32_t arrive_acq_rel_gpu(uint32_t* counter) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
+  return old;
+}
 
 // Barrier among `nthreads` threads (whole warps) on hardware barrier `id`.
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {

@@ -27,10 +27,10 @@ struct PermuteOut {
   int32_t* row_of_src;      // [R]
   int32_t* pad_row_of_src;  // [R]
   int32_t* src_of_padrow;   // [Rpad]
-  int4* tiles;              // [tile bound] {expert, first padded row, valid rows, 0}
+  int4* tiles;              // [tile bound] {expert, first padded row, valid rows, first activation row}
   int32_t* num_tiles;       // [1]
 };
-// tile_rows: 32 (small batches) or 128 rows per GEMM tile.
+// tile_rows: 128 rows per GEMM tile.
 cudaError_t launch_permute(const int32_t* topk_ids, const int32_t* counts, int T, int K, int E, int tile_rows,
                            const PermuteOut& o, cudaStream_t s);
 
@@ -56,14 +56,48 @@ cudaError_t launch_finalize_ordered(const float* ybuf, const float* topk_w, void
                                     cudaStream_t s);
 
 // ---- block-scaled FP4 GEMMs (kernels_gemm.cu) ----
+// Small batches (T <= SMALL_BATCH_TOKENS): router logits, per-token
+// quantization, top-k and the expert grouping in one kernel.  Every token is
+// quantized once into one shared activation tile (row t = token t), which
+// every expert's w13 GEMM reads; the expanded row (token t, slot j) of expert
+// e is padded row e*128 + t.
+constexpr int SMALL_BATCH_TOKENS = 64;
+struct FrontArgs {
+  const void* x;              // [T, H] bf16
+  const void* gate_w;         // [H, E] bf16
+  const float* bias;          // [E] or nullptr
+  int T, H, E, K;
+  float* logits;              // [T, E]
+  int32_t* topk_ids;          // [T, K]
+  float* topk_w;              // [T, K]
+  uint8_t* a_codes;           // shared activation tile (operand layout, rows 0..T-1)
+  float* gs_rows;             // [T] per-token global scales
+  float* out_acc;             // [T, H] cleared here (atomic finalize), or nullptr
+  int32_t* src_of_padrow;     // [E*128]
+  int32_t* expert_offsets;    // [E+1]
+  int32_t* src_of_row;        // [T*K]
+  int32_t* row_of_src;        // [T*K]
+  int32_t* pad_row_of_src;    // [T*K]
+  int4* tiles;                // one tile per expert with rows
+  int32_t* num_tiles;
+  uint32_t* sync;             // FRONT_SYNC_WORDS counters, zero between launches
+};
+constexpr int FRONT_SYNC_WORDS = 64;
+cudaError_t front_setup(int H, int E);
+cudaError_t launch_front_small(const FrontArgs& a, cudaStream_t s);
+
 struct GemmArgs {
   const uint8_t* a_codes;     // A operand (codes and block scales), operand layout
   const uint8_t* b_codes;     // B operand (codes and block scales), operand layout
   int k_stages;               // Kpad / 256
-  const int4* tiles;          // {expert, first padded row, valid rows, 0}
+  // {expert, first padded row, valid rows, first activation row}.  The padded
+  // row indexes the outputs (intermediate, scales, src_of_padrow); the w13
+  // GEMM reads its activation rows from the fourth field, which equals the
+  // second in the expanded layout and is 0 in the shared small-batch tile.
+  const int4* tiles;
   const int32_t* num_tiles;   // device tile count
   int b_rows_per_expert;      // 2I (w13) or H (w2)
-  const float* gs_rows;       // global scale per padded A row
+  const float* gs_rows;       // global scale per activation row
   const float* gs_w;          // global scale per expert
   // w13 epilogue: SwiGLU + requantization into the w2 operand (codes and
   // block scales share one operand buffer)
@@ -71,8 +105,10 @@ struct GemmArgs {
   uint8_t* h_sf;
   float* h_gs;
   int i_pad;                  // K of the w2 GEMM (padded intermediate width)
-  // w2 epilogue: top-k weighted reduction
+  // padded row -> token * top_k + slot, or -1 for a row no token routed here
+  // (both epilogues skip such rows)
   const int32_t* src_of_padrow;
+  // w2 epilogue: top-k weighted reduction
   const float* topk_w;
   int top_k;
   float* out_acc;             // atomic mode
@@ -84,6 +120,17 @@ struct GemmArgs {
   int n_tiles;                // 128-column tiles per row tile (w2 / plain)
   int m_tiles;                // row tiles (plain)
   int* status;                // device status word
+  // Before its dependency wait, each CTA may warm L2 with the weights of its
+  // first prefetch_units work units, taking tile i to be expert i's (exact in
+  // the small-batch layout when every expert has rows; only a hint).
+  int prefetch_units;
+  int num_experts;
+  // small-batch w13 without clusters: column pairs per m-tile (I/128), the
+  // FP32 SwiGLU rows [padded row][i_pad] and the per-row maxima (zero on
+  // entry; the requantization kernel returns them to zero)
+  int w13_pairs;
+  float* hbuf;
+  float* row_amax;
 };
 
 int gemm_smem_bytes();
@@ -93,9 +140,17 @@ cudaError_t gemm_setup_attributes(int w13_chunks);
 int gemm_w13_max_clusters(int w13_chunks, int a_rows);
 // Persistent launches: the w13 kernel runs n_clusters clusters of n_chunks
 // CTAs; the w2 / plain kernels run n_ctas CTAs.  Each walks a static tile list.
-// a_rows: rows of the activation operand per tile (32 or 128; every tile of
+// a_rows: rows of the activation operand per tile (64 or 128; every tile of
 // the list must have at most that many valid rows).
 cudaError_t launch_gemm_w13(const GemmArgs& a, int n_chunks, int n_clusters, int a_rows, cudaStream_t s);
+// Small batches (64-row tiles sharing one activation tile): the w13 GEMM
+// without clusters over n_ctas CTAs, then the per-row requantization of its
+// FP32 output into the w2 operand.  resident keeps the shared activation tile
+// in shared memory for the whole kernel (K <= 2048).
+cudaError_t launch_gemm_w13s(const GemmArgs& a, int n_ctas, bool resident, cudaStream_t s);
+cudaError_t launch_requant_rows(const float* hbuf, float* row_amax, const int32_t* src_of_padrow, const int4* tiles,
+                                const int32_t* num_tiles, int max_tiles, int I, int i_pad, uint8_t* h_codes,
+                                float* h_gs, cudaStream_t s);
 cudaError_t launch_gemm_w2(const GemmArgs& a, int n_ctas, bool ordered, int a_rows, cudaStream_t s);
 cudaError_t launch_gemm_plain(const GemmArgs& a, int n_ctas, cudaStream_t s);
 

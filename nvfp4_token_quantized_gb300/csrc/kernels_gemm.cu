@@ -54,10 +54,10 @@ namespace {
 
 constexpr int B_SLOT = OPERAND_TILE_BYTES;   // 18 KB: [scales | 128 rows x 128 bytes]
 constexpr int MAX_STAGES = 8;
-// Activation rows reserved per stage: 128, or 32 for small batches.  The MMA
-// always reads 128 rows; with 32 reserved, rows 32..127 read the next stages'
+// Activation rows reserved per stage: 128, or 64 for small batches.  The MMA
+// always reads 128 rows; with 64 reserved, rows 64..127 read the next stages'
 // data (or the tail pad after the last stage) - in bounds, and their results
-// are never used because such tiles have at most 32 valid rows.
+// are never used because such tiles have at most 64 valid rows.
 constexpr int TMEM_COLS = 512;
 constexpr int TMEM_SF_BASE = 2 * TILE_N;     // two accumulator buffers in columns [0, 256)
 constexpr int TMEM_SF_STAGE = 32;            // 16 columns SFA + 16 columns SFB per stage
@@ -68,13 +68,18 @@ constexpr int CTRL_BYTES = 256;
 constexpr int MAX_SMEM = 232448;
 static_assert(TMEM_SF_BASE + MAX_STAGES * TMEM_SF_STAGE <= TMEM_COLS, "tensor memory overflow");
 
-enum Mode { MODE_W13 = 0, MODE_W2_ATOMIC = 1, MODE_W2_ORDERED = 2, MODE_PLAIN = 3 };
+// MODE_W13S: the small-batch w13 GEMM without clusters - its epilogue writes
+// the FP32 SwiGLU rows and folds each row's absolute maximum into a global
+// word; a separate kernel requantizes (the same arithmetic as MODE_W13's
+// fused requantization).
+enum Mode { MODE_W13 = 0, MODE_W2_ATOMIC = 1, MODE_W2_ORDERED = 2, MODE_PLAIN = 3, MODE_W13S = 4 };
 
 struct Ctrl {
   uint64_t full[MAX_STAGES];
   uint64_t empty[MAX_STAGES];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
+  uint64_t a_full;  // resident activations loaded (resident-A kernels)
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -86,6 +91,14 @@ __host__ __device__ constexpr int a_tail_bytes(int a_rows) { return (TILE_M - a_
 __host__ __device__ constexpr int stage_bytes(int a_rows) { return a_slot_bytes(a_rows) + B_SLOT; }
 __host__ __device__ constexpr int smem_bytes_for(int stages, int nch, int a_rows) {
   return stages * stage_bytes(a_rows) + a_tail_bytes(a_rows) + CTRL_BYTES + 2 * nch * TILE_M * 4 + 1024;
+}
+// Resident activations (the small-batch w13 GEMM, whose tiles all read the
+// same shared activation tile): all K stages of A stay in shared memory for
+// the whole kernel, loaded once; the ring carries only weight tiles.
+constexpr int ARES_MAX_KS = 8;  // K <= 2048
+__host__ __device__ constexpr int smem_bytes_res(int stages, int nch, int a_rows) {
+  return ARES_MAX_KS * a_slot_bytes(a_rows) + a_tail_bytes(a_rows) + stages * B_SLOT + CTRL_BYTES +
+         2 * nch * TILE_M * 4 + 1024;
 }
 
 __device__ __forceinline__ float swiglu(float g_acc, float u_acc, float alpha) {
@@ -101,15 +114,17 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 
 struct Unit {
   int e, row0, valid, col;  // expert, first padded row, valid rows, 128-column block of B
+  int arow;                 // first row of the activation operand
 };
 
-template <int MODE, int A_ROWS, int STAGES>
+template <int MODE, int A_ROWS, int STAGES, bool ARES>
 __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_constant__ GemmArgs p) {
   constexpr int A_SLOT = a_slot_bytes(A_ROWS);
+  constexpr int A_SLOTS = ARES ? ARES_MAX_KS : STAGES;  // resident: one slot per K stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = base;                                          // [STAGES][A_SLOT] + tail
-  uint8_t* sB = sA + STAGES * A_SLOT + a_tail_bytes(A_ROWS);   // [STAGES][B_SLOT]
+  uint8_t* sA = base;                                          // [A_SLOTS][A_SLOT] + tail
+  uint8_t* sB = sA + A_SLOTS * A_SLOT + a_tail_bytes(A_ROWS);  // [STAGES][B_SLOT]
   Ctrl& c = *reinterpret_cast<Ctrl*>(sB + STAGES * B_SLOT);
   // [2][nch][128] words: partial row maximum bits (non-negative, so bit 31
   // is free) with bit 31 holding the m-tile tag
@@ -121,32 +136,43 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
   // w13: cluster blockIdx.y takes m-tiles blockIdx.y, +gridDim.y, ...; CTA
   //      rank r of the cluster takes units (m-tile, B column blocks 2r, 2r+1).
   // w2 / plain: CTA b takes units b, b + gridDim.x, ... of (m-tile, n-tile).
-  const int nch = (MODE == MODE_W13) ? (int)gridDim.x : 1;
+  // w13s: CTA b takes unit pairs b, b + gridDim.x, ... of (m-tile, column
+  //      pair r), pair index = m-tile * (I/128) + r.
+  constexpr bool W13L = (MODE == MODE_W13 || MODE == MODE_W13S);  // units in column pairs
+  const int nch = (MODE == MODE_W13) ? (int)gridDim.x : (MODE == MODE_W13S ? p.w13_pairs : 1);
   const uint32_t rank = (MODE == MODE_W13) ? blockIdx.x : 0;
   pdl_trigger();
   int first, stride;
   if constexpr (MODE == MODE_W13) {
     first = 2 * blockIdx.y;
     stride = 2 * gridDim.y;
+  } else if constexpr (MODE == MODE_W13S) {
+    first = 2 * blockIdx.x;
+    stride = 2 * gridDim.x;
   } else {
     first = blockIdx.x;
     stride = gridDim.x;
   }
   // w13 units come in pairs (2 per m-tile); `next` skips to the next pair.
   auto next = [&](int u) -> int {
-    if constexpr (MODE == MODE_W13) return (u & 1) ? u - 1 + stride : u + 1;
+    if constexpr (W13L) return (u & 1) ? u - 1 + stride : u + 1;
     else return u + stride;
   };
   auto unit_at = [&](int u) -> Unit {
     Unit r;
     if constexpr (MODE == MODE_W13) {
       const int4 ti = p.tiles[u >> 1];
-      r.e = ti.x; r.row0 = ti.y; r.valid = ti.z; r.col = 2 * (int)rank + (u & 1);
+      r.e = ti.x; r.row0 = ti.y; r.valid = ti.z; r.col = 2 * (int)rank + (u & 1); r.arow = ti.w;
+    } else if constexpr (MODE == MODE_W13S) {
+      const int pair = u >> 1;
+      const int4 ti = p.tiles[pair / nch];
+      r.e = ti.x; r.row0 = ti.y; r.valid = ti.z; r.col = 2 * (pair % nch) + (u & 1); r.arow = ti.w;
     } else if constexpr (MODE == MODE_PLAIN) {
-      r.e = 0; r.row0 = (u / p.n_tiles) * TILE_M; r.valid = TILE_M; r.col = u % p.n_tiles;
+      r.e = 0; r.row0 = (u / p.n_tiles) * TILE_M; r.valid = TILE_M; r.col = u % p.n_tiles; r.arow = r.row0;
     } else {
       const int4 ti = p.tiles[u / p.n_tiles];
-      r.e = ti.x; r.row0 = ti.y; r.valid = ti.z; r.col = u % p.n_tiles;
+      // the w2 GEMM's activations are the intermediate rows at the padded rows
+      r.e = ti.x; r.row0 = ti.y; r.valid = ti.z; r.col = u % p.n_tiles; r.arow = ti.y;
     }
     return r;
   };
@@ -160,6 +186,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
       mbar_init(&c.acc_full[b], 1);
       mbar_init(&c.acc_empty[b], EPI_WARPS);
     }
+    mbar_init(&c.a_full, 1);
     c.abort_flag = 0;
     if (MODE == MODE_W13)
       for (int i = 0; i < 2 * nch * TILE_M; ++i) part[i] = 0x80000000u;  // tag of no first use
@@ -175,24 +202,51 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
   tc_fence_after();
   const uint32_t tmem = c.tmem_base;
   const int KS = p.k_stages;
+  if (MODE != MODE_PLAIN && warp == 0 && lane == 0 && p.prefetch_units > 0) {
+    // Weights do not depend on the previous kernels: stream the expected
+    // first units' weight tiles into L2 while those kernels still run.
+    int u = first;
+    for (int k = 0; k < p.prefetch_units; ++k, u = next(u)) {
+      const int tile = (MODE == MODE_W13) ? (u >> 1) : (MODE == MODE_W13S ? (u >> 1) / nch : u / p.n_tiles);
+      if (tile >= p.num_experts) break;
+      const int col = (MODE == MODE_W13)    ? 2 * (int)rank + (u & 1)
+                      : (MODE == MODE_W13S) ? 2 * ((u >> 1) % nch) + (u & 1)
+                                            : u % p.n_tiles;
+      const int brow0 = tile * p.b_rows_per_expert + col * TILE_N;
+      const uint8_t* b_src = p.b_codes + (size_t)(brow0 >> 7) * KS * OPERAND_TILE_BYTES;
+      for (int ks = 0; ks < KS; ++ks) prefetch_l2_bulk(b_src + (size_t)ks * OPERAND_TILE_BYTES, OPERAND_TILE_BYTES);
+    }
+  }
   // Everything above overlaps the previous kernel's tail; its outputs (the
   // tile list, operands, scales) are read only from here on.
   pdl_wait();
   int nunits;
   if constexpr (MODE == MODE_W13) nunits = 2 * (*p.num_tiles);
+  else if constexpr (MODE == MODE_W13S) nunits = 2 * nch * (*p.num_tiles);
   else nunits = (MODE == MODE_PLAIN ? p.m_tiles : *p.num_tiles) * p.n_tiles;
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- producer ----------------
       uint32_t g = 0;  // stages issued so far (ring position)
+      bool a_issued = false;
+      if (ARES && first < nunits) {
+        // every tile reads the same activation rows: load all K stages once
+        const Unit un = unit_at(first);
+        const uint32_t a_bytes = OPERAND_SF_BYTES + (uint32_t)((un.valid + 7) & ~7) * 128;
+        const uint8_t* a_src = p.a_codes + (size_t)(un.arow >> 7) * KS * OPERAND_TILE_BYTES;
+        mbar_arrive_expect_tx(&c.a_full, a_bytes * (uint32_t)KS);
+        for (int ks = 0; ks < KS; ++ks)
+          bulk_load(sA + ks * A_SLOT, a_src + (size_t)ks * OPERAND_TILE_BYTES, a_bytes, &c.a_full);
+        a_issued = true;
+      }
       for (int u = first; u < nunits && !c.abort_flag; u = next(u)) {
         const Unit un = unit_at(u);
         const int brow0 = (MODE == MODE_PLAIN ? 0 : un.e * p.b_rows_per_expert) + un.col * TILE_N;
         // scales + valid rows, in whole 8-row swizzle groups
         const uint32_t a_bytes = OPERAND_SF_BYTES + (uint32_t)((un.valid + 7) & ~7) * 128;
-        const uint32_t bytes = a_bytes + B_SLOT;
-        const uint8_t* a_src = p.a_codes + (size_t)(un.row0 >> 7) * KS * OPERAND_TILE_BYTES;
+        const uint32_t bytes = (ARES ? 0u : a_bytes) + B_SLOT;
+        const uint8_t* a_src = p.a_codes + (size_t)(un.arow >> 7) * KS * OPERAND_TILE_BYTES;
         const uint8_t* b_src = p.b_codes + (size_t)(brow0 >> 7) * KS * OPERAND_TILE_BYTES;
         for (int ks = 0; ks < KS; ++ks, ++g) {
           const int s = g % STAGES;
@@ -202,7 +256,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
             break;
           }
           mbar_arrive_expect_tx(&c.full[s], bytes);
-          bulk_load(sA + s * A_SLOT, a_src + (size_t)ks * OPERAND_TILE_BYTES, a_bytes, &c.full[s]);
+          if (!ARES) bulk_load(sA + s * A_SLOT, a_src + (size_t)ks * OPERAND_TILE_BYTES, a_bytes, &c.full[s]);
           bulk_load(sB + s * B_SLOT, b_src + (size_t)ks * OPERAND_TILE_BYTES, B_SLOT, &c.full[s]);
         }
       }
@@ -211,6 +265,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
         // shared memory is released (bounded, no early exit).
         for (uint32_t k = g > STAGES ? g - STAGES : 0; k < g; ++k)
           mbar_wait_bounded(&c.full[k % STAGES], (k / STAGES) & 1, nullptr, 1000000000ull);
+        if (a_issued) mbar_wait_bounded(&c.a_full, 0, nullptr, 1000000000ull);
       }
     }
     __syncwarp();
@@ -219,6 +274,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
       // ---------------- MMA issuer ----------------
       uint32_t g = 0;
       int n = 0;  // units processed by this CTA
+      if (ARES && first < nunits && !mbar_wait_bounded(&c.a_full, 0, &c.abort_flag)) {
+        c.abort_flag = 1;
+        report_device_error(p.status, DEV_ERR_TIMEOUT);
+      }
       for (int u = first; u < nunits; u = next(u), ++n) {
         if (c.abort_flag) break;
         const int buf = n & 1;
@@ -239,7 +298,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
           tc_fence_after();
           const uint32_t sfa_t = tmem + TMEM_SF_BASE + s * TMEM_SF_STAGE;
           const uint32_t sfb_t = sfa_t + 16;
-          const uint8_t* slot_a = sA + s * A_SLOT;
+          const uint8_t* slot_a = sA + (ARES ? ks : s) * A_SLOT;
           const uint8_t* slot_b = sB + s * B_SLOT;
 #pragma unroll
           for (int kb = 0; kb < 4; ++kb) {
@@ -283,14 +342,16 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
       if (lane == 0) mbar_arrive(&c.acc_empty[buf]);
     };
 
-    if constexpr (MODE == MODE_W13) {
-      int i = 0;  // m-tiles processed
+    if constexpr (W13L) {
+      int i = 0;  // m-tiles (w13s: unit pairs) processed
       for (int u = first; u < nunits; u = next(next(u)), ++i) {
         const Unit un = unit_at(u);
         const bool warp_rows = quarter * 32 < un.valid;  // warp-uniform
-        const bool row_ok = m < un.valid;
         const int prow = un.row0 + m;
-        const float alpha = row_ok ? __fdiv_rn(1.0f, __fmul_rn(p.gs_rows[prow], p.gs_w[un.e])) : 0.0f;
+        // rows of the shared small-batch tile whose token did not pick this
+        // expert take no part (their amax counts as 0 in the exchange)
+        const bool row_ok = m < un.valid && p.src_of_padrow[prow] >= 0;
+        const float alpha = row_ok ? __fdiv_rn(1.0f, __fmul_rn(p.gs_rows[un.arow + m], p.gs_w[un.e])) : 0.0f;
         float h[128];
         float amax = 0.0f;
         bool ready = true;
@@ -317,6 +378,19 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
           release_acc(buf);  // the tensor cores may refill this buffer now
         }
         if (!row_ok) amax = 0.0f;
+        if constexpr (MODE == MODE_W13S) {
+          // FP32 SwiGLU row to the scratch, its maximum folded into the
+          // row's global word (non-negative floats order like their bits);
+          // the requantization kernel finishes the row.
+          if (ready && row_ok) {
+            const int f0 = ((u >> 1) % nch) * 128;
+            atomicMax(reinterpret_cast<unsigned int*>(p.row_amax) + prow, __float_as_uint(amax));
+            float4* dst = reinterpret_cast<float4*>(p.hbuf + (size_t)prow * p.i_pad + f0);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) dst[q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+          }
+          continue;
+        }
         // Exchange the row maxima across the cluster.  Slot buffer i & 1;
         // a peer can be at most one m-tile ahead (it needs this CTA's value
         // of its next m-tile first), so two buffers never overwrite a value
@@ -366,15 +440,18 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
       for (int u = first; u < nunits; u = next(u), ++n) {
         const Unit un = unit_at(u);
         const bool warp_rows = quarter * 32 < un.valid;
-        const bool row_ok = m < un.valid;
         const int prow = un.row0 + m;
+        int src = 0;
+        bool row_ok = m < un.valid;
+        if constexpr (MODE != MODE_PLAIN) {
+          src = row_ok ? p.src_of_padrow[prow] : -1;
+          row_ok = src >= 0;  // a token that did not pick this expert
+        }
         const int buf = n & 1;
         const bool ready = wait_acc(buf, n);
         if (ready && warp_rows) {
-          int src = 0;
           float alpha = 0.0f, wj = 0.0f;
           if (MODE != MODE_PLAIN && row_ok) {
-            src = p.src_of_padrow[prow];
             alpha = __fdiv_rn(1.0f, __fmul_rn(p.gs_rows[prow], p.gs_w[un.e]));
             wj = p.topk_w[src];
           }
@@ -433,13 +510,23 @@ constexpr int stages_for(int nch, int a_rows) {
     if (smem_bytes_for(s, nch, a_rows) <= MAX_SMEM) return s;
   return 0;
 }
+constexpr int stages_for_res(int nch, int a_rows) {
+  for (int s = MAX_STAGES; s >= 3; --s)
+    if (smem_bytes_res(s, nch, a_rows) <= MAX_SMEM) return s;
+  return 0;
+}
+
+template <int MODE, int A_ROWS, int STAGES, bool ARES>
+constexpr int kernel_smem(int nch) {
+  return ARES ? smem_bytes_res(STAGES, nch, A_ROWS) : smem_bytes_for(STAGES, nch, A_ROWS);
+}
 
 // The shared-memory cap belongs to the kernel instantiation, which handles of
 // different widths share: it is only ever raised.
-template <int MODE, int A_ROWS, int STAGES>
+template <int MODE, int A_ROWS, int STAGES, bool ARES = false>
 cudaError_t set_attrs(int nch) {
-  auto k = gemm_fp4_kernel<MODE, A_ROWS, STAGES>;
-  const int bytes = smem_bytes_for(STAGES, nch, A_ROWS);
+  auto k = gemm_fp4_kernel<MODE, A_ROWS, STAGES, ARES>;
+  const int bytes = kernel_smem<MODE, A_ROWS, STAGES, ARES>(nch);
   cudaFuncAttributes fa{};
   cudaError_t err = cudaFuncGetAttributes(&fa, k);
   if (err != cudaSuccess) return err;
@@ -450,12 +537,12 @@ cudaError_t set_attrs(int nch) {
   return err;
 }
 
-template <int MODE, int A_ROWS, int STAGES>
+template <int MODE, int A_ROWS, int STAGES, bool ARES = false>
 cudaLaunchConfig_t make_cfg(dim3 grid, int nch, cudaStream_t s, cudaLaunchAttribute* attr, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = smem_bytes_for(STAGES, MODE == MODE_W13 ? nch : 0, A_ROWS);
+  cfg.dynamicSmemBytes = kernel_smem<MODE, A_ROWS, STAGES, ARES>(MODE == MODE_W13 ? nch : 0);
   cfg.stream = s;
   int n = 0;
   if (MODE == MODE_W13) {
@@ -475,33 +562,37 @@ cudaLaunchConfig_t make_cfg(dim3 grid, int nch, cudaStream_t s, cudaLaunchAttrib
   return cfg;
 }
 
-template <int MODE, int A_ROWS, int STAGES>
+template <int MODE, int A_ROWS, int STAGES, bool ARES = false>
 cudaError_t launch(const GemmArgs& a, dim3 grid, int nch, cudaStream_t s) {
   cudaLaunchAttribute attr[2];
   // The expert GEMMs always follow another kernel of the same forward.
-  cudaLaunchConfig_t cfg = make_cfg<MODE, A_ROWS, STAGES>(grid, nch, s, attr, MODE != MODE_PLAIN);
-  return cudaLaunchKernelEx(&cfg, gemm_fp4_kernel<MODE, A_ROWS, STAGES>, a);
+  cudaLaunchConfig_t cfg = make_cfg<MODE, A_ROWS, STAGES, ARES>(grid, nch, s, attr, MODE != MODE_PLAIN);
+  return cudaLaunchKernelEx(&cfg, gemm_fp4_kernel<MODE, A_ROWS, STAGES, ARES>, a);
 }
 
 // Ring depths that occur: w2 / plain kernels (no exchange slots) and w13
 // kernels with clusters of up to 6 CTAs get the deepest ring that fits; larger
 // clusters one stage less.
 constexpr int W2_STAGES_128 = stages_for(0, 128);
-constexpr int W2_STAGES_32 = stages_for(0, 32);
+constexpr int W2_STAGES_64 = stages_for(0, 64);
 constexpr int W13_STAGES_128 = stages_for(6, 128);
 constexpr int W13_STAGES_128_L = stages_for(16, 128);
-constexpr int W13_STAGES_32 = stages_for(6, 32);
-constexpr int W13_STAGES_32_L = stages_for(16, 32);
-static_assert(W2_STAGES_128 >= 4 && W13_STAGES_128_L >= 3 && W13_STAGES_32_L >= 4, "ring too shallow");
+constexpr int W13_STAGES_64 = stages_for(6, 64);
+constexpr int W13_STAGES_64_L = stages_for(16, 64);
+constexpr int W13S_STAGES_RES = stages_for_res(0, 64);
+constexpr int W13S_STAGES = stages_for(0, 64);
+static_assert(W2_STAGES_128 >= 4 && W13_STAGES_128_L >= 3 && W13_STAGES_64_L >= 4 && W13S_STAGES_RES >= 4,
+              "ring too shallow");
 
 template <typename F>
 cudaError_t with_w13(int nch, int a_rows, F&& f) {
-  if (a_rows == 32) {
-    if (nch <= 6) return f(std::integral_constant<int, 32>{}, std::integral_constant<int, W13_STAGES_32>{});
-    return f(std::integral_constant<int, 32>{}, std::integral_constant<int, W13_STAGES_32_L>{});
+  using std::integral_constant;
+  if (a_rows == 64) {
+    if (nch <= 6) return f(integral_constant<int, 64>{}, integral_constant<int, W13_STAGES_64>{});
+    return f(integral_constant<int, 64>{}, integral_constant<int, W13_STAGES_64_L>{});
   }
-  if (nch <= 6) return f(std::integral_constant<int, 128>{}, std::integral_constant<int, W13_STAGES_128>{});
-  return f(std::integral_constant<int, 128>{}, std::integral_constant<int, W13_STAGES_128_L>{});
+  if (nch <= 6) return f(integral_constant<int, 128>{}, integral_constant<int, W13_STAGES_128>{});
+  return f(integral_constant<int, 128>{}, integral_constant<int, W13_STAGES_128_L>{});
 }
 
 }  // namespace
@@ -512,16 +603,18 @@ cudaError_t gemm_setup_attributes(int nch) {
   static std::mutex m;
   std::lock_guard<std::mutex> lock(m);
   cudaError_t e;
-  for (int a_rows : {32, 128}) {
+  for (int a_rows : {64, 128}) {
     e = with_w13(nch, a_rows, [&](auto ar, auto st) {
       return set_attrs<MODE_W13, decltype(ar)::value, decltype(st)::value>(nch);
     });
     if (e != cudaSuccess) return e;
   }
+  if ((e = set_attrs<MODE_W13S, 64, W13S_STAGES_RES, true>(0)) != cudaSuccess) return e;
+  if ((e = set_attrs<MODE_W13S, 64, W13S_STAGES, false>(0)) != cudaSuccess) return e;
   if ((e = set_attrs<MODE_W2_ATOMIC, 128, W2_STAGES_128>(0)) != cudaSuccess) return e;
-  if ((e = set_attrs<MODE_W2_ATOMIC, 32, W2_STAGES_32>(0)) != cudaSuccess) return e;
+  if ((e = set_attrs<MODE_W2_ATOMIC, 64, W2_STAGES_64>(0)) != cudaSuccess) return e;
   if ((e = set_attrs<MODE_W2_ORDERED, 128, W2_STAGES_128>(0)) != cudaSuccess) return e;
-  if ((e = set_attrs<MODE_W2_ORDERED, 32, W2_STAGES_32>(0)) != cudaSuccess) return e;
+  if ((e = set_attrs<MODE_W2_ORDERED, 64, W2_STAGES_64>(0)) != cudaSuccess) return e;
   return set_attrs<MODE_PLAIN, 128, W2_STAGES_128>(0);
 }
 
@@ -531,7 +624,7 @@ int gemm_w13_max_clusters(int nch, int a_rows) {
     constexpr int AR = decltype(ar)::value, S = decltype(st)::value;
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = make_cfg<MODE_W13, AR, S>(dim3(nch, 1, 1), nch, 0, attr, false);
-    return cudaOccupancyMaxActiveClusters(&n, gemm_fp4_kernel<MODE_W13, AR, S>, &cfg);
+    return cudaOccupancyMaxActiveClusters(&n, gemm_fp4_kernel<MODE_W13, AR, S, false>, &cfg);
   });
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -547,11 +640,18 @@ cudaError_t launch_gemm_w13(const GemmArgs& a, int n_chunks, int n_clusters, int
   });
 }
 
+cudaError_t launch_gemm_w13s(const GemmArgs& a, int n_ctas, bool resident, cudaStream_t s) {
+  if (resident && a.k_stages > ARES_MAX_KS) return cudaErrorInvalidValue;
+  const dim3 grid(n_ctas, 1, 1);
+  if (resident) return launch<MODE_W13S, 64, W13S_STAGES_RES, true>(a, grid, 0, s);
+  return launch<MODE_W13S, 64, W13S_STAGES, false>(a, grid, 0, s);
+}
+
 cudaError_t launch_gemm_w2(const GemmArgs& a, int n_ctas, bool ordered, int a_rows, cudaStream_t s) {
   const dim3 grid(n_ctas, 1, 1);
-  if (a_rows == 32) {
-    if (ordered) return launch<MODE_W2_ORDERED, 32, W2_STAGES_32>(a, grid, 0, s);
-    return launch<MODE_W2_ATOMIC, 32, W2_STAGES_32>(a, grid, 0, s);
+  if (a_rows == 64) {
+    if (ordered) return launch<MODE_W2_ORDERED, 64, W2_STAGES_64>(a, grid, 0, s);
+    return launch<MODE_W2_ATOMIC, 64, W2_STAGES_64>(a, grid, 0, s);
   }
   if (ordered) return launch<MODE_W2_ORDERED, 128, W2_STAGES_128>(a, grid, 0, s);
   return launch<MODE_W2_ATOMIC, 128, W2_STAGES_128>(a, grid, 0, s);

@@ -70,6 +70,51 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __r
   }
 }
 
+// Requantization of the small-batch w13 output: one warp per (tile, row).
+// Row maximum -> global scale -> block scales and codes, the same arithmetic
+// as the fused w13 epilogue; returns the row's maximum word to zero.
+// grid (max tiles, 8): warp w of CTA (i, y) takes row 8*y + w of tile i.
+__global__ void __launch_bounds__(256) requant_rows_kernel(const float* __restrict__ hbuf,
+                                                          float* __restrict__ row_amax,
+                                                          const int32_t* __restrict__ src_of_padrow,
+                                                          const int4* __restrict__ tiles,
+                                                          const int32_t* __restrict__ num_tiles, int I, int i_pad,
+                                                          uint8_t* __restrict__ h_codes, float* __restrict__ h_gs) {
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.y * 8 + (threadIdx.x >> 5);
+  pdl_trigger();
+  pdl_wait();
+  if ((int)blockIdx.x >= *num_tiles) return;
+  const int4 ti = tiles[blockIdx.x];
+  if (row >= ti.z) return;
+  const int prow = ti.y + row;
+  if (src_of_padrow[prow] < 0) return;
+  const float amax = row_amax[prow];
+  const float gs = nvfp4_global_scale(amax);
+  const float* hr = hbuf + (size_t)prow * i_pad;
+  const int nblk = I / SF_VEC, k16_row = i_pad / SF_VEC;
+  for (int b = lane; b < nblk; b += 32) {
+    float v[16];
+    const float4* src = reinterpret_cast<const float4*>(hr + 16 * b);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 f = src[q];
+      v[4 * q] = f.x;
+      v[4 * q + 1] = f.y;
+      v[4 * q + 2] = f.z;
+      v[4 * q + 3] = f.w;
+    }
+    uint2 packed;
+    const uint32_t sf = nvfp4_quant_block16(v, gs, packed);
+    *reinterpret_cast<uint2*>(h_codes + operand_offset(prow, 8 * b, i_pad / 2)) = packed;
+    h_codes[sf_atom_offset(prow, b, k16_row)] = (uint8_t)sf;
+  }
+  if (lane == 0) {
+    h_gs[prow] = gs;
+    row_amax[prow] = 0.0f;
+  }
+}
+
 // amax over each expert's whole matrix: grid (chunks, E).
 __global__ void __launch_bounds__(256) weight_amax_kernel(const __nv_bfloat16* __restrict__ w, size_t per_expert,
                                                          uint32_t* __restrict__ amax_bits) {
@@ -273,6 +318,13 @@ cudaError_t launch_codes_to_tiled(const uint8_t* codes, int rows, int row_bytes,
 cudaError_t launch_sf_to_atoms(const uint8_t* sf, int rows, int k16, uint8_t* atoms, cudaStream_t s) {
   sf_to_atoms_kernel<<<grid_for((size_t)rows * k16, 256), 256, 0, s>>>(sf, rows, k16, atoms);
   return cudaGetLastError();
+}
+
+cudaError_t launch_requant_rows(const float* hbuf, float* row_amax, const int32_t* src_of_padrow, const int4* tiles,
+                                const int32_t* num_tiles, int max_tiles, int I, int i_pad, uint8_t* h_codes,
+                                float* h_gs, cudaStream_t s) {
+  return launch_k(requant_rows_kernel, dim3(max_tiles, SMALL_BATCH_TOKENS / 8), dim3(256), 0, s, true, hbuf,
+                  row_amax, src_of_padrow, tiles, num_tiles, I, i_pad, h_codes, h_gs);
 }
 
 cudaError_t launch_finalize_atomic(const float* out_acc, void* out, int T, int H, cudaStream_t s) {

@@ -9,6 +9,7 @@
 // inside an expert, and pads each GEMM tile of an expert to its own 128-row
 // block for the tensor-core GEMMs.
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -39,8 +40,9 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
   return *reinterpret_cast<float2*>(&d);
 }
 
-// grid: (ceil(T / (8*TB)), E / EB); block: 256 threads = 8 warps; dynamic
-// shared memory H * EB * 2 bytes holding the CTA's whole router-weight slice,
+// Logits of one (token block, expert block) tile, for a CTA of a grid
+// (ceil(T / (8*TB)), E / EB) of 256 threads = 8 warps; dynamic shared
+// memory H * EB * 2 bytes holding the CTA's whole router-weight slice,
 // laid out [round j][k][partial p][EB] (row h = 256 j + 8 p + k).
 // Warp w handles tokens t0..t0+TB-1; lane p is partial p of every
 // (token, expert) pair of the CTA's expert block: it accumulates chunks
@@ -49,25 +51,21 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
 //
 // XALL: every round's activations are loaded into registers up front (one
 // memory round trip; H <= 2048), for small token counts where latency rules.
-// The kernel also clears the per-expert row counters the top-k kernel fills.
-template <int TB, int EB, bool XALL>
-__global__ void __launch_bounds__(256) router_logits_kernel(const __nv_bfloat16* __restrict__ x,
-                                                           const __nv_bfloat16* __restrict__ wg,
-                                                           const float* __restrict__ bias,
-                                                           float* __restrict__ logits, int T, int H, int E,
-                                                           int32_t* __restrict__ counts) {
+// Ends with a __syncthreads-free store of the logits; the caller may reuse
+// the shared memory only after its own barrier.
+template <int TB, int EB, bool XALL, bool XSMEM = false>
+__device__ __forceinline__ void router_tile(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ wg,
+                                            const float* __restrict__ bias, float* __restrict__ logits, int T,
+                                            int H, int E) {
   constexpr int UNITS = EB / 8;                 // 16-byte units (8 bf16) per staged row
   constexpr int NV = TB * EB;                   // partial sums per lane
-  static_assert(NV % 32 == 0, "TB*EB must be a multiple of 32");
+  static_assert(NV % 32 == 0 || NV == 8 || NV == 16, "TB*EB must be 8, 16 or a multiple of 32");
   extern __shared__ uint4 sw[];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e0 = blockIdx.y * EB;
   const int t0 = (blockIdx.x * ROUTER_WARPS + warp) * TB;
   const int rounds = H / 256;
-  pdl_trigger();
-  if (blockIdx.x == 0 && blockIdx.y == 0)
-    for (int e = threadIdx.x; e < E; e += blockDim.x) counts[e] = 0;
 
   for (int h = threadIdx.x; h < H; h += 256) {
     const int j = h >> 8, hr = h & 255, k = hr & 7, p = (hr >> 3) & 31;
@@ -76,6 +74,22 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const __nv_bfloat16*
     for (int u = 0; u < UNITS; ++u) {
       const uint32_t dst = smem_u32(&sw[((j * 8 + k) * 32 + p) * UNITS + (u ^ router_swz<UNITS>(p))]);
       asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + 16 * u) : "memory");
+    }
+  }
+  // XSMEM: the CTA's activation rows [8*TB tokens][H] are staged after the
+  // weight slice (rows past T are zero), so all operands arrive in one round
+  // trip and the round loop below can stay rolled.
+  uint4* sx = sw + (size_t)H * EB * 2 / 16;
+  if constexpr (XSMEM) {
+    const int cpr = H / 8;  // 16-byte chunks per row
+    const int tb0 = blockIdx.x * ROUTER_WARPS * TB;
+    for (int idx = threadIdx.x; idx < ROUTER_WARPS * TB * cpr; idx += 256) {
+      const int r = idx / cpr, c = idx - r * cpr;
+      const int tok = tb0 + r;
+      const uint32_t dst = smem_u32(&sx[idx]);
+      const __nv_bfloat16* src = x + (size_t)(tok < T ? tok : 0) * H + 8 * c;
+      const int nbytes = tok < T ? 16 : 0;  // zero fill
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(nbytes) : "memory");
     }
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
@@ -90,7 +104,8 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const __nv_bfloat16*
   };
   constexpr int XR = XALL ? 8 : 2;              // rounds of activations held in registers
   uint4 xb[XR][TB];
-  if constexpr (XALL) {
+  if constexpr (XSMEM) {
+  } else if constexpr (XALL) {
 #pragma unroll
     for (int j = 0; j < XR; ++j)
       if (j < rounds) load_x(j, xb[j]);
@@ -130,7 +145,15 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const __nv_bfloat16*
     }
   };
 
-  if constexpr (XALL) {
+  if constexpr (XSMEM) {
+    const int cpr = H / 8;
+#pragma unroll 1
+    for (int j = 0; j < rounds; ++j) {
+#pragma unroll
+      for (int t = 0; t < TB; ++t) xb[0][t] = sx[(warp * TB + t) * cpr + j * 32 + lane];
+      round_fma(j, xb[0]);
+    }
+  } else if constexpr (XALL) {
 #pragma unroll
     for (int j = 0; j < XR; ++j)
       if (j < rounds) round_fma(j, xb[j]);
@@ -146,8 +169,11 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const __nv_bfloat16*
   }
 
   // Pairwise tree over the 32 partials (lanes), partial p with p^o for
-  // o = 16..1.  Each level halves the values a lane keeps, so lane p ends
-  // with the sums of values [p*M, p*M + M), M = NV / 32.
+  // o = 16..1.  With NV >= 32 each level halves the values a lane keeps, so
+  // lane p ends with the sums of values [p*M, p*M + M), M = NV / 32; with
+  // fewer values every lane keeps all of them (a plain butterfly: the same
+  // sums, since each level adds the same two partials) and lane i < NV
+  // writes value i.
   float v[NV];
 #pragma unroll
   for (int t = 0; t < TB; ++t)
@@ -156,6 +182,23 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const __nv_bfloat16*
       v[t * EB + 2 * e] = acc[t][e].x;
       v[t * EB + 2 * e + 1] = acc[t][e].y;
     }
+  if constexpr (NV < 32) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int i = 0; i < NV; ++i) v[i] = __fadd_rn(v[i], __shfl_xor_sync(0xffffffffu, v[i], o));
+    float mine = v[0];
+#pragma unroll
+    for (int i = 1; i < NV; ++i)
+      if (lane == i) mine = v[i];
+    const int t = lane / EB, e = lane % EB;
+    const int tok = t0 + t;
+    if (lane < NV && tok < T) {
+      if (bias) mine = __fadd_rn(mine, bias[e0 + e]);
+      logits[(size_t)tok * E + e0 + e] = mine;
+    }
+    return;
+  }
 #pragma unroll
   for (int lvl = 0; lvl < 5; ++lvl) {
     const int o = 16 >> lvl;
@@ -183,33 +226,55 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const __nv_bfloat16*
   }
 }
 
-// One warp per token: top-k by (logit desc, expert asc), softmax weights of
-// the chosen experts renormalised, and the per-expert row counts.
-__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int T, int E, int K,
-                                                  int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
-                                                  int32_t* __restrict__ counts) {
-  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
+// The router kernel: one (token block, expert block) tile per CTA.  It also
+// clears the per-expert row counters the top-k kernel fills.
+template <int TB, int EB, bool XALL>
+__global__ void __launch_bounds__(256) router_logits_kernel(const __nv_bfloat16* __restrict__ x,
+                                                           const __nv_bfloat16* __restrict__ wg,
+                                                           const float* __restrict__ bias,
+                                                           float* __restrict__ logits, int T, int H, int E,
+                                                           int32_t* __restrict__ counts) {
   pdl_trigger();
-  pdl_wait();
-  if (t >= T) return;
-  constexpr int MAXE = 8;  // up to 256 experts
-  float l[MAXE], cand[MAXE];
+  if (blockIdx.x == 0 && blockIdx.y == 0)
+    for (int e = threadIdx.x; e < E; e += blockDim.x) counts[e] = 0;
+  router_tile<TB, EB, XALL>(x, wg, bias, logits, T, H, E);
+}
+
+// (value, expert) order of the top-k: larger logit first, ties to the lower
+// expert id.
+__device__ __forceinline__ bool topk_before(float av, int ae, float bv, int be) {
+  return av > bv || (av == bv && ae < be);
+}
+
+// Top-k of one token's logits by one warp: K rounds of a warp argmax over
+// the remaining candidates (lane holds experts lane, lane + 32, ...; E <= 256)
+// by (logit desc, expert asc); softmax over all E experts (lane sums in
+// ascending order, then the xor tree), chosen probabilities renormalised in
+// slot order.  The round loop is kept rolled: its body stays in the
+// instruction cache (fully unrolled, the selection ran from cold instruction
+// fetches).  Lane j < K returns slot j: its expert in e_lane and its weight in
+// w_lane.  Logits are read through L2 (another CTA of the same grid may have
+// written them).  All 32 lanes must call it.
+__device__ __forceinline__ void topk_warp(const float* __restrict__ lrow, int E, int K, int lane, int& e_lane,
+                                          float& w_lane) {
+  constexpr int NE = 8;
+  float l[NE], cand[NE];
 #pragma unroll
-  for (int i = 0; i < MAXE; ++i) {
+  for (int i = 0; i < NE; ++i) {
     const int e = lane + 32 * i;
-    l[i] = e < E ? logits[(size_t)t * E + e] : -INFINITY;
+    l[i] = e < E ? __ldcg(lrow + e) : -INFINITY;
     cand[i] = l[i];
   }
-  float sel_l[16];
-  int sel_e[16];
+  float l_lane = -INFINITY;
+  e_lane = 0;
+#pragma unroll 1
   for (int j = 0; j < K; ++j) {
     float bv = -INFINITY;
     int be = 0x7fffffff;
 #pragma unroll
-    for (int i = 0; i < MAXE; ++i) {
+    for (int i = 0; i < NE; ++i) {
       const int e = lane + 32 * i;
-      if (e < E && (cand[i] > bv || (cand[i] == bv && e < be))) {
+      if (e < E && topk_before(cand[i], e, bv, be)) {
         bv = cand[i];
         be = e;
       }
@@ -218,36 +283,51 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
     for (int o = 16; o > 0; o >>= 1) {
       const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
       const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (ov > bv || (ov == bv && oe < be)) {
+      if (topk_before(ov, oe, bv, be)) {
         bv = ov;
         be = oe;
       }
     }
-    sel_l[j] = bv;
-    sel_e[j] = be;
+    if (lane == j) {
+      l_lane = bv;
+      e_lane = be;
+    }
 #pragma unroll
-    for (int i = 0; i < MAXE; ++i)
+    for (int i = 0; i < NE; ++i)
       if (lane + 32 * i == be) cand[i] = -INFINITY;
   }
   // softmax over all experts, then renormalise the chosen probabilities
-  const float m = sel_l[0];
+  const float m = __shfl_sync(0xffffffffu, l_lane, 0);
   float s = 0.0f;
 #pragma unroll
-  for (int i = 0; i < MAXE; ++i)
+  for (int i = 0; i < NE; ++i)
     if (lane + 32 * i < E) s += expf(l[i] - m);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  float p[16], psum = 0.0f;
-  for (int j = 0; j < K; ++j) {
-    p[j] = expf(sel_l[j] - m) / s;
-    psum += p[j];
-  }
-  for (int j = 0; j < K; ++j) {
-    if (lane == j) {
-      topk_ids[(size_t)t * K + j] = sel_e[j];
-      topk_w[(size_t)t * K + j] = p[j] / psum;
-      atomicAdd(&counts[sel_e[j]], 1);
-    }
+  const float pj = lane < K ? expf(l_lane - m) / s : 0.0f;
+  float psum = 0.0f;
+#pragma unroll 1
+  for (int j = 0; j < K; ++j) psum += __shfl_sync(0xffffffffu, pj, j);
+  w_lane = pj / psum;
+}
+
+// One warp per token: the top-k choice and weights, and the per-expert row
+// counts.
+__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int T, int E, int K,
+                                                  int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
+                                                  int32_t* __restrict__ counts) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  pdl_trigger();
+  pdl_wait();
+  if (t >= T) return;
+  int e;
+  float w;
+  topk_warp(logits + (size_t)t * E, E, K, lane, e, w);
+  if (lane < K) {
+    topk_ids[(size_t)t * K + lane] = e;
+    topk_w[(size_t)t * K + lane] = w;
+    atomicAdd(&counts[e], 1);
   }
 }
 
@@ -348,7 +428,7 @@ __global__ void __launch_bounds__(PERM_THREADS) permute_kernel(const int32_t* __
   }
   const int ntile = (cnt + tile_rows - 1) >> tile_shift;
   for (int i = threadIdx.x; i < ntile; i += blockDim.x)
-    o.tiles[tbase + i] = make_int4(e, poff + 128 * i, min(tile_rows, cnt - tile_rows * i), 0);
+    o.tiles[tbase + i] = make_int4(e, poff + 128 * i, min(tile_rows, cnt - tile_rows * i), poff + 128 * i);
   if (threadIdx.x == 0) {
     o.expert_offsets[e] = off;
     if (e == E - 1) {
@@ -356,6 +436,132 @@ __global__ void __launch_bounds__(PERM_THREADS) permute_kernel(const int32_t* __
       o.num_tiles[0] = tbase + ntile;
     }
   }
+}
+
+// Small-batch front end, one launch: router logits, per-token quantization,
+// top-k, and the expert grouping.  Grid and tiles are the router's.
+//  1. every CTA computes its (token block, expert block) logits, and
+//     quantizes its share of the token block's rows into the shared
+//     activation tile (row t = token t);
+//  2. the last CTA of a token block to finish (an acquire-release counter)
+//     takes the top-k of the block's tokens and writes, for every expert e,
+//     the padded row e*128 + t's source (token * K + slot, or -1);
+//  3. the last CTA of the grid derives the expert grouping from all top-k
+//     ids: offsets, the stable token-order permutation, and one GEMM tile
+//     per expert with rows.
+// Counters are returned to zero by the CTA that consumed them.  No CTA ever
+// waits for another.
+template <int TB, int EB, bool XSMEM>
+__global__ void __launch_bounds__(256) front_small_kernel(const FrontArgs p) {
+  extern __shared__ uint4 front_smem[];
+  __shared__ int red[ROUTER_WARPS];
+  __shared__ int last;
+  constexpr int TOK = ROUTER_WARPS * TB;  // tokens per token block
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = p.T, H = p.H, E = p.E, K = p.K;
+  const int tb0 = blockIdx.x * TOK;
+  const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(p.x);
+  // The w13 GEMM may launch now and stage weights; it reads this kernel's
+  // outputs only after its dependency wait.
+  pdl_trigger();
+  router_tile<TB, EB, false, XSMEM>(x, reinterpret_cast<const __nv_bfloat16*>(p.gate_w), p.bias, p.logits, T, H,
+                                     E);
+
+  // 1b. per-token NVFP4 quantization (one warp per token)
+  const int nblk = H / SF_VEC;
+  for (int i = blockIdx.y + gridDim.y * warp; i < TOK; i += gridDim.y * ROUTER_WARPS) {
+    const int t = tb0 + i;
+    if (t >= T) break;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    float amax = 0.0f;
+    for (int b = lane; b < nblk; b += 32) {
+      float v[16];
+      bf16x16_to_f32(__ldg(xr + 2 * b), __ldg(xr + 2 * b + 1), v);
+#pragma unroll
+      for (int q = 0; q < 16; ++q) amax = fmaxf(amax, fabsf(v[q]));
+    }
+    amax = warp_max(amax);
+    const float gs = nvfp4_global_scale(amax);
+    for (int b = lane; b < nblk; b += 32) {
+      float v[16];
+      bf16x16_to_f32(__ldg(xr + 2 * b), __ldg(xr + 2 * b + 1), v);
+      uint2 packed;
+      const uint32_t sf = nvfp4_quant_block16(v, gs, packed);
+      *reinterpret_cast<uint2*>(p.a_codes + operand_offset(t, 8 * b, H / 2)) = packed;
+      p.a_codes[sf_atom_offset(t, b, nblk)] = (uint8_t)sf;
+    }
+    if (lane == 0) p.gs_rows[t] = gs;
+    if (p.out_acc) {
+      float4* o = reinterpret_cast<float4*>(p.out_acc + (size_t)t * H);
+      for (int q = lane; q < H / 4; q += 32) o[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+
+  // 2. top-k, by the last CTA of the token block
+  __syncthreads();
+  if (threadIdx.x == 0) last = arrive_acq_rel_gpu(&p.sync[blockIdx.x]) == gridDim.y - 1;
+  __syncthreads();
+  if (last) {
+    for (int i = warp; i < TOK; i += ROUTER_WARPS) {
+      const int t = tb0 + i;
+      if (t >= T) break;
+      int e_lane;
+      float w;
+      topk_warp(p.logits + (size_t)t * E, E, K, lane, e_lane, w);
+      if (lane < K) {
+        p.topk_ids[(size_t)t * K + lane] = e_lane;
+        p.topk_w[(size_t)t * K + lane] = w;
+      }
+      for (int base = 0; base < E; base += 32) {  // every expert's padded row t
+        const int e = base + lane;
+        int src = -1;
+#pragma unroll 1
+        for (int j = 0; j < K; ++j)
+          if (__shfl_sync(0xffffffffu, e_lane, j) == e) src = t * K + j;
+        if (e < E) p.src_of_padrow[e * 128 + t] = src;
+      }
+    }
+    if (threadIdx.x == 0) p.sync[blockIdx.x] = 0;
+  }
+
+  // 3. the expert grouping, by the last CTA of the grid
+  __syncthreads();
+  if (threadIdx.x == 0) last = arrive_acq_rel_gpu(&p.sync[FRONT_SYNC_WORDS - 1]) == gridDim.x * gridDim.y - 1;
+  __syncthreads();
+  if (!last) return;
+  // T <= 64: the tokens that chose expert e form one 64-bit mask, so counts
+  // and the stable (token-order) rank of every row are population counts.
+  unsigned long long* tok_mask = reinterpret_cast<unsigned long long*>(front_smem);  // [E]
+  int* offs = reinterpret_cast<int*>(tok_mask + 256);                                // [E]
+  const int n = T * K;
+  const int e = threadIdx.x;  // E <= 256 = blockDim.x
+  if (e < E) tok_mask[e] = 0ull;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x)
+    atomicOr(&tok_mask[__ldcg(p.topk_ids + i)], 1ull << (i / K));
+  __syncthreads();
+  const int cnt = e < E ? __popcll(tok_mask[e]) : 0;
+  int total, touched;
+  const int off = block_excl_scan(cnt, red, &total);
+  const int tix = block_excl_scan(cnt > 0 ? 1 : 0, red, &touched);
+  if (e < E) {
+    offs[e] = off;
+    p.expert_offsets[e] = off;
+    if (e == E - 1) {
+      p.expert_offsets[E] = off + cnt;
+      p.num_tiles[0] = touched;
+    }
+    if (cnt > 0) p.tiles[tix] = make_int4(e, e * 128, T, 0);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int ei = __ldcg(p.topk_ids + i), t = i / K;
+    const int r = offs[ei] + __popcll(tok_mask[ei] & ((1ull << t) - 1ull));
+    p.src_of_row[r] = i;
+    p.row_of_src[i] = r;
+    p.pad_row_of_src[i] = ei * 128 + t;
+  }
+  if (threadIdx.x == 0) p.sync[FRONT_SYNC_WORDS - 1] = 0;
 }
 
 template <int TB, int EB, bool XALL>
@@ -425,6 +631,61 @@ cudaError_t router_setup_max(int bytes) {
 }
 
 int router_smem_bytes(int H, int E) { return H * router_eb(H, E) * 2; }
+
+namespace {
+
+
+// Dynamic shared memory of the front kernel: the router-weight slice, plus
+// the token block's activation rows when they are staged (XSMEM).
+constexpr int FRONT_XSMEM_LIMIT = 200 * 1024;
+int front_smem_bytes(int H, int eb, int tb, bool xsmem) { return H * eb * 2 + (xsmem ? ROUTER_WARPS * tb * H * 2 : 0); }
+
+template <int TB, int EB, bool XSMEM>
+cudaError_t raise_front_attr(int H) {
+  const int bytes = front_smem_bytes(H, EB, TB, XSMEM);
+  cudaFuncAttributes a{};
+  cudaError_t e = cudaFuncGetAttributes(&a, front_small_kernel<TB, EB, XSMEM>);
+  if (e != cudaSuccess || a.maxDynamicSharedSizeBytes >= bytes) return e;
+  return cudaFuncSetAttribute(front_small_kernel<TB, EB, XSMEM>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+template <int TB, int EB, bool XSMEM>
+cudaError_t launch_front_t(const FrontArgs& a, cudaStream_t s) {
+  dim3 grid((a.T + ROUTER_WARPS * TB - 1) / (ROUTER_WARPS * TB), a.E / EB);
+  // first kernel of a forward: ordinary stream order
+  return launch_k(front_small_kernel<TB, EB, XSMEM>, grid, dim3(256), (size_t)front_smem_bytes(a.H, EB, TB, XSMEM), s,
+                  false, a);
+}
+
+// Tiles of the front kernel: 8 tokens x 8 experts per CTA (E/8 x T/8 CTAs),
+// so the operands staged per CTA stay small (32 bytes per hidden element) and
+// the last CTA of a token block takes one token per warp in the top-k phase.
+// The activation rows are staged in shared memory when they fit.  Calls f
+// with (tokens per warp, experts per CTA, staged) as types.
+template <typename F>
+cudaError_t with_front(int H, int E, F&& f) {
+  using std::integral_constant;
+  if (front_smem_bytes(H, 8, 1, true) <= FRONT_XSMEM_LIMIT)
+    return f(integral_constant<int, 1>{}, integral_constant<int, 8>{}, integral_constant<bool, true>{});
+  return f(integral_constant<int, 1>{}, integral_constant<int, 8>{}, integral_constant<bool, false>{});
+}
+
+}  // namespace
+
+
+cudaError_t front_setup(int H, int E) {
+  std::lock_guard<std::mutex> lock(router_attr_mutex);
+  return with_front(H, E, [&](auto tb, auto eb, auto xs) {
+    return raise_front_attr<decltype(tb)::value, decltype(eb)::value, decltype(xs)::value>(H);
+  });
+}
+
+cudaError_t launch_front_small(const FrontArgs& a, cudaStream_t s) {
+  if (a.T > SMALL_BATCH_TOKENS || a.E > 256 || a.K > 16) return cudaErrorInvalidValue;
+  return with_front(a.H, a.E, [&](auto tb, auto eb, auto xs) {
+    return launch_front_t<decltype(tb)::value, decltype(eb)::value, decltype(xs)::value>(a, s);
+  });
+}
 
 cudaError_t launch_router_logits(const void* x, const void* gate_w, const float* bias, float* logits, int T,
                                  int H, int E, int32_t* counts, cudaStream_t s) {

@@ -28,11 +28,12 @@ struct moe_handle {
   int Rpad = 0;         // padded expert-grouped rows, worst case
   int tile_cap = 0;     // worst-case number of GEMM tiles
   int num_sms = 0;      // persistent w2 grid
-  int w13_clusters[2] = {0, 0};  // persistent w13 grid (clusters of I/128 CTAs), 32- / 128-row tiles
+  int w13_clusters[2] = {0, 0};  // persistent w13 grid (clusters of I/128 CTAs), 64- / 128-row tiles
   bool deterministic = false;
   bool loaded = false;
   moe_weight_desc w13_desc{}, w2_desc{};
   int last_T = -1;
+  bool last_small = false;  // the last forward used the shared small-batch activation tile
   std::string err;
   size_t bytes = 0;
   std::vector<void*> allocs;
@@ -49,6 +50,9 @@ struct moe_handle {
   int32_t *src_of_row = nullptr, *row_of_src = nullptr, *pad_row_of_src = nullptr, *src_of_padrow = nullptr;
   int4* tiles = nullptr;
   int32_t* num_tiles = nullptr;
+  uint32_t* front_sync = nullptr;  // completion counters of the small-batch front kernel
+  float* hbuf = nullptr;           // small batches: FP32 SwiGLU rows [E*128][Ipad]
+  float* row_amax = nullptr;       // small batches: their row maxima [E*128], zero between forwards
 
   // operands of the two GEMMs
   uint8_t *a_codes = nullptr, *a_sf = nullptr, *h_codes = nullptr, *h_sf = nullptr;
@@ -133,12 +137,18 @@ int device_of(const void* p) {
   return at.device;
 }
 
-// Forwards of at most this many tokens use 32-row GEMM tiles: their experts
-// get a handful of rows each, and reserving 32 instead of 128 activation rows
-// per pipeline stage leaves room for a deeper weight-streaming ring.
-constexpr int SMALL_BATCH_TOKENS = 64;
+// Forwards of at most SMALL_BATCH_TOKENS tokens quantize every token once
+// into one shared 64-row activation tile that all experts' w13 GEMMs read:
+// their experts get a handful of rows each, no expanded copy of the
+// activations is made, and reserving 64 instead of 128 activation rows per
+// pipeline stage leaves room for a deeper weight-streaming ring.
+int tile_rows_for(int T) { return T <= SMALL_BATCH_TOKENS ? 64 : 128; }
 
-int tile_rows_for(int T) { return T <= SMALL_BATCH_TOKENS ? 32 : 128; }
+// Small batches: weight units each GEMM CTA streams into L2 before its
+// dependency wait (w13: two experts' column pairs, ~590 KB per CTA; w2: four
+// units of I x 128 weights).  Together they stay well inside L2.
+constexpr int W13_PREFETCH_UNITS = 4;
+constexpr int W2_PREFETCH_UNITS = 4;
 
 // Worst-case number of GEMM tiles of tile_rows rows when T tokens each pick
 // K of E experts (each tile is padded to its own 128-row block).
@@ -220,20 +230,51 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
                         cudaStream_t s) {
   const int H = h->H, E = h->E, K = h->K;
   if (T > 0) {
-    CK(h, mark(h, 0, s));
-    CK(h, launch_router_logits(x, gate_w, bias, h->logits, T, H, E, h->counts, s));
-    CK(h, mark(h, 1, s));
-    CK(h, launch_topk(h->logits, T, E, K, h->topk_ids, h->topk_w, h->counts, s));
-    CK(h, mark(h, 2, s));
     const int tile_rows = tile_rows_for(T);
-    PermuteOut po{h->expert_offsets, h->src_of_row, h->row_of_src, h->pad_row_of_src,
-                  h->src_of_padrow,  h->tiles,      h->num_tiles};
-    CK(h, launch_permute(h->topk_ids, h->counts, T, K, E, tile_rows, po, s));
-    CK(h, mark(h, 3, s));
-    CK(h, launch_act_quant(x, T, H, K, h->pad_row_of_src, h->a_codes, h->a_sf, h->gs_rows,
-                           h->deterministic ? nullptr : h->out_acc, s));
-    CK(h, mark(h, 4, s));
-    const int tb = tile_bound(T, K, E, tile_rows);
+    const bool small = T <= SMALL_BATCH_TOKENS;
+    CK(h, mark(h, 0, s));
+    if (small) {
+      // one kernel for router, quantization, top-k and grouping; its time is
+      // reported as the router stage, the next three stages as empty
+      FrontArgs fa{};
+      fa.x = x;
+      fa.gate_w = gate_w;
+      fa.bias = bias;
+      fa.T = T;
+      fa.H = H;
+      fa.E = E;
+      fa.K = K;
+      fa.logits = h->logits;
+      fa.topk_ids = h->topk_ids;
+      fa.topk_w = h->topk_w;
+      fa.a_codes = h->a_codes;
+      fa.gs_rows = h->gs_rows;
+      fa.out_acc = h->deterministic ? nullptr : h->out_acc;
+      fa.src_of_padrow = h->src_of_padrow;
+      fa.expert_offsets = h->expert_offsets;
+      fa.src_of_row = h->src_of_row;
+      fa.row_of_src = h->row_of_src;
+      fa.pad_row_of_src = h->pad_row_of_src;
+      fa.tiles = h->tiles;
+      fa.num_tiles = h->num_tiles;
+      fa.sync = h->front_sync;
+      CK(h, launch_front_small(fa, s));
+      for (int i = 1; i <= 4; ++i) CK(h, mark(h, i, s));
+    } else {
+      CK(h, launch_router_logits(x, gate_w, bias, h->logits, T, H, E, h->counts, s));
+      CK(h, mark(h, 1, s));
+      CK(h, launch_topk(h->logits, T, E, K, h->topk_ids, h->topk_w, h->counts, s));
+      CK(h, mark(h, 2, s));
+      PermuteOut po{h->expert_offsets, h->src_of_row, h->row_of_src, h->pad_row_of_src,
+                    h->src_of_padrow,  h->tiles,      h->num_tiles};
+      CK(h, launch_permute(h->topk_ids, h->counts, T, K, E, tile_rows, po, s));
+      CK(h, mark(h, 3, s));
+      CK(h, launch_act_quant(x, T, H, K, h->pad_row_of_src, h->a_codes, h->a_sf, h->gs_rows,
+                             h->deterministic ? nullptr : h->out_acc, s));
+      CK(h, mark(h, 4, s));
+    }
+    // bound on the tile count: one per expert with rows (small batches)
+    const int tb = small ? std::min(E, T * K) : tile_bound(T, K, E, tile_rows);
     GemmArgs g{};
     g.status = h->status_dev;
     g.tiles = h->tiles;
@@ -249,7 +290,22 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
     g.h_sf = h->h_sf;
     g.h_gs = h->h_gs;
     g.i_pad = h->Ipad;
-    CK(h, launch_gemm_w13(g, h->I / 128, std::min(h->w13_clusters[tile_rows == 128], tb), tile_rows, s));
+    g.src_of_padrow = h->src_of_padrow;
+    g.num_experts = E;
+    g.prefetch_units = small ? W13_PREFETCH_UNITS : 0;
+    if (small) {
+      // every tile reads the one shared activation tile (kept resident when
+      // K <= 2048); no clusters: the units spread over all SMs, and the
+      // requantization follows as its own kernel
+      g.w13_pairs = h->I / 128;
+      g.hbuf = h->hbuf;
+      g.row_amax = h->row_amax;
+      CK(h, launch_gemm_w13s(g, std::min(h->num_sms, tb * g.w13_pairs), H / STAGE_K <= 8, s));
+      CK(h, launch_requant_rows(h->hbuf, h->row_amax, h->src_of_padrow, h->tiles, h->num_tiles, std::min(E, T * K),
+                                h->I, h->Ipad, h->h_codes, h->h_gs, s));
+    } else {
+      CK(h, launch_gemm_w13(g, h->I / 128, std::min(h->w13_clusters[tile_rows == 128], tb), tile_rows, s));
+    }
     CK(h, mark(h, 5, s));
     // w2: A = requantized intermediate [Rpad, Ipad], B = w2 [E*H, Ipad]
     GemmArgs g2{};
@@ -269,6 +325,8 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
     g2.ybuf = h->ybuf;
     g2.hidden = H;
     g2.n_tiles = H / TILE_N;
+    g2.num_experts = E;
+    g2.prefetch_units = small ? W2_PREFETCH_UNITS : 0;
     CK(h, launch_gemm_w2(g2, std::min(h->num_sms, tb * g2.n_tiles), h->deterministic, tile_rows, s));
     CK(h, mark(h, 6, s));
     if (h->deterministic) CK(h, launch_finalize_ordered(h->ybuf, h->topk_w, out, T, H, K, s));
@@ -276,6 +334,7 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
     CK(h, mark(h, 7, s));
   }
   h->last_T = T;
+  h->last_small = T > 0 && T <= SMALL_BATCH_TOKENS;
   return MOE_OK;
 }
 
@@ -326,7 +385,8 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
   h->Tmax = T;
   h->Ipad = (I + 255) / 256 * 256;
   h->Rmax = T * K;
-  h->tile_cap = std::max(tile_bound(T, K, E, 128), tile_bound(std::min(T, SMALL_BATCH_TOKENS), K, E, 32));
+  // small batches: one tile (one 128-row block) per expert with rows
+  h->tile_cap = std::max(tile_bound(T, K, E, 128), E);
   h->Rpad = h->tile_cap * 128;
   h->deterministic = (cfg->flags & MOE_FLAG_DETERMINISTIC) != 0;
 
@@ -359,6 +419,10 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
   A(h->src_of_padrow, sizeof(int32_t) * Rp);
   A(h->tiles, sizeof(int4) * (size_t)h->tile_cap);
   A(h->num_tiles, sizeof(int32_t) * 4);
+  A(h->front_sync, sizeof(uint32_t) * FRONT_SYNC_WORDS);
+  // small batches: FP32 SwiGLU rows and row maxima of the expert blocks
+  A(h->hbuf, sizeof(float) * (size_t)E * 128 * h->Ipad);
+  A(h->row_amax, sizeof(float) * (size_t)E * 128);
   A(h->a_codes, operand_bytes(Rp, H / 2));
   h->a_sf = h->a_codes;
   A(h->gs_rows, sizeof(float) * Rp);
@@ -383,9 +447,10 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
     cudaError_t e = gemm_setup_attributes(I / 128);
     if (e != cudaSuccess) return fail(cuda_fail(h, e, "cudaFuncSetAttribute"));
     e = router_setup(H, E);
+    if (e == cudaSuccess) e = front_setup(H, E);
     if (e != cudaSuccess) return fail(cuda_fail(h, e, "cudaFuncSetAttribute(router)"));
     h->num_sms = prop.multiProcessorCount;
-    h->w13_clusters[0] = gemm_w13_max_clusters(I / 128, 32);
+    h->w13_clusters[0] = gemm_w13_max_clusters(I / 128, 64);
     h->w13_clusters[1] = gemm_w13_max_clusters(I / 128, 128);
     if (h->w13_clusters[0] <= 0 || h->w13_clusters[1] <= 0) {
       set_err(h, "no thread-block cluster of %d CTAs fits on the device", I / 128);
@@ -589,8 +654,13 @@ moe_status moe_debug_act_quant(moe_handle* h, uint8_t* codes, uint8_t* sf, float
   // token t's quantization is the one written to its slot-0 expanded row,
   // pad_row_of_src[t*K].
   if (h->last_T == 0) return MOE_OK;
-  CK(h, launch_export_rows(h->a_codes, h->a_sf, h->gs_rows, h->last_T, h->H, h->H, h->pad_row_of_src, h->K, 0, 0,
-                           codes, sf, gs, reinterpret_cast<cudaStream_t>(stream)));
+  // (small batches: row t of the shared activation tile)
+  if (h->last_small)
+    CK(h, launch_export_rows(h->a_codes, h->a_sf, h->gs_rows, h->last_T, h->H, h->H, nullptr, 0, 1, 0, codes, sf,
+                             gs, reinterpret_cast<cudaStream_t>(stream)));
+  else
+    CK(h, launch_export_rows(h->a_codes, h->a_sf, h->gs_rows, h->last_T, h->H, h->H, h->pad_row_of_src, h->K, 0,
+                             0, codes, sf, gs, reinterpret_cast<cudaStream_t>(stream)));
   return MOE_OK;
 }
 
