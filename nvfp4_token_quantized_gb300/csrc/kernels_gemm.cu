@@ -62,11 +62,18 @@ constexpr int TMEM_COLS = 512;
 constexpr int TMEM_SF_BASE = 2 * TILE_N;     // two accumulator buffers in columns [0, 256)
 constexpr int TMEM_SF_STAGE = 32;            // 16 columns SFA + 16 columns SFB per stage
 constexpr uint32_t IDESC = idesc_fp4(TILE_M, TILE_N);
+// Column-pair kernels (w13): one 128 x 256 accumulator in columns [0, 256)
+// fed by N = 256 MMAs over both 128-row weight tiles of a pair; the B scale
+// factors of a K block take 8 columns (rows 128..255 after rows 0..127).
+constexpr int TMEM_SF_STAGE_PAIR = 48;       // 16 columns SFA + 32 columns SFB per stage
+constexpr uint32_t IDESC_PAIR = idesc_fp4(TILE_M, 2 * TILE_N);
+constexpr int MAX_STAGES_PAIR = 5;
 constexpr int THREADS = 192;
 constexpr int EPI_WARPS = 4;
 constexpr int CTRL_BYTES = 256;
 constexpr int MAX_SMEM = 232448;
 static_assert(TMEM_SF_BASE + MAX_STAGES * TMEM_SF_STAGE <= TMEM_COLS, "tensor memory overflow");
+static_assert(TMEM_SF_BASE + MAX_STAGES_PAIR * TMEM_SF_STAGE_PAIR <= TMEM_COLS, "tensor memory overflow");
 
 // MODE_W13S: the small-batch w13 GEMM without clusters - its epilogue writes
 // the FP32 SwiGLU rows and folds each row's absolute maximum into a global
@@ -88,16 +95,21 @@ static_assert(sizeof(Ctrl) <= CTRL_BYTES, "control block too large");
 // A slot: [2 KB scales | a_rows x 128 bytes of codes]
 __host__ __device__ constexpr int a_slot_bytes(int a_rows) { return OPERAND_SF_BYTES + a_rows * 128; }
 __host__ __device__ constexpr int a_tail_bytes(int a_rows) { return (TILE_M - a_rows) * 128; }
-__host__ __device__ constexpr int stage_bytes(int a_rows) { return a_slot_bytes(a_rows) + B_SLOT; }
-__host__ __device__ constexpr int smem_bytes_for(int stages, int nch, int a_rows) {
-  return stages * stage_bytes(a_rows) + a_tail_bytes(a_rows) + CTRL_BYTES + 2 * nch * TILE_M * 4 + 1024;
+// B slot: one 18 KB weight tile, or for column pairs [scales a | scales b |
+// codes a | codes b] (36 KB), so the pair's 256 rows of codes are contiguous.
+__host__ __device__ constexpr int b_slot_bytes(bool pair) { return pair ? 2 * B_SLOT : B_SLOT; }
+__host__ __device__ constexpr int stage_bytes(int a_rows, bool pair = false) {
+  return a_slot_bytes(a_rows) + b_slot_bytes(pair);
+}
+__host__ __device__ constexpr int smem_bytes_for(int stages, int nch, int a_rows, bool pair = false) {
+  return stages * stage_bytes(a_rows, pair) + a_tail_bytes(a_rows) + CTRL_BYTES + 2 * nch * TILE_M * 4 + 1024;
 }
 // Resident activations (the small-batch w13 GEMM, whose tiles all read the
 // same shared activation tile): all K stages of A stay in shared memory for
 // the whole kernel, loaded once; the ring carries only weight tiles.
 constexpr int ARES_MAX_KS = 8;  // K <= 2048
-__host__ __device__ constexpr int smem_bytes_res(int stages, int nch, int a_rows) {
-  return ARES_MAX_KS * a_slot_bytes(a_rows) + a_tail_bytes(a_rows) + stages * B_SLOT + CTRL_BYTES +
+__host__ __device__ constexpr int smem_bytes_res(int stages, int nch, int a_rows, bool pair = false) {
+  return ARES_MAX_KS * a_slot_bytes(a_rows) + a_tail_bytes(a_rows) + stages * b_slot_bytes(pair) + CTRL_BYTES +
          2 * nch * TILE_M * 4 + 1024;
 }
 
@@ -121,11 +133,15 @@ template <int MODE, int A_ROWS, int STAGES, bool ARES>
 __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_constant__ GemmArgs p) {
   constexpr int A_SLOT = a_slot_bytes(A_ROWS);
   constexpr int A_SLOTS = ARES ? ARES_MAX_KS : STAGES;  // resident: one slot per K stage
+  constexpr bool PAIR = (MODE == MODE_W13 || MODE == MODE_W13S);  // N = 256 over column pairs
+  constexpr int BS = b_slot_bytes(PAIR);
+  constexpr int SF_STAGE = PAIR ? TMEM_SF_STAGE_PAIR : TMEM_SF_STAGE;
+  static_assert(!PAIR || STAGES <= MAX_STAGES_PAIR, "tensor memory overflow");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = base;                                          // [A_SLOTS][A_SLOT] + tail
-  uint8_t* sB = sA + A_SLOTS * A_SLOT + a_tail_bytes(A_ROWS);  // [STAGES][B_SLOT]
-  Ctrl& c = *reinterpret_cast<Ctrl*>(sB + STAGES * B_SLOT);
+  uint8_t* sB = sA + A_SLOTS * A_SLOT + a_tail_bytes(A_ROWS);  // [STAGES][BS]
+  Ctrl& c = *reinterpret_cast<Ctrl*>(sB + STAGES * BS);
   // [2][nch][128] words: partial row maximum bits (non-negative, so bit 31
   // is free) with bit 31 holding the m-tile tag
   uint32_t* part = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(&c) + CTRL_BYTES);
@@ -240,12 +256,12 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
           bulk_load(sA + ks * A_SLOT, a_src + (size_t)ks * OPERAND_TILE_BYTES, a_bytes, &c.a_full);
         a_issued = true;
       }
-      for (int u = first; u < nunits && !c.abort_flag; u = next(u)) {
+      for (int u = first; u < nunits && !c.abort_flag; u = PAIR ? next(next(u)) : next(u)) {
         const Unit un = unit_at(u);
         const int brow0 = (MODE == MODE_PLAIN ? 0 : un.e * p.b_rows_per_expert) + un.col * TILE_N;
         // scales + valid rows, in whole 8-row swizzle groups
         const uint32_t a_bytes = OPERAND_SF_BYTES + (uint32_t)((un.valid + 7) & ~7) * 128;
-        const uint32_t bytes = (ARES ? 0u : a_bytes) + B_SLOT;
+        const uint32_t bytes = (ARES ? 0u : a_bytes) + BS;
         const uint8_t* a_src = p.a_codes + (size_t)(un.arow >> 7) * KS * OPERAND_TILE_BYTES;
         const uint8_t* b_src = p.b_codes + (size_t)(brow0 >> 7) * KS * OPERAND_TILE_BYTES;
         for (int ks = 0; ks < KS; ++ks, ++g) {
@@ -257,7 +273,19 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
           }
           mbar_arrive_expect_tx(&c.full[s], bytes);
           if (!ARES) bulk_load(sA + s * A_SLOT, a_src + (size_t)ks * OPERAND_TILE_BYTES, a_bytes, &c.full[s]);
-          bulk_load(sB + s * B_SLOT, b_src + (size_t)ks * OPERAND_TILE_BYTES, B_SLOT, &c.full[s]);
+          uint8_t* slot_b = sB + s * BS;
+          const uint8_t* tile_a = b_src + (size_t)ks * OPERAND_TILE_BYTES;
+          if constexpr (PAIR) {
+            // the pair's second tile is the next 128-row block of the expert
+            const uint8_t* tile_b = tile_a + (size_t)KS * OPERAND_TILE_BYTES;
+            bulk_load(slot_b, tile_a, OPERAND_SF_BYTES, &c.full[s]);
+            bulk_load(slot_b + OPERAND_SF_BYTES, tile_b, OPERAND_SF_BYTES, &c.full[s]);
+            bulk_load(slot_b + 2 * OPERAND_SF_BYTES, tile_a + OPERAND_SF_BYTES, OPERAND_CODE_BYTES, &c.full[s]);
+            bulk_load(slot_b + 2 * OPERAND_SF_BYTES + OPERAND_CODE_BYTES, tile_b + OPERAND_SF_BYTES, OPERAND_CODE_BYTES,
+                      &c.full[s]);
+          } else {
+            bulk_load(slot_b, tile_a, B_SLOT, &c.full[s]);
+          }
         }
       }
       if (c.abort_flag) {
@@ -278,10 +306,12 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
         c.abort_flag = 1;
         report_device_error(p.status, DEV_ERR_TIMEOUT);
       }
-      for (int u = first; u < nunits; u = next(u), ++n) {
+      for (int u = first; u < nunits; u = PAIR ? next(next(u)) : next(u), ++n) {
         if (c.abort_flag) break;
-        const int buf = n & 1;
-        if (!mbar_wait_bounded(&c.acc_empty[buf], ((n >> 1) & 1) ^ 1, &c.abort_flag)) {
+        // column pairs: one accumulator (buffer 0), used by every pair
+        const int buf = PAIR ? 0 : n & 1;
+        const uint32_t acc_parity = PAIR ? ((n & 1) ^ 1) : (((n >> 1) & 1) ^ 1);
+        if (!mbar_wait_bounded(&c.acc_empty[buf], acc_parity, &c.abort_flag)) {
           c.abort_flag = 1;
           report_device_error(p.status, DEV_ERR_TIMEOUT);
           break;
@@ -296,21 +326,25 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
             break;
           }
           tc_fence_after();
-          const uint32_t sfa_t = tmem + TMEM_SF_BASE + s * TMEM_SF_STAGE;
+          const uint32_t sfa_t = tmem + TMEM_SF_BASE + s * SF_STAGE;
           const uint32_t sfb_t = sfa_t + 16;
           const uint8_t* slot_a = sA + (ARES ? ks : s) * A_SLOT;
-          const uint8_t* slot_b = sB + s * B_SLOT;
+          const uint8_t* slot_b = sB + s * BS;
+          constexpr int SFB_COLS = PAIR ? 8 : 4;  // B scale columns per K block
 #pragma unroll
           for (int kb = 0; kb < 4; ++kb) {
             tc_copy_sf(sfa_t + kb * 4, smem_desc_sf(smem_u32(slot_a + kb * SF_ATOM_BYTES)));
-            tc_copy_sf(sfb_t + kb * 4, smem_desc_sf(smem_u32(slot_b + kb * SF_ATOM_BYTES)));
+            tc_copy_sf(sfb_t + kb * SFB_COLS, smem_desc_sf(smem_u32(slot_b + kb * SF_ATOM_BYTES)));
+            if (PAIR)
+              tc_copy_sf(sfb_t + kb * SFB_COLS + 4,
+                         smem_desc_sf(smem_u32(slot_b + OPERAND_SF_BYTES + kb * SF_ATOM_BYTES)));
           }
           const uint32_t a_base = smem_u32(slot_a + OPERAND_SF_BYTES);
-          const uint32_t b_base = smem_u32(slot_b + OPERAND_SF_BYTES);
+          const uint32_t b_base = smem_u32(slot_b + (PAIR ? 2 : 1) * OPERAND_SF_BYTES);
 #pragma unroll
           for (int kb = 0; kb < 4; ++kb)
-            tc_mma_fp4(d_tmem, smem_desc_sw128(a_base + kb * 32), smem_desc_sw128(b_base + kb * 32), IDESC,
-                       sfa_t + kb * 4, sfb_t + kb * 4, (ks | kb) != 0);
+            tc_mma_fp4(d_tmem, smem_desc_sw128(a_base + kb * 32), smem_desc_sw128(b_base + kb * 32),
+                       PAIR ? IDESC_PAIR : IDESC, sfa_t + kb * 4, sfb_t + kb * SFB_COLS, (ks | kb) != 0);
           tc_commit(&c.empty[s]);
         }
         // Always signal, even after an abort: the epilogue waits for the
@@ -354,13 +388,18 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
         const float alpha = row_ok ? __fdiv_rn(1.0f, __fmul_rn(p.gs_rows[un.arow + m], p.gs_w[un.e])) : 0.0f;
         float h[128];
         float amax = 0.0f;
-        bool ready = true;
+        // the pair's 128 x 256 accumulator: columns [0, 128) then [128, 256)
+        bool ready = mbar_wait_bounded(&c.acc_full[0], i & 1, nullptr);
+        if (!ready) {
+          c.abort_flag = 1;
+          report_device_error(p.status, DEV_ERR_TIMEOUT);
+        }
+        tc_fence_after();
+        ready = ready && !c.abort_flag;
 #pragma unroll
-        for (int j = 0; j < 2; ++j, ++n) {
-          const int buf = n & 1;
-          ready = wait_acc(buf, n) && ready;
+        for (int j = 0; j < 2; ++j) {
           if (ready && warp_rows) {
-            const uint32_t t = lane_base + buf * TILE_N;
+            const uint32_t t = lane_base + j * TILE_N;
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
               float gv[32], uv[32];
@@ -375,8 +414,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
               }
             }
           }
-          release_acc(buf);  // the tensor cores may refill this buffer now
         }
+        release_acc(0);  // the tensor cores may refill the accumulator now
         if (!row_ok) amax = 0.0f;
         if constexpr (MODE == MODE_W13S) {
           // FP32 SwiGLU row to the scratch, its maximum folded into the
@@ -505,20 +544,21 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
   }
 }
 
-constexpr int stages_for(int nch, int a_rows) {
-  for (int s = MAX_STAGES; s >= 3; --s)
-    if (smem_bytes_for(s, nch, a_rows) <= MAX_SMEM) return s;
+constexpr int stages_for(int nch, int a_rows, bool pair = false) {
+  for (int s = pair ? MAX_STAGES_PAIR : MAX_STAGES; s >= 3; --s)
+    if (smem_bytes_for(s, nch, a_rows, pair) <= MAX_SMEM) return s;
   return 0;
 }
-constexpr int stages_for_res(int nch, int a_rows) {
-  for (int s = MAX_STAGES; s >= 3; --s)
-    if (smem_bytes_res(s, nch, a_rows) <= MAX_SMEM) return s;
+constexpr int stages_for_res(int nch, int a_rows, bool pair = false) {
+  for (int s = pair ? MAX_STAGES_PAIR : MAX_STAGES; s >= 3; --s)
+    if (smem_bytes_res(s, nch, a_rows, pair) <= MAX_SMEM) return s;
   return 0;
 }
 
 template <int MODE, int A_ROWS, int STAGES, bool ARES>
 constexpr int kernel_smem(int nch) {
-  return ARES ? smem_bytes_res(STAGES, nch, A_ROWS) : smem_bytes_for(STAGES, nch, A_ROWS);
+  constexpr bool pair = (MODE == MODE_W13 || MODE == MODE_W13S);
+  return ARES ? smem_bytes_res(STAGES, nch, A_ROWS, pair) : smem_bytes_for(STAGES, nch, A_ROWS, pair);
 }
 
 // The shared-memory cap belongs to the kernel instantiation, which handles of
@@ -575,14 +615,15 @@ cudaError_t launch(const GemmArgs& a, dim3 grid, int nch, cudaStream_t s) {
 // clusters one stage less.
 constexpr int W2_STAGES_128 = stages_for(0, 128);
 constexpr int W2_STAGES_64 = stages_for(0, 64);
-constexpr int W13_STAGES_128 = stages_for(6, 128);
-constexpr int W13_STAGES_128_L = stages_for(16, 128);
-constexpr int W13_STAGES_64 = stages_for(6, 64);
-constexpr int W13_STAGES_64_L = stages_for(16, 64);
-constexpr int W13S_STAGES_RES = stages_for_res(0, 64);
-constexpr int W13S_STAGES = stages_for(0, 64);
-static_assert(W2_STAGES_128 >= 4 && W13_STAGES_128_L >= 3 && W13_STAGES_64_L >= 4 && W13S_STAGES_RES >= 4,
+constexpr int W13_STAGES_128 = stages_for(6, 128, true);
+constexpr int W13_STAGES_128_L = stages_for(16, 128, true);
+constexpr int W13_STAGES_64 = stages_for(6, 64, true);
+constexpr int W13_STAGES_64_L = stages_for(16, 64, true);
+constexpr int W13S_STAGES_RES = stages_for_res(0, 64, true);
+constexpr int W13S_STAGES = stages_for(0, 64, true);
+static_assert(W2_STAGES_128 >= 4 && W13_STAGES_128_L >= 3 && W13_STAGES_64_L >= 3 && W13S_STAGES_RES >= 3,
               "ring too shallow");
+static_assert(W13_STAGES_128 >= 4 && W13S_STAGES >= 4, "ring too shallow");
 
 template <typename F>
 cudaError_t with_w13(int nch, int a_rows, F&& f) {

@@ -294,13 +294,14 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
     g.num_experts = E;
     g.prefetch_units = small ? W13_PREFETCH_UNITS : 0;
     if (small) {
-      // every tile reads the one shared activation tile (kept resident when
-      // K <= 2048); no clusters: the units spread over all SMs, and the
-      // requantization follows as its own kernel
+      // every tile reads the one shared activation tile; no clusters: the
+      // units spread over all SMs, and the requantization follows as its own
+      // kernel.  The tile is streamed with the weights: keeping it resident
+      // costs a ring stage, which measured slower.
       g.w13_pairs = h->I / 128;
       g.hbuf = h->hbuf;
       g.row_amax = h->row_amax;
-      CK(h, launch_gemm_w13s(g, std::min(h->num_sms, tb * g.w13_pairs), H / STAGE_K <= 8, s));
+      CK(h, launch_gemm_w13s(g, std::min(h->num_sms, tb * g.w13_pairs), false, s));
       CK(h, launch_requant_rows(h->hbuf, h->row_amax, h->src_of_padrow, h->tiles, h->num_tiles, std::min(E, T * K),
                                 h->I, h->Ipad, h->h_codes, h->h_gs, s));
     } else {
