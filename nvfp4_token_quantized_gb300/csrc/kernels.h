@@ -133,7 +133,6 @@ struct GemmArgs {
   float* row_amax;
 };
 
-int gemm_smem_bytes();
 cudaError_t gemm_setup_attributes(int w13_chunks);
 // Thread-block clusters of the w13 kernel (w13_chunks CTAs each) that fit on
 // the device at once; 0 if none.

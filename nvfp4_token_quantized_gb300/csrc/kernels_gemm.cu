@@ -2,20 +2,26 @@
 // on the sm_103a tensor cores (tcgen05.mma kind::mxf4nvf4, E2M1 operands with
 // UE4M3 scales per 16 elements, FP32 accumulators in tensor memory).
 //
-// Persistent kernels.  A work unit is one 128-row x 128-column MMA tile of
-// one expert; each CTA (w2, plain) or cluster (w13) walks a static list.
-//   warp 0      producer: per 256-element K stage, two bulk copies into a
-//               STAGES-deep shared-memory ring - the B tile (its 2 KB of
-//               block scales and 16 KB of pre-swizzled codes are one
-//               contiguous 18 KB block) and the A tile's scales plus its
-//               valid rows - running ahead across unit boundaries;
+// Persistent kernels.  A work unit is one 128-row x 128-column tile of one
+// expert; the expert GEMMs take units in pairs of adjacent 128-column tiles
+// and compute a pair as one 128 x 256 tile.  Each CTA (w2, plain) or cluster
+// (w13) walks a static list.
+//   warp 0      producer: per 256-element K stage, bulk copies into a
+//               STAGES-deep shared-memory ring - the activation tile's
+//               scales plus its valid rows, and the weight tile(s) (a pair
+//               is staged as [scales a | scales b | codes a | codes b] so its
+//               256 rows of pre-swizzled codes are contiguous) - running
+//               ahead across unit boundaries;
 //   warp 1      tensor-memory allocation and the single MMA-issuing thread:
 //               block scales shared -> tensor memory (tcgen05.cp), then four
-//               K=64 MMAs per 256-element stage, into one of two accumulator
-//               buffers (tensor-memory columns [0,128) and [128,256));
+//               K=64 MMAs per 256-element stage: N = 256 into the one
+//               256-column accumulator (pairs), or N = 128 into one of two
+//               128-column buffers (plain);
 //   warps 2-5   epilogue, one accumulator row (tensor-memory lane) per thread.
-// With two accumulator buffers the epilogue drains unit u while the tensor
-// cores compute unit u+1, so weight streaming never waits for an epilogue.
+// With two accumulator buffers (plain) the epilogue drains unit u while the
+// tensor cores compute unit u+1; with one 256-column accumulator (pairs) the
+// tensor cores wait only for the epilogue's tensor-memory reads, while the
+// ring keeps streaming weights.
 //
 // Epilogues:
 //   w13  a unit's 128 columns are 64 gate features and the matching 64 up
@@ -81,6 +87,11 @@ static_assert(TMEM_SF_BASE + MAX_STAGES_PAIR * TMEM_SF_STAGE_PAIR <= TMEM_COLS, 
 // fused requantization).
 enum Mode { MODE_W13 = 0, MODE_W2_ATOMIC = 1, MODE_W2_ORDERED = 2, MODE_PLAIN = 3, MODE_W13S = 4 };
 
+// The expert GEMMs take their 128-column units in pairs (N = 256 MMAs); the
+// plain GEMM (tests) does not.  The one definition the kernel's shared-memory
+// layout and the host's launch size both use.
+__host__ __device__ constexpr bool pair_mode(int mode) { return mode != MODE_PLAIN; }
+
 struct Ctrl {
   uint64_t full[MAX_STAGES];
   uint64_t empty[MAX_STAGES];
@@ -133,7 +144,7 @@ template <int MODE, int A_ROWS, int STAGES, bool ARES>
 __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_constant__ GemmArgs p) {
   constexpr int A_SLOT = a_slot_bytes(A_ROWS);
   constexpr int A_SLOTS = ARES ? ARES_MAX_KS : STAGES;  // resident: one slot per K stage
-  constexpr bool PAIR = (MODE == MODE_W13 || MODE == MODE_W13S);  // N = 256 over column pairs
+  constexpr bool PAIR = pair_mode(MODE);  // N = 256 over pairs of adjacent 128-column tiles
   constexpr int BS = b_slot_bytes(PAIR);
   constexpr int SF_STAGE = PAIR ? TMEM_SF_STAGE_PAIR : TMEM_SF_STAGE;
   static_assert(!PAIR || STAGES <= MAX_STAGES_PAIR, "tensor memory overflow");
@@ -145,13 +156,26 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
   // [2][nch][128] words: partial row maximum bits (non-negative, so bit 31
   // is free) with bit 31 holding the m-tile tag
   uint32_t* part = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(&c) + CTRL_BYTES);
+  {
+    // The layout above must fit the launch's dynamic shared memory; if the
+    // host sized it differently, report and leave before touching any of it
+    // (the condition is the same in every CTA of the grid).
+    uint32_t dyn;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+    const uint8_t* end = reinterpret_cast<const uint8_t*>(part) + (MODE == MODE_W13 ? 2 * gridDim.x * TILE_M * 4 : 0);
+    if (end > smem_raw + dyn) {
+      if (threadIdx.x == 0) report_device_error(p.status, DEV_ERR_BAD_STATE);
+      return;
+    }
+  }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- static schedule, identical in every role ----
   // w13: cluster blockIdx.y takes m-tiles blockIdx.y, +gridDim.y, ...; CTA
   //      rank r of the cluster takes units (m-tile, B column blocks 2r, 2r+1).
-  // w2 / plain: CTA b takes units b, b + gridDim.x, ... of (m-tile, n-tile).
+  // w2: CTA b takes unit pairs b, b + gridDim.x, ... of (m-tile, n-tiles
+  //      2c, 2c+1); plain: CTA b takes units b, b + gridDim.x, ...
   // w13s: CTA b takes unit pairs b, b + gridDim.x, ... of (m-tile, column
   //      pair r), pair index = m-tile * (I/128) + r.
   constexpr bool W13L = (MODE == MODE_W13 || MODE == MODE_W13S);  // units in column pairs
@@ -162,7 +186,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
   if constexpr (MODE == MODE_W13) {
     first = 2 * blockIdx.y;
     stride = 2 * gridDim.y;
-  } else if constexpr (MODE == MODE_W13S) {
+  } else if constexpr (PAIR) {  // w13s, w2: unit pairs b, b + gridDim.x, ...
     first = 2 * blockIdx.x;
     stride = 2 * gridDim.x;
   } else {
@@ -171,7 +195,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
   }
   // w13 units come in pairs (2 per m-tile); `next` skips to the next pair.
   auto next = [&](int u) -> int {
-    if constexpr (W13L) return (u & 1) ? u - 1 + stride : u + 1;
+    if constexpr (PAIR) return (u & 1) ? u - 1 + stride : u + 1;
     else return u + stride;
   };
   auto unit_at = [&](int u) -> Unit {
@@ -476,7 +500,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
         }
       }
     } else {
-      for (int u = first; u < nunits; u = next(u), ++n) {
+      for (int u = first; u < nunits; u = PAIR ? next(next(u)) : next(u), ++n) {
         const Unit un = unit_at(u);
         const bool warp_rows = quarter * 32 < un.valid;
         const int prow = un.row0 + m;
@@ -486,8 +510,20 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
           src = row_ok ? p.src_of_padrow[prow] : -1;
           row_ok = src >= 0;  // a token that did not pick this expert
         }
-        const int buf = n & 1;
-        const bool ready = wait_acc(buf, n);
+        // pairs: one 128 x 256 accumulator (buffer 0) holding both tiles
+        const int buf = PAIR ? 0 : n & 1;
+        bool ready;
+        if constexpr (PAIR) {
+          ready = mbar_wait_bounded(&c.acc_full[0], n & 1, nullptr);
+          if (!ready) {
+            c.abort_flag = 1;
+            report_device_error(p.status, DEV_ERR_TIMEOUT);
+          }
+          tc_fence_after();
+          ready = ready && !c.abort_flag;
+        } else {
+          ready = wait_acc(buf, n);
+        }
         if (ready && warp_rows) {
           float alpha = 0.0f, wj = 0.0f;
           if (MODE != MODE_PLAIN && row_ok) {
@@ -495,15 +531,16 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
             wj = p.topk_w[src];
           }
           const int tok = src / (p.top_k > 0 ? p.top_k : 1);
-          const int n0 = un.col * TILE_N;
-          const uint32_t t = lane_base + buf * TILE_N;
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
+          for (int part = 0; part < (PAIR ? 4 : 2); ++part) {  // 64-column parts
+            const int j = part >> 1, half = part & 1;
+            const int n0 = (un.col + j) * TILE_N;
+            const uint32_t t = lane_base + (PAIR ? j : buf) * TILE_N;
             float a[64];
             tmem_ld32(t + 64 * half, a);
             tmem_ld32(t + 64 * half + 32, a + 32);
             tmem_ld_wait();
-            if (half == 1) release_acc(buf);  // everything is in registers now
+            if (part == (PAIR ? 3 : 1)) release_acc(buf);  // everything is in registers now
             if (row_ok) {
               const int col = n0 + 64 * half;
               if constexpr (MODE == MODE_W2_ATOMIC) {
@@ -557,7 +594,7 @@ constexpr int stages_for_res(int nch, int a_rows, bool pair = false) {
 
 template <int MODE, int A_ROWS, int STAGES, bool ARES>
 constexpr int kernel_smem(int nch) {
-  constexpr bool pair = (MODE == MODE_W13 || MODE == MODE_W13S);
+  constexpr bool pair = pair_mode(MODE);
   return ARES ? smem_bytes_res(STAGES, nch, A_ROWS, pair) : smem_bytes_for(STAGES, nch, A_ROWS, pair);
 }
 
@@ -613,15 +650,16 @@ cudaError_t launch(const GemmArgs& a, dim3 grid, int nch, cudaStream_t s) {
 // Ring depths that occur: w2 / plain kernels (no exchange slots) and w13
 // kernels with clusters of up to 6 CTAs get the deepest ring that fits; larger
 // clusters one stage less.
-constexpr int W2_STAGES_128 = stages_for(0, 128);
-constexpr int W2_STAGES_64 = stages_for(0, 64);
+constexpr int W2_STAGES_128 = stages_for(0, 128, true);
+constexpr int W2_STAGES_64 = stages_for(0, 64, true);
+constexpr int PLAIN_STAGES = stages_for(0, 128);
 constexpr int W13_STAGES_128 = stages_for(6, 128, true);
 constexpr int W13_STAGES_128_L = stages_for(16, 128, true);
 constexpr int W13_STAGES_64 = stages_for(6, 64, true);
 constexpr int W13_STAGES_64_L = stages_for(16, 64, true);
 constexpr int W13S_STAGES_RES = stages_for_res(0, 64, true);
 constexpr int W13S_STAGES = stages_for(0, 64, true);
-static_assert(W2_STAGES_128 >= 4 && W13_STAGES_128_L >= 3 && W13_STAGES_64_L >= 3 && W13S_STAGES_RES >= 3,
+static_assert(W2_STAGES_128 >= 4 && PLAIN_STAGES >= 4 && W13_STAGES_128_L >= 3 && W13_STAGES_64_L >= 3 && W13S_STAGES_RES >= 3,
               "ring too shallow");
 static_assert(W13_STAGES_128 >= 4 && W13S_STAGES >= 4, "ring too shallow");
 
@@ -637,8 +675,6 @@ cudaError_t with_w13(int nch, int a_rows, F&& f) {
 }
 
 }  // namespace
-
-int gemm_smem_bytes() { return smem_bytes_for(W2_STAGES_128, 0, 128); }
 
 cudaError_t gemm_setup_attributes(int nch) {
   static std::mutex m;
@@ -656,7 +692,7 @@ cudaError_t gemm_setup_attributes(int nch) {
   if ((e = set_attrs<MODE_W2_ATOMIC, 64, W2_STAGES_64>(0)) != cudaSuccess) return e;
   if ((e = set_attrs<MODE_W2_ORDERED, 128, W2_STAGES_128>(0)) != cudaSuccess) return e;
   if ((e = set_attrs<MODE_W2_ORDERED, 64, W2_STAGES_64>(0)) != cudaSuccess) return e;
-  return set_attrs<MODE_PLAIN, 128, W2_STAGES_128>(0);
+  return set_attrs<MODE_PLAIN, 128, PLAIN_STAGES>(0);
 }
 
 int gemm_w13_max_clusters(int nch, int a_rows) {
@@ -699,7 +735,7 @@ cudaError_t launch_gemm_w2(const GemmArgs& a, int n_ctas, bool ordered, int a_ro
 }
 
 cudaError_t launch_gemm_plain(const GemmArgs& a, int n_ctas, cudaStream_t s) {
-  return launch<MODE_PLAIN, 128, W2_STAGES_128>(a, dim3(n_ctas, 1, 1), 0, s);
+  return launch<MODE_PLAIN, 128, PLAIN_STAGES>(a, dim3(n_ctas, 1, 1), 0, s);
 }
 
 }  // namespace moe

@@ -328,7 +328,8 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
     g2.n_tiles = H / TILE_N;
     g2.num_experts = E;
     g2.prefetch_units = small ? W2_PREFETCH_UNITS : 0;
-    CK(h, launch_gemm_w2(g2, std::min(h->num_sms, tb * g2.n_tiles), h->deterministic, tile_rows, s));
+    // units are pairs of 128-column tiles
+    CK(h, launch_gemm_w2(g2, std::min(h->num_sms, tb * g2.n_tiles / 2), h->deterministic, tile_rows, s));
     CK(h, mark(h, 6, s));
     if (h->deterministic) CK(h, launch_finalize_ordered(h->ybuf, h->topk_w, out, T, H, K, s));
     else CK(h, launch_finalize_atomic(h->out_acc, out, T, H, s));
