@@ -66,6 +66,29 @@ __host__ __device__ __forceinline__ size_t sf_atom_offset(size_t row, int k16, i
          (size_t)((row & 31) * 16 + ((row >> 5) & 3) * 4 + (k16 & 3));
 }
 
+// Weights are read by the expert GEMMs as pairs of 128-row tiles (N = 256
+// MMAs), so they are stored as 256-row pair tiles: per (row / 256, K / 256)
+// one contiguous 36 KB block [scales of rows 0..127 | scales of rows
+// 128..255 | codes of rows 0..255], each part in the layout above (the codes'
+// swizzle uses row % 8, the same in both halves).  A pipeline stage fetches a
+// pair of weight tiles with one bulk copy.  Same total size as
+// operand_bytes(); rows a multiple of 256.
+constexpr int WPAIR_BYTES = 2 * OPERAND_TILE_BYTES;
+
+__host__ __device__ __forceinline__ size_t wpair_offset(size_t row, int kb, int row_bytes) {
+  const int stages = row_bytes >> 7;
+  const int r = (int)(row & 255), b = kb & 127;
+  return ((row >> 8) * stages + (size_t)(kb >> 7)) * WPAIR_BYTES + 2 * OPERAND_SF_BYTES + (size_t)r * 128 +
+         ((((b >> 4) ^ r) & 7) << 4) + (b & 15);
+}
+
+__host__ __device__ __forceinline__ size_t wpair_sf_offset(size_t row, int k16, int k16_per_row) {
+  const int stages = k16_per_row >> 4;
+  const int r = (int)(row & 255);
+  return ((row >> 8) * stages + (size_t)(k16 >> 4)) * WPAIR_BYTES + (size_t)(r >> 7) * OPERAND_SF_BYTES +
+         (size_t)((k16 >> 2) & 3) * SF_ATOM_BYTES + (size_t)((r & 31) * 16 + ((r >> 5) & 3) * 4 + (k16 & 3));
+}
+
 // ---------------------------------------------------------------------------
 // Generic helpers
 // ---------------------------------------------------------------------------

@@ -38,14 +38,17 @@ cudaError_t launch_permute(const int32_t* topk_ids, const int32_t* counts, int T
 cudaError_t launch_act_quant(const void* x, int T, int H, int K, const int32_t* pad_row_of_src,
                              uint8_t* a_codes, uint8_t* a_sf, float* gs_rows, float* out_acc, cudaStream_t s);
 cudaError_t launch_weight_amax(const void* w, int E, int N, int Kd, uint32_t* amax_bits, cudaStream_t s);
-// interleave: 0 = rows in caller order; 1 = w13 gate/up rows interleaved in
-// chunks of 64 so that internal chunk f (128 rows) is [gate f, up f].
+// Weights go to the pair-tile layout (wpair_offset).  interleave: 0 = rows
+// in caller order; 1 = w13 gate/up rows interleaved in chunks of 64 so that
+// internal chunk f (128 rows) is [gate f, up f].
 cudaError_t launch_weight_quant(const void* w, int E, int N, int Kd, int Kpad, int interleave,
                                 const uint32_t* amax_bits, uint8_t* codes, uint8_t* sf, float* gs,
                                 cudaStream_t s);
+// pair: the operand is a weight buffer (pair-tile layout).
 cudaError_t launch_export_rows(const uint8_t* codes, const uint8_t* sf, const float* gs_rows, int n_rows,
                                int Kd, int Kpad, const int32_t* row_map, int map_stride, int row_map_mode,
-                               int E_rows, uint8_t* out_codes, uint8_t* out_sf, float* out_gs, cudaStream_t s);
+                               int E_rows, int pair, uint8_t* out_codes, uint8_t* out_sf, float* out_gs,
+                               cudaStream_t s);
 cudaError_t launch_convert(const float* in, uint8_t* e2m1, uint8_t* e4m3, int64_t n, cudaStream_t s);
 cudaError_t launch_sf_to_atoms(const uint8_t* sf, int rows, int k16, uint8_t* atoms, cudaStream_t s);
 cudaError_t launch_codes_to_tiled(const uint8_t* codes, int rows, int row_bytes, uint8_t* tiled, cudaStream_t s);

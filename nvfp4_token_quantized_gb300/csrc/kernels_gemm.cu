@@ -252,9 +252,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
       const int col = (MODE == MODE_W13)    ? 2 * (int)rank + (u & 1)
                       : (MODE == MODE_W13S) ? 2 * ((u >> 1) % nch) + (u & 1)
                                             : u % p.n_tiles;
+      if (u & 1) continue;  // the pair block of an even unit holds both tiles
       const int brow0 = tile * p.b_rows_per_expert + col * TILE_N;
-      const uint8_t* b_src = p.b_codes + (size_t)(brow0 >> 7) * KS * OPERAND_TILE_BYTES;
-      for (int ks = 0; ks < KS; ++ks) prefetch_l2_bulk(b_src + (size_t)ks * OPERAND_TILE_BYTES, OPERAND_TILE_BYTES);
+      const uint8_t* b_src = p.b_codes + (size_t)(brow0 >> 8) * KS * WPAIR_BYTES;
+      for (int ks = 0; ks < KS; ++ks) prefetch_l2_bulk(b_src + (size_t)ks * WPAIR_BYTES, WPAIR_BYTES);
     }
   }
   // Everything above overlaps the previous kernel's tail; its outputs (the
@@ -298,17 +299,12 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
           mbar_arrive_expect_tx(&c.full[s], bytes);
           if (!ARES) bulk_load(sA + s * A_SLOT, a_src + (size_t)ks * OPERAND_TILE_BYTES, a_bytes, &c.full[s]);
           uint8_t* slot_b = sB + s * BS;
-          const uint8_t* tile_a = b_src + (size_t)ks * OPERAND_TILE_BYTES;
           if constexpr (PAIR) {
-            // the pair's second tile is the next 128-row block of the expert
-            const uint8_t* tile_b = tile_a + (size_t)KS * OPERAND_TILE_BYTES;
-            bulk_load(slot_b, tile_a, OPERAND_SF_BYTES, &c.full[s]);
-            bulk_load(slot_b + OPERAND_SF_BYTES, tile_b, OPERAND_SF_BYTES, &c.full[s]);
-            bulk_load(slot_b + 2 * OPERAND_SF_BYTES, tile_a + OPERAND_SF_BYTES, OPERAND_CODE_BYTES, &c.full[s]);
-            bulk_load(slot_b + 2 * OPERAND_SF_BYTES + OPERAND_CODE_BYTES, tile_b + OPERAND_SF_BYTES, OPERAND_CODE_BYTES,
-                      &c.full[s]);
+            // weights are stored in pair tiles: the stage is one 36 KB block
+            // [scales a | scales b | codes a | codes b]
+            bulk_load(slot_b, p.b_codes + ((size_t)(brow0 >> 8) * KS + ks) * WPAIR_BYTES, WPAIR_BYTES, &c.full[s]);
           } else {
-            bulk_load(slot_b, tile_a, B_SLOT, &c.full[s]);
+            bulk_load(slot_b, b_src + (size_t)ks * OPERAND_TILE_BYTES, B_SLOT, &c.full[s]);
           }
         }
       }

@@ -150,7 +150,7 @@ __device__ __forceinline__ int w13_internal_row(int n, int N) {
 }
 
 // One warp per (expert, row): block scales and codes of the row with the
-// expert's global scale, written into the internal operand layout.
+// expert's global scale, written into the weights' pair-tile layout.
 __global__ void __launch_bounds__(256) weight_quant_kernel(const __nv_bfloat16* __restrict__ w, int E, int N,
                                                           int Kd, int Kpad, int interleave,
                                                           const uint32_t* __restrict__ amax_bits,
@@ -169,8 +169,8 @@ __global__ void __launch_bounds__(256) weight_quant_kernel(const __nv_bfloat16* 
     bf16x16_to_f32(__ldg(src + 2 * b), __ldg(src + 2 * b + 1), v);
     uint2 packed;
     const uint32_t s = nvfp4_quant_block16(v, gs, packed);
-    *reinterpret_cast<uint2*>(codes + operand_offset(irow, 8 * b, Kpad / 2)) = packed;
-    sf[sf_atom_offset(irow, b, Kpad / SF_VEC)] = (uint8_t)s;
+    *reinterpret_cast<uint2*>(codes + wpair_offset(irow, 8 * b, Kpad / 2)) = packed;
+    sf[wpair_sf_offset(irow, b, Kpad / SF_VEC)] = (uint8_t)s;
   }
   if (n == 0 && lane == 0) gs_out[e] = gs;
 }
@@ -180,11 +180,13 @@ __global__ void __launch_bounds__(256) weight_quant_kernel(const __nv_bfloat16* 
 //         intermediate);
 // mode 1: internal row = i (weights in caller order);
 // mode 2: internal row = w13 interleave of i within its expert (E_rows rows per expert).
+// pair: the operand is in the weights' pair-tile layout.
 __global__ void __launch_bounds__(256) export_rows_kernel(const uint8_t* __restrict__ codes,
                                                          const uint8_t* __restrict__ sf,
                                                          const float* __restrict__ gs_rows, int n_rows, int Kd,
                                                          int Kpad, const int32_t* __restrict__ row_map,
-                                                         int map_stride, int mode, int E_rows, uint8_t* __restrict__ out_codes,
+                                                         int map_stride, int mode, int E_rows, int pair,
+                                                         uint8_t* __restrict__ out_codes,
                                                          uint8_t* __restrict__ out_sf, float* __restrict__ out_gs) {
   const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -195,10 +197,11 @@ __global__ void __launch_bounds__(256) export_rows_kernel(const uint8_t* __restr
   else r = (i / E_rows) * E_rows + w13_internal_row(i % E_rows, E_rows);
   if (out_codes)
     for (int b = lane; b < Kd / 2; b += 32)
-      out_codes[(size_t)i * (Kd / 2) + b] = codes[operand_offset(r, b, Kpad / 2)];
+      out_codes[(size_t)i * (Kd / 2) + b] = codes[pair ? wpair_offset(r, b, Kpad / 2) : operand_offset(r, b, Kpad / 2)];
   if (out_sf)
     for (int b = lane; b < Kd / SF_VEC; b += 32)
-      out_sf[(size_t)i * (Kd / SF_VEC) + b] = sf[sf_atom_offset(r, b, Kpad / SF_VEC)];
+      out_sf[(size_t)i * (Kd / SF_VEC) + b] =
+          sf[pair ? wpair_sf_offset(r, b, Kpad / SF_VEC) : sf_atom_offset(r, b, Kpad / SF_VEC)];
   if (out_gs && gs_rows && lane == 0) out_gs[i] = gs_rows[r];
 }
 
@@ -297,10 +300,10 @@ cudaError_t launch_weight_quant(const void* w, int E, int N, int Kd, int Kpad, i
 
 cudaError_t launch_export_rows(const uint8_t* codes, const uint8_t* sf, const float* gs_rows, int n_rows, int Kd,
                                int Kpad, const int32_t* row_map, int map_stride, int row_map_mode, int E_rows,
-                               uint8_t* out_codes, uint8_t* out_sf, float* out_gs, cudaStream_t s) {
+                               int pair, uint8_t* out_codes, uint8_t* out_sf, float* out_gs, cudaStream_t s) {
   if (n_rows <= 0) return cudaSuccess;
   export_rows_kernel<<<(n_rows + 7) / 8, 256, 0, s>>>(codes, sf, gs_rows, n_rows, Kd, Kpad, row_map, map_stride,
-                                                      row_map_mode, E_rows, out_codes, out_sf, out_gs);
+                                                      row_map_mode, E_rows, pair, out_codes, out_sf, out_gs);
   return cudaGetLastError();
 }
 

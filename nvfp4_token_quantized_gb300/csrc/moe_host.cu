@@ -658,11 +658,11 @@ moe_status moe_debug_act_quant(moe_handle* h, uint8_t* codes, uint8_t* sf, float
   if (h->last_T == 0) return MOE_OK;
   // (small batches: row t of the shared activation tile)
   if (h->last_small)
-    CK(h, launch_export_rows(h->a_codes, h->a_sf, h->gs_rows, h->last_T, h->H, h->H, nullptr, 0, 1, 0, codes, sf,
+    CK(h, launch_export_rows(h->a_codes, h->a_sf, h->gs_rows, h->last_T, h->H, h->H, nullptr, 0, 1, 0, 0, codes, sf,
                              gs, reinterpret_cast<cudaStream_t>(stream)));
   else
     CK(h, launch_export_rows(h->a_codes, h->a_sf, h->gs_rows, h->last_T, h->H, h->H, h->pad_row_of_src, h->K, 0,
-                             0, codes, sf, gs, reinterpret_cast<cudaStream_t>(stream)));
+                             0, 0, codes, sf, gs, reinterpret_cast<cudaStream_t>(stream)));
   return MOE_OK;
 }
 
@@ -673,10 +673,10 @@ moe_status moe_debug_weight_quant(moe_handle* h, int which, uint8_t* codes, uint
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (which == 0) {
     CK(h, launch_export_rows(h->w13_codes, h->w13_sf, nullptr, h->E * 2 * h->I, h->H, h->H, nullptr, 0, 2,
-                             2 * h->I, codes, sf, nullptr, s));
+                             2 * h->I, 1, codes, sf, nullptr, s));
     if (gs) CK(h, cudaMemcpyAsync(gs, h->gs_w13, sizeof(float) * h->E, cudaMemcpyDeviceToDevice, s));
   } else {
-    CK(h, launch_export_rows(h->w2_codes, h->w2_sf, nullptr, h->E * h->H, h->I, h->Ipad, nullptr, 0, 1, 0, codes,
+    CK(h, launch_export_rows(h->w2_codes, h->w2_sf, nullptr, h->E * h->H, h->I, h->Ipad, nullptr, 0, 1, 0, 1, codes,
                              sf, nullptr, s));
     if (gs) CK(h, cudaMemcpyAsync(gs, h->gs_w2, sizeof(float) * h->E, cudaMemcpyDeviceToDevice, s));
   }
@@ -689,7 +689,7 @@ moe_status moe_debug_intermediate(moe_handle* h, uint8_t* h_codes, uint8_t* h_sf
   DeviceGuard dg(h->cfg.device);
   if (h->last_T == 0) return MOE_OK;
   CK(h, launch_export_rows(h->h_codes, h->h_sf, h->h_gs, h->last_T * h->K, h->I, h->Ipad, h->pad_row_of_src, 1, 0,
-                           0, h_codes, h_sf, h_gs, reinterpret_cast<cudaStream_t>(stream)));
+                           0, 0, h_codes, h_sf, h_gs, reinterpret_cast<cudaStream_t>(stream)));
   return MOE_OK;
 }
 
