@@ -150,9 +150,8 @@ cudaError_t launch_gemm_w13(const GemmArgs& a, int n_chunks, int n_clusters, int
 // FP32 output into the w2 operand.  resident keeps the shared activation tile
 // in shared memory for the whole kernel (K <= 2048).
 cudaError_t launch_gemm_w13s(const GemmArgs& a, int n_ctas, bool resident, cudaStream_t s);
-cudaError_t launch_requant_rows(const float* hbuf, float* row_amax, const int32_t* src_of_padrow, const int4* tiles,
-                                const int32_t* num_tiles, int max_tiles, int I, int i_pad, uint8_t* h_codes,
-                                float* h_gs, cudaStream_t s);
+cudaError_t launch_requant_rows(const float* hbuf, float* row_amax, const int32_t* pad_row_of_src, int n_rows,
+                                int I, int i_pad, uint8_t* h_codes, float* h_gs, cudaStream_t s);
 cudaError_t launch_gemm_w2(const GemmArgs& a, int n_ctas, bool ordered, int a_rows, cudaStream_t s);
 cudaError_t launch_gemm_plain(const GemmArgs& a, int n_ctas, cudaStream_t s);
 

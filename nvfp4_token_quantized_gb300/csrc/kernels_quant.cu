@@ -70,25 +70,21 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __r
   }
 }
 
-// Requantization of the small-batch w13 output: one warp per (tile, row).
-// Row maximum -> global scale -> block scales and codes, the same arithmetic
-// as the fused w13 epilogue; returns the row's maximum word to zero.
-// grid (max tiles, 8): warp w of CTA (i, y) takes row 8*y + w of tile i.
+// Requantization of the small-batch w13 output: one warp per expanded row
+// (token * K + slot), at its padded row pad_row_of_src[row].  Row maximum ->
+// global scale -> block scales and codes, the same arithmetic as the fused
+// w13 epilogue; returns the row's maximum word to zero.
 __global__ void __launch_bounds__(256) requant_rows_kernel(const float* __restrict__ hbuf,
                                                           float* __restrict__ row_amax,
-                                                          const int32_t* __restrict__ src_of_padrow,
-                                                          const int4* __restrict__ tiles,
-                                                          const int32_t* __restrict__ num_tiles, int I, int i_pad,
-                                                          uint8_t* __restrict__ h_codes, float* __restrict__ h_gs) {
+                                                          const int32_t* __restrict__ pad_row_of_src, int n_rows,
+                                                          int I, int i_pad, uint8_t* __restrict__ h_codes,
+                                                          float* __restrict__ h_gs) {
   const int lane = threadIdx.x & 31;
-  const int row = blockIdx.y * 8 + (threadIdx.x >> 5);
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   pdl_trigger();
   pdl_wait();
-  if ((int)blockIdx.x >= *num_tiles) return;
-  const int4 ti = tiles[blockIdx.x];
-  if (row >= ti.z) return;
-  const int prow = ti.y + row;
-  if (src_of_padrow[prow] < 0) return;
+  if (row >= n_rows) return;
+  const int prow = pad_row_of_src[row];
   const float amax = row_amax[prow];
   const float gs = nvfp4_global_scale(amax);
   const float* hr = hbuf + (size_t)prow * i_pad;
@@ -323,11 +319,10 @@ cudaError_t launch_sf_to_atoms(const uint8_t* sf, int rows, int k16, uint8_t* at
   return cudaGetLastError();
 }
 
-cudaError_t launch_requant_rows(const float* hbuf, float* row_amax, const int32_t* src_of_padrow, const int4* tiles,
-                                const int32_t* num_tiles, int max_tiles, int I, int i_pad, uint8_t* h_codes,
-                                float* h_gs, cudaStream_t s) {
-  return launch_k(requant_rows_kernel, dim3(max_tiles, SMALL_BATCH_TOKENS / 8), dim3(256), 0, s, true, hbuf,
-                  row_amax, src_of_padrow, tiles, num_tiles, I, i_pad, h_codes, h_gs);
+cudaError_t launch_requant_rows(const float* hbuf, float* row_amax, const int32_t* pad_row_of_src, int n_rows,
+                                int I, int i_pad, uint8_t* h_codes, float* h_gs, cudaStream_t s) {
+  return launch_k(requant_rows_kernel, dim3((n_rows + 7) / 8), dim3(256), 0, s, true, hbuf, row_amax, pad_row_of_src,
+                  n_rows, I, i_pad, h_codes, h_gs);
 }
 
 cudaError_t launch_finalize_atomic(const float* out_acc, void* out, int T, int H, cudaStream_t s) {

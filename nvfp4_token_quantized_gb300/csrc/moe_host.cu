@@ -144,11 +144,13 @@ int device_of(const void* p) {
 // pipeline stage leaves room for a deeper weight-streaming ring.
 int tile_rows_for(int T) { return T <= SMALL_BATCH_TOKENS ? 64 : 128; }
 
-// Small batches: weight units each GEMM CTA streams into L2 before its
-// dependency wait (w13: two experts' column pairs, ~590 KB per CTA; w2: four
-// units of I x 128 weights).  Together they stay well inside L2.
-constexpr int W13_PREFETCH_UNITS = 4;
-constexpr int W2_PREFETCH_UNITS = 4;
+// Small batches: 128-column units whose weights each GEMM CTA streams into
+// L2 before its dependency wait - its first 256-column pair.  Measured on the
+// decode workload: one pair per CTA is as fast as two and faster than none;
+// prefetching from the front kernel instead slowed the front kernel more
+// than it saved.
+constexpr int W13_PREFETCH_UNITS = 2;
+constexpr int W2_PREFETCH_UNITS = 2;
 
 // Worst-case number of GEMM tiles of tile_rows rows when T tokens each pick
 // K of E experts (each tile is padded to its own 128-row block).
@@ -302,8 +304,8 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
       g.hbuf = h->hbuf;
       g.row_amax = h->row_amax;
       CK(h, launch_gemm_w13s(g, std::min(h->num_sms, tb * g.w13_pairs), false, s));
-      CK(h, launch_requant_rows(h->hbuf, h->row_amax, h->src_of_padrow, h->tiles, h->num_tiles, std::min(E, T * K),
-                                h->I, h->Ipad, h->h_codes, h->h_gs, s));
+      CK(h, launch_requant_rows(h->hbuf, h->row_amax, h->pad_row_of_src, T * K, h->I, h->Ipad, h->h_codes, h->h_gs,
+                                s));
     } else {
       CK(h, launch_gemm_w13(g, h->I / 128, std::min(h->w13_clusters[tile_rows == 128], tb), tile_rows, s));
     }
