@@ -481,6 +481,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
         const float gs_h = nvfp4_global_scale(amax_row);
         if (ready && row_ok) {
           const int k16_row = p.i_pad / SF_VEC;
+          uint32_t sf4 = 0;
 #pragma unroll
           for (int cc = 0; cc < 8; ++cc) {
             float v[16];
@@ -490,7 +491,12 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
             const uint32_t sf = nvfp4_quant_block16(v, gs_h, packed);
             const int k = (int)rank * 128 + 16 * cc;  // feature index of this block
             *reinterpret_cast<uint2*>(p.h_codes + operand_offset(prow, k / 2, p.i_pad / 2)) = packed;
-            p.h_sf[sf_atom_offset(prow, k / SF_VEC, k16_row)] = (uint8_t)sf;
+            // blocks 4m..4m+3 of the row have consecutive scale bytes
+            sf4 |= sf << (8 * (cc & 3));
+            if ((cc & 3) == 3) {
+              *reinterpret_cast<uint32_t*>(p.h_sf + sf_atom_offset(prow, (k - 48) / SF_VEC, k16_row)) = sf4;
+              sf4 = 0;
+            }
           }
           if (rank == 0) p.h_gs[prow] = gs_h;
         }

@@ -18,7 +18,7 @@ namespace {
 // K expanded rows (the rows of its K experts in the padded expert-grouped
 // layout the w13 GEMM reads).  In atomic-finalize mode the token's FP32
 // output accumulator row is cleared here as well.
-__global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int K,
+__global__ void __launch_bounds__(256, 4) act_quant_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int K,
                                                        const int32_t* __restrict__ pad_row_of_src,
                                                        uint8_t* __restrict__ a_codes, uint8_t* __restrict__ a_sf,
                                                        float* __restrict__ gs_rows, float* __restrict__ out_acc) {
@@ -50,16 +50,28 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __r
   for (int j = 0; j < 16; ++j) prow[j] = j < K ? pad_row_of_src[(size_t)t * K + j] : 0;
 
   const size_t row_bytes = (size_t)H / 2;
-  for (int b = lane; b < nblk; b += 32) {
-    float v[16];
-    bf16x16_to_f32(__ldg(xr + 2 * b), __ldg(xr + 2 * b + 1), v);
-    uint2 packed;
-    const uint32_t sf = nvfp4_quant_block16(v, gs, packed);
+  // nblk is a multiple of 16: the loop bound is warp-uniform, and blocks
+  // 4m..4m+3 of a row (one lane group) have consecutive scale bytes, written
+  // as one 32-bit word by the group's first lane.
+  for (int b0 = 0; b0 < nblk; b0 += 32) {
+    const int b = b0 + lane;
+    const bool active = b < nblk;
+    uint2 packed = make_uint2(0u, 0u);
+    uint32_t sf = 0;
+    if (active) {
+      float v[16];
+      bf16x16_to_f32(__ldg(xr + 2 * b), __ldg(xr + 2 * b + 1), v);
+      sf = nvfp4_quant_block16(v, gs, packed);
+    }
+    const uint32_t sf4 = sf | (__shfl_down_sync(0xffffffffu, sf, 1) << 8) | (__shfl_down_sync(0xffffffffu, sf, 2) << 16) |
+                         (__shfl_down_sync(0xffffffffu, sf, 3) << 24);
+    if (active) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      if (j < K) {
-        *reinterpret_cast<uint2*>(a_codes + operand_offset(prow[j], 8 * b, (int)row_bytes)) = packed;
-        a_sf[sf_atom_offset(prow[j], b, nblk)] = (uint8_t)sf;
+      for (int j = 0; j < 16; ++j) {
+        if (j < K) {
+          *reinterpret_cast<uint2*>(a_codes + operand_offset(prow[j], 8 * b, (int)row_bytes)) = packed;
+          if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(a_sf + sf_atom_offset(prow[j], b, nblk)) = sf4;
+        }
       }
     }
   }
@@ -89,21 +101,30 @@ __global__ void __launch_bounds__(256) requant_rows_kernel(const float* __restri
   const float gs = nvfp4_global_scale(amax);
   const float* hr = hbuf + (size_t)prow * i_pad;
   const int nblk = I / SF_VEC, k16_row = i_pad / SF_VEC;
-  for (int b = lane; b < nblk; b += 32) {
-    float v[16];
-    const float4* src = reinterpret_cast<const float4*>(hr + 16 * b);
+  for (int b0 = 0; b0 < nblk; b0 += 32) {  // nblk = I/16, a multiple of 8: uniform bound
+    const int b = b0 + lane;
+    uint2 packed = make_uint2(0u, 0u);
+    uint32_t sf = 0;
+    if (b < nblk) {
+      float v[16];
+      const float4* src = reinterpret_cast<const float4*>(hr + 16 * b);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float4 f = src[q];
-      v[4 * q] = f.x;
-      v[4 * q + 1] = f.y;
-      v[4 * q + 2] = f.z;
-      v[4 * q + 3] = f.w;
+      for (int q = 0; q < 4; ++q) {
+        const float4 f = src[q];
+        v[4 * q] = f.x;
+        v[4 * q + 1] = f.y;
+        v[4 * q + 2] = f.z;
+        v[4 * q + 3] = f.w;
+      }
+      sf = nvfp4_quant_block16(v, gs, packed);
     }
-    uint2 packed;
-    const uint32_t sf = nvfp4_quant_block16(v, gs, packed);
-    *reinterpret_cast<uint2*>(h_codes + operand_offset(prow, 8 * b, i_pad / 2)) = packed;
-    h_codes[sf_atom_offset(prow, b, k16_row)] = (uint8_t)sf;
+    // blocks 4m..4m+3 have consecutive scale bytes: one 32-bit store
+    const uint32_t sf4 = sf | (__shfl_down_sync(0xffffffffu, sf, 1) << 8) | (__shfl_down_sync(0xffffffffu, sf, 2) << 16) |
+                         (__shfl_down_sync(0xffffffffu, sf, 3) << 24);
+    if (b < nblk) {
+      *reinterpret_cast<uint2*>(h_codes + operand_offset(prow, 8 * b, i_pad / 2)) = packed;
+      if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(h_codes + sf_atom_offset(prow, b, k16_row)) = sf4;
+    }
   }
   if (lane == 0) {
     h_gs[prow] = gs;
@@ -231,12 +252,29 @@ __global__ void __launch_bounds__(256) finalize_atomic_kernel(const float* __res
                                                              __nv_bfloat16* __restrict__ out, size_t n8) {
   pdl_trigger();
   pdl_wait();
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
-    const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
-    const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
-    __nv_bfloat162 o[4] = {__floats2bfloat162_rn(a.x, a.y), __floats2bfloat162_rn(a.z, a.w),
-                           __floats2bfloat162_rn(b.x, b.y), __floats2bfloat162_rn(b.z, b.w)};
-    reinterpret_cast<uint4*>(out)[i] = *reinterpret_cast<const uint4*>(o);
+  // FIN_ILP independent 8-float chunks per thread per pass (coalesced: chunk
+  // q of a pass is blockDim.x apart), all loads issued before any store.
+  constexpr int FIN_ILP = 4;
+  const size_t step = (size_t)gridDim.x * blockDim.x * FIN_ILP;
+  for (size_t base = (size_t)blockIdx.x * blockDim.x * FIN_ILP + threadIdx.x; base < n8; base += step) {
+    float4 a[FIN_ILP], b[FIN_ILP];
+#pragma unroll
+    for (int q = 0; q < FIN_ILP; ++q) {
+      const size_t i = base + (size_t)q * blockDim.x;
+      if (i < n8) {
+        a[q] = reinterpret_cast<const float4*>(acc)[2 * i];
+        b[q] = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < FIN_ILP; ++q) {
+      const size_t i = base + (size_t)q * blockDim.x;
+      if (i < n8) {
+        __nv_bfloat162 o[4] = {__floats2bfloat162_rn(a[q].x, a[q].y), __floats2bfloat162_rn(a[q].z, a[q].w),
+                               __floats2bfloat162_rn(b[q].x, b[q].y), __floats2bfloat162_rn(b[q].z, b[q].w)};
+        reinterpret_cast<uint4*>(out)[i] = *reinterpret_cast<const uint4*>(o);
+      }
+    }
   }
 }
 
@@ -327,7 +365,7 @@ cudaError_t launch_requant_rows(const float* hbuf, float* row_amax, const int32_
 
 cudaError_t launch_finalize_atomic(const float* out_acc, void* out, int T, int H, cudaStream_t s) {
   const size_t n8 = (size_t)T * H / 8;
-  return launch_k(finalize_atomic_kernel, dim3(grid_for(n8, 256)), dim3(256), 0, s, true, out_acc,
+  return launch_k(finalize_atomic_kernel, dim3(grid_for(n8, 256 * 4)), dim3(256), 0, s, true, out_acc,
                   reinterpret_cast<__nv_bfloat16*>(out), n8);
 }
 

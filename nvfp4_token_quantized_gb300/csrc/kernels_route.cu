@@ -404,8 +404,26 @@ __global__ void __launch_bounds__(PERM_THREADS) permute_kernel(const int32_t* __
       slot[i] = -1;
       const int t = tb + i;
       if (t < T) {
-        for (int j = 0; j < K; ++j)
-          if (topk_ids[(size_t)t * K + j] == e) slot[i] = j;
+        // the token's K <= 16 ids into registers first (8-byte loads when K
+        // is even), then the comparisons: all loads are in flight together
+        int id[16];
+        const int32_t* row = topk_ids + (size_t)t * K;
+        if ((K & 1) == 0) {
+#pragma unroll
+          for (int j = 0; j < 16; j += 2)
+            if (j < K) {
+              const int2 v = __ldg(reinterpret_cast<const int2*>(row + j));
+              id[j] = v.x;
+              id[j + 1] = v.y;
+            }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (j < K) id[j] = __ldg(row + j);
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (j < K && id[j] == e) slot[i] = j;
       }
       n += slot[i] >= 0;
     }
@@ -482,13 +500,22 @@ __global__ void __launch_bounds__(256) front_small_kernel(const FrontArgs p) {
     }
     amax = warp_max(amax);
     const float gs = nvfp4_global_scale(amax);
-    for (int b = lane; b < nblk; b += 32) {
-      float v[16];
-      bf16x16_to_f32(__ldg(xr + 2 * b), __ldg(xr + 2 * b + 1), v);
-      uint2 packed;
-      const uint32_t sf = nvfp4_quant_block16(v, gs, packed);
-      *reinterpret_cast<uint2*>(p.a_codes + operand_offset(t, 8 * b, H / 2)) = packed;
-      p.a_codes[sf_atom_offset(t, b, nblk)] = (uint8_t)sf;
+    for (int b0 = 0; b0 < nblk; b0 += 32) {  // nblk % 16 == 0: uniform bound
+      const int b = b0 + lane;
+      uint2 packed = make_uint2(0u, 0u);
+      uint32_t sf = 0;
+      if (b < nblk) {
+        float v[16];
+        bf16x16_to_f32(__ldg(xr + 2 * b), __ldg(xr + 2 * b + 1), v);
+        sf = nvfp4_quant_block16(v, gs, packed);
+      }
+      // blocks 4m..4m+3 have consecutive scale bytes: one 32-bit store
+      const uint32_t sf4 = sf | (__shfl_down_sync(0xffffffffu, sf, 1) << 8) |
+                           (__shfl_down_sync(0xffffffffu, sf, 2) << 16) | (__shfl_down_sync(0xffffffffu, sf, 3) << 24);
+      if (b < nblk) {
+        *reinterpret_cast<uint2*>(p.a_codes + operand_offset(t, 8 * b, H / 2)) = packed;
+        if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(p.a_codes + sf_atom_offset(t, b, nblk)) = sf4;
+      }
     }
     if (lane == 0) p.gs_rows[t] = gs;
     if (p.out_acc) {
