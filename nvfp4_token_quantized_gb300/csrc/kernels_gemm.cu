@@ -124,10 +124,21 @@ __host__ __device__ constexpr int smem_bytes_res(int stages, int nch, int a_rows
          2 * nch * TILE_M * 4 + 1024;
 }
 
+// SwiGLU silu(g) * u with sigmoid(g) = 1/2 + tanh(g/2)/2: one special-function
+// operation per element (the hardware tanh, relative error about 2^-11, far
+// below the FP4 requantization that follows).  With an exponential and a
+// reciprocal per element, the w13 epilogue was bound by the special-function
+// units at full 128-row tiles.
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ float swiglu(float g_acc, float u_acc, float alpha) {
   const float g = __fmul_rn(g_acc, alpha);
   const float u = __fmul_rn(u_acc, alpha);
-  return __fdividef(__fmul_rn(g, u), __fadd_rn(1.0f, __expf(-g)));
+  const float sig = fmaf(0.5f, tanh_approx(0.5f * g), 0.5f);
+  return __fmul_rn(__fmul_rn(g, u), sig);
 }
 
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
