@@ -188,8 +188,12 @@ def silu(g: np.ndarray) -> np.ndarray:
     return g / (1.0 + np.exp(-g))
 
 
-def expert_rows(a_codes, a_sf, a_gs, w13: QuantWeights, w2: QuantWeights, e: int):
+def expert_rows(a_codes, a_sf, a_gs, w13: QuantWeights, w2: QuantWeights, e: int, h_gs_static=None):
     """Run one expert on already-quantized input rows.
+
+    ``h_gs_static``: None for the per-row (dynamic) requantization of the
+    SwiGLU output; otherwise the expert's calibrated FP32 global scale, used
+    for all its rows (the static per-tensor contract).
 
     Returns a dict with the FP32 w13 output ``y1`` [n, 2I], the FP32 SwiGLU
     output ``h`` [n, I], its quantization (``h_codes``, ``h_sf``, ``h_gs``)
@@ -203,7 +207,10 @@ def expert_rows(a_codes, a_sf, a_gs, w13: QuantWeights, w2: QuantWeights, e: int
     I = y1.shape[1] // 2
     gate, up = y1[:, :I], y1[:, I:]
     h = (silu(gate) * up.astype(np.float64)).astype(np.float32)
-    h_codes, h_sf, h_gs = nvfp4.quantize_rows(h)
+    if h_gs_static is None:
+        h_codes, h_sf, h_gs = nvfp4.quantize_rows(h)
+    else:
+        h_codes, h_sf, h_gs = nvfp4.quantize_rows_static(h, h_gs_static)
     A2 = nvfp4.decode_scaled(h_codes, h_sf)                      # [n, I]
     B2 = nvfp4.decode_scaled(w2.codes[e], w2.sf[e])              # [H, I]
     acc2 = A2 @ B2.T
@@ -248,12 +255,20 @@ class ForwardResult:
 
 def moe_forward(x: np.ndarray, wg: np.ndarray, w13: QuantWeights, w2: QuantWeights,
                 top_k: int, bias: Optional[np.ndarray] = None,
-                tokens: Optional[Sequence[int]] = None) -> ForwardResult:
+                tokens: Optional[Sequence[int]] = None, static_scales=None) -> ForwardResult:
     """Forward of the routed MoE layer for all tokens, or for ``tokens`` only.
 
     Tokens are independent in this layer, so a subset gives the same rows as
     the full batch (the permutation is needed only by the GPU's layout).
     ``x`` float32 [T, H] and ``wg`` float32 [H, E] hold bf16 values.
+
+    ``static_scales``: None for the per-token contract (activation global
+    scales from each token's and each expanded row's maximum), or a pair
+    (x_gs, h_gs) for the per-tensor static contract the pages keep separate
+    ("CuTe DSL backend gets per-token NVFP4 online quantization and reload",
+    Summary and Implementation item 2): one calibrated FP32 global scale for
+    the first GEMM's input, and one per expert (``h_gs`` [E]) for the second
+    GEMM's input.
     """
     x = np.asarray(x, dtype=np.float32)
     tok = np.arange(x.shape[0]) if tokens is None else np.asarray(tokens, dtype=np.int64)
@@ -261,14 +276,18 @@ def moe_forward(x: np.ndarray, wg: np.ndarray, w13: QuantWeights, w2: QuantWeigh
     n, H = xs.shape
     logits = router_logits(xs, wg, bias)
     ids, weights = topk_route(logits, top_k)
-    x_codes, x_sf, x_gs = nvfp4.quantize_rows(xs)
+    if static_scales is None:
+        x_codes, x_sf, x_gs = nvfp4.quantize_rows(xs)
+    else:
+        x_codes, x_sf, x_gs = nvfp4.quantize_rows_static(xs, static_scales[0])
     y_rows = np.zeros((n, top_k, H), dtype=np.float32)
     h_gs, y2_map = {}, {}
     for e in range(w13.num_experts):
         sel_t, sel_j = np.nonzero(ids == e)          # token-ascending
         if sel_t.size == 0:
             continue
-        r = expert_rows(x_codes[sel_t], x_sf[sel_t], x_gs[sel_t], w13, w2, e)
+        h_static = None if static_scales is None else np.float32(np.asarray(static_scales[1])[e])
+        r = expert_rows(x_codes[sel_t], x_sf[sel_t], x_gs[sel_t], w13, w2, e, h_static)
         y_rows[sel_t, sel_j] = r["y2"]
         for i, (t, j) in enumerate(zip(sel_t, sel_j)):
             h_gs[(int(tok[t]), int(j))] = r["h_gs"][i]

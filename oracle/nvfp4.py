@@ -190,6 +190,20 @@ def quantize_rows(x: np.ndarray):
     return codes, sf, gs
 
 
+def quantize_rows_static(x: np.ndarray, gs):
+    """Per-tensor static quantization: every row uses the given global scale
+    ``gs`` (a calibrated FP32 scalar) instead of one derived from the row's
+    maximum.  Blocks whose scaled maximum exceeds the formats saturate (block
+    scale 448, codes +-6).
+
+    Returns (codes uint8 [rows, K], sf uint8 [rows, K/16], gs float32 [rows]).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    g = np.full(x.shape[0], np.float32(gs), dtype=np.float32)
+    codes, sf = quantize_blocks(x, g)
+    return codes, sf, g
+
+
 def quantize_tensor(w: np.ndarray):
     """One global scale for the whole matrix (an expert's weight).
 
