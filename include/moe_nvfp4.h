@@ -85,6 +85,16 @@ typedef enum {
  * accumulated with FP32 atomic adds (the fused finalize). */
 #define MOE_FLAG_DETERMINISTIC 1u
 
+/* Static per-tensor activation scales: the contract "CuTe DSL backend gets
+ * per-token NVFP4 online quantization and reload" (Summary; Implementation
+ * item 2) keeps apart from per-token quantization.  With this flag the
+ * forward quantizes every token of x with one calibrated FP32 global scale,
+ * and each expert's SwiGLU output with that expert's calibrated global
+ * scale, both set with moe_set_static_scales, instead of scales derived from
+ * each token's and each expanded row's maximum.  Blocks whose maximum times
+ * the scale exceeds 2688 saturate (block scale 448, codes +-6). */
+#define MOE_FLAG_STATIC_ACT_SCALES 2u
+
 typedef struct {
   int hidden;          /* H: model width (K dim of w13, N dim of w2) */
   int inter;           /* I: expert intermediate width */
@@ -133,6 +143,17 @@ MOE_API moe_status moe_load_weights(moe_handle* h, const void* w13, const moe_we
  * graph would then need to be recaptured).  Never reallocates. */
 MOE_API moe_status moe_refresh_scales_inplace(moe_handle* h, const void* w13, const moe_weight_desc* w13_desc,
                                       const void* w2, const moe_weight_desc* w2_desc, void* stream);
+
+/* Calibrated global scales of the static contract, copied on `stream` into
+ * handle-owned buffers (the same buffers every time, so a captured graph
+ * replays with new values):
+ *   x_gs: device pointer to 1 float, the w13 input's scale (all tokens);
+ *   h_gs: device pointer to E floats, expert e's w2 input scale.
+ * Scales follow gs = 2688 / calibrated maximum and must be positive and
+ * finite.  MOE_ERR_INVALID_ARG unless the handle was created with
+ * MOE_FLAG_STATIC_ACT_SCALES; a forward of such a handle before the first
+ * call returns MOE_ERR_NOT_LOADED. */
+MOE_API moe_status moe_set_static_scales(moe_handle* h, const float* x_gs, const float* h_gs, void* stream);
 
 /* One forward of the routed MoE layer.
  *   x:      [num_tokens, H] bf16 activations (read only).

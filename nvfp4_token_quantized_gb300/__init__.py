@@ -10,6 +10,7 @@ from .builder import build, LIB_PATH  # noqa: F401
 from .binding import (  # noqa: F401
     EXPORTED,
     MOE_FLAG_DETERMINISTIC,
+    MOE_FLAG_STATIC_ACT_SCALES,
     MoE,
     MoEError,
     load_library,
@@ -26,4 +27,5 @@ from .binding import (  # noqa: F401
     moe_load_weights,
     moe_refresh_scales_inplace,
     moe_route_noalloc,
+    moe_set_static_scales,
 )

@@ -26,6 +26,7 @@ MOE_ERR_CUDA = 6
 MOE_ERR_DEVICE_TIMEOUT = 7
 MOE_ERR_UNSUPPORTED = 8
 MOE_FLAG_DETERMINISTIC = 1
+MOE_FLAG_STATIC_ACT_SCALES = 2
 MOE_DTYPE_BF16 = 1
 
 EXPORTED = (
@@ -34,7 +35,7 @@ EXPORTED = (
     "moe_status_string", "moe_get_status", "moe_debug_routing", "moe_debug_logits",
     "moe_debug_act_quant", "moe_debug_weight_quant", "moe_debug_intermediate", "moe_debug_buffer_ptrs",
     "moe_debug_convert", "moe_debug_block_scaled_gemm", "moe_set_stage_timing", "moe_get_stage_times",
-    "moe_stage_name", "moe_route_noalloc",
+    "moe_stage_name", "moe_route_noalloc", "moe_set_static_scales",
 )
 MOE_ROUTE_NOALLOC_MAX_LOGITS = 1 << 20
 MOE_NUM_STAGES = 7
@@ -98,6 +99,7 @@ def load_library() -> ctypes.CDLL:
         "moe_get_stage_times": (I, [P, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(I)]),
         "moe_stage_name": (ctypes.c_char_p, [I]),
         "moe_route_noalloc": (I, [P, P, P, I, I, I, I, P, P, P]),
+        "moe_set_static_scales": (I, [P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -178,6 +180,13 @@ def moe_refresh_scales_inplace(h, w13: torch.Tensor, w2: torch.Tensor, stream=No
                                                         ctypes.byref(d2), _stream(stream)))
 
 
+def moe_set_static_scales(h, x_gs: torch.Tensor, h_gs: torch.Tensor, stream=None) -> None:
+    """Calibrated global scales of the static per-tensor contract: x_gs float32
+    [1] (the w13 input, all tokens), h_gs float32 [E] (each expert's w2 input),
+    CUDA tensors on the handle's device."""
+    _raise(h, load_library().moe_set_static_scales(h, _ptr(x_gs), _ptr(h_gs), _stream(stream)))
+
+
 def moe_forward(h, x: torch.Tensor, gate_w: torch.Tensor, out: torch.Tensor, num_tokens: int, stream=None) -> None:
     _raise(h, load_library().moe_forward(h, _ptr(x), _ptr(gate_w), _ptr(out), int(num_tokens), _stream(stream)))
 
@@ -251,18 +260,23 @@ class MoE:
     """Owner of one library handle: a routed-MoE layer with fixed sizes."""
 
     def __init__(self, hidden: int, inter: int, num_experts: int, top_k: int, max_num_tokens: int,
-                 device: int = 0, deterministic: bool = False):
+                 device: int = 0, deterministic: bool = False, static_scales: bool = False):
         self.H, self.I, self.E, self.K, self.Tmax = hidden, inter, num_experts, top_k, max_num_tokens
         self.device = device
         self.deterministic = deterministic
-        self._h = moe_create(hidden, inter, num_experts, top_k, max_num_tokens, device,
-                             MOE_FLAG_DETERMINISTIC if deterministic else 0)
+        self.static_scales = static_scales
+        flags = (MOE_FLAG_DETERMINISTIC if deterministic else 0) | (MOE_FLAG_STATIC_ACT_SCALES if static_scales else 0)
+        self._h = moe_create(hidden, inter, num_experts, top_k, max_num_tokens, device, flags)
         self.last_T = None
 
     @classmethod
-    def from_shape(cls, shape, device: int = 0, deterministic: Optional[bool] = None, max_num_tokens=None):
+    def from_shape(cls, shape, device: int = 0, deterministic: Optional[bool] = None, max_num_tokens=None,
+                   static_scales: bool = False):
         return cls(shape.H, shape.I, shape.E, shape.K, max_num_tokens or shape.max_num_tokens, device,
-                   shape.deterministic if deterministic is None else deterministic)
+                   shape.deterministic if deterministic is None else deterministic, static_scales)
+
+    def set_static_scales(self, x_gs: torch.Tensor, h_gs: torch.Tensor, stream=None):
+        moe_set_static_scales(self._h, x_gs, h_gs, stream)
 
     @property
     def handle(self):

@@ -35,8 +35,11 @@ cudaError_t launch_permute(const int32_t* topk_ids, const int32_t* counts, int T
                            const PermuteOut& o, cudaStream_t s);
 
 // ---- quantization (kernels_quant.cu) ----
+// static_gs: nullptr for per-token global scales, else the calibrated
+// per-tensor scale (device scalar) every token uses.
 cudaError_t launch_act_quant(const void* x, int T, int H, int K, const int32_t* pad_row_of_src,
-                             uint8_t* a_codes, uint8_t* a_sf, float* gs_rows, float* out_acc, cudaStream_t s);
+                             uint8_t* a_codes, uint8_t* a_sf, float* gs_rows, float* out_acc,
+                             const float* static_gs, cudaStream_t s);
 cudaError_t launch_weight_amax(const void* w, int E, int N, int Kd, uint32_t* amax_bits, cudaStream_t s);
 // Weights go to the pair-tile layout (wpair_offset).  interleave: 0 = rows
 // in caller order; 1 = w13 gate/up rows interleaved in chunks of 64 so that
@@ -84,6 +87,7 @@ struct FrontArgs {
   int4* tiles;                // one tile per expert with rows
   int32_t* num_tiles;
   uint32_t* sync;             // FRONT_SYNC_WORDS counters, zero between launches
+  const float* static_gs;     // calibrated per-tensor scale (static contract), or nullptr
 };
 constexpr int FRONT_SYNC_WORDS = 64;
 cudaError_t front_setup(int H, int E);
@@ -134,6 +138,9 @@ struct GemmArgs {
   int w13_pairs;
   float* hbuf;
   float* row_amax;
+  // static per-tensor contract: the w2 input's calibrated global scale per
+  // expert (the w13 epilogue requantizes with it directly), or nullptr
+  const float* h_gs_static;
 };
 
 cudaError_t gemm_setup_attributes(int w13_chunks);

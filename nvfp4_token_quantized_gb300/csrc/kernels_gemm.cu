@@ -448,48 +448,56 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
         }
         release_acc(0);  // the tensor cores may refill the accumulator now
         if (!row_ok) amax = 0.0f;
-        if constexpr (MODE == MODE_W13S) {
-          // FP32 SwiGLU row to the scratch, its maximum folded into the
-          // row's global word (non-negative floats order like their bits);
-          // the requantization kernel finishes the row.
-          if (ready && row_ok) {
-            const int f0 = ((u >> 1) % nch) * 128;
-            atomicMax(reinterpret_cast<unsigned int*>(p.row_amax) + prow, __float_as_uint(amax));
-            float4* dst = reinterpret_cast<float4*>(p.hbuf + (size_t)prow * p.i_pad + f0);
+        // this CTA's 128 features of the row start at feature f0
+        const int f0 = (MODE == MODE_W13 ? (int)rank : (u >> 1) % nch) * 128;
+        float gs_h;
+        if (p.h_gs_static) {
+          // static per-tensor contract: the expert's calibrated scale, no
+          // row maximum needed (the same branch in every CTA of a cluster)
+          gs_h = p.h_gs_static[un.e];
+        } else {
+          if constexpr (MODE == MODE_W13S) {
+            // FP32 SwiGLU row to the scratch, its maximum folded into the
+            // row's global word (non-negative floats order like their bits);
+            // the requantization kernel finishes the row.
+            if (ready && row_ok) {
+              atomicMax(reinterpret_cast<unsigned int*>(p.row_amax) + prow, __float_as_uint(amax));
+              float4* dst = reinterpret_cast<float4*>(p.hbuf + (size_t)prow * p.i_pad + f0);
 #pragma unroll
-            for (int q = 0; q < 32; ++q) dst[q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+              for (int q = 0; q < 32; ++q) dst[q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+            }
+            continue;
           }
-          continue;
-        }
-        // Exchange the row maxima across the cluster.  Slot buffer i & 1;
-        // a peer can be at most one m-tile ahead (it needs this CTA's value
-        // of its next m-tile first), so two buffers never overwrite a value
-        // that has not been read, and the successive uses of a buffer
-        // alternate the tag bit.
-        const int b = i & 1;
-        const uint32_t tag = ((uint32_t)(i >> 1) & 1u) << 31;
-        const uint32_t* slots = part + (size_t)b * nch * TILE_M + m;
-        for (int r = 0; r < nch; ++r)
-          st_shared_cluster_u32(slots + (size_t)rank * TILE_M, (uint32_t)r, tag | __float_as_uint(amax));
-        float amax_row = 0.0f;
-        for (int r = 0; r < nch; ++r) {
-          const uint32_t* slot = slots + (size_t)r * TILE_M;
-          uint32_t v = ld_shared_relaxed_u32(slot);
-          if ((v & 0x80000000u) != tag) {
-            const uint64_t t0 = global_timer_ns();
-            for (uint32_t it = 1; (v & 0x80000000u) != tag; ++it) {
-              v = ld_shared_relaxed_u32(slot);
-              if ((it & 255u) == 0 && global_timer_ns() - t0 > 2000000000ull) {
-                c.abort_flag = 1;
-                report_device_error(p.status, DEV_ERR_TIMEOUT);
-                ready = false;
-                break;
+          // Exchange the row maxima across the cluster.  Slot buffer i & 1;
+          // a peer can be at most one m-tile ahead (it needs this CTA's value
+          // of its next m-tile first), so two buffers never overwrite a value
+          // that has not been read, and the successive uses of a buffer
+          // alternate the tag bit.
+          const int b = i & 1;
+          const uint32_t tag = ((uint32_t)(i >> 1) & 1u) << 31;
+          const uint32_t* slots = part + (size_t)b * nch * TILE_M + m;
+          for (int r = 0; r < nch; ++r)
+            st_shared_cluster_u32(slots + (size_t)rank * TILE_M, (uint32_t)r, tag | __float_as_uint(amax));
+          float amax_row = 0.0f;
+          for (int r = 0; r < nch; ++r) {
+            const uint32_t* slot = slots + (size_t)r * TILE_M;
+            uint32_t v = ld_shared_relaxed_u32(slot);
+            if ((v & 0x80000000u) != tag) {
+              const uint64_t t0 = global_timer_ns();
+              for (uint32_t it = 1; (v & 0x80000000u) != tag; ++it) {
+                v = ld_shared_relaxed_u32(slot);
+                if ((it & 255u) == 0 && global_timer_ns() - t0 > 2000000000ull) {
+                  c.abort_flag = 1;
+                  report_device_error(p.status, DEV_ERR_TIMEOUT);
+                  ready = false;
+                  break;
+                }
               }
             }
+            amax_row = fmaxf(amax_row, __uint_as_float(v & 0x7FFFFFFFu));
           }
-          amax_row = fmaxf(amax_row, __uint_as_float(v & 0x7FFFFFFFu));
+          gs_h = nvfp4_global_scale(amax_row);
         }
-        const float gs_h = nvfp4_global_scale(amax_row);
         if (ready && row_ok) {
           const int k16_row = p.i_pad / SF_VEC;
           uint32_t sf4 = 0;
@@ -500,7 +508,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
             for (int q = 0; q < 16; ++q) v[q] = h[16 * cc + q];
             uint2 packed;
             const uint32_t sf = nvfp4_quant_block16(v, gs_h, packed);
-            const int k = (int)rank * 128 + 16 * cc;  // feature index of this block
+            const int k = f0 + 16 * cc;  // feature index of this block
             *reinterpret_cast<uint2*>(p.h_codes + operand_offset(prow, k / 2, p.i_pad / 2)) = packed;
             // blocks 4m..4m+3 of the row have consecutive scale bytes
             sf4 |= sf << (8 * (cc & 3));
@@ -509,7 +517,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
               sf4 = 0;
             }
           }
-          if (rank == 0) p.h_gs[prow] = gs_h;
+          if (f0 == 0) p.h_gs[prow] = gs_h;
         }
       }
     } else {

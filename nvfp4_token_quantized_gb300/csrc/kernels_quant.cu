@@ -21,7 +21,8 @@ namespace {
 __global__ void __launch_bounds__(256, 4) act_quant_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int K,
                                                        const int32_t* __restrict__ pad_row_of_src,
                                                        uint8_t* __restrict__ a_codes, uint8_t* __restrict__ a_sf,
-                                                       float* __restrict__ gs_rows, float* __restrict__ out_acc) {
+                                                       float* __restrict__ gs_rows, float* __restrict__ out_acc,
+                                                       const float* __restrict__ static_gs) {
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   pdl_trigger();
@@ -34,15 +35,22 @@ __global__ void __launch_bounds__(256, 4) act_quant_kernel(const __nv_bfloat16* 
 
   // x is the caller's input: reading it and forming the row maximum may
   // overlap the permutation kernel; its outputs are read after pdl_wait().
-  float amax = 0.0f;
-  for (int b = lane; b < nblk; b += 32) {
-    float v[16];
-    bf16x16_to_f32(__ldg(xr + 2 * b), __ldg(xr + 2 * b + 1), v);
+  // per-token global scale from the row maximum, or the calibrated
+  // per-tensor scale of the static contract
+  float gs;
+  if (static_gs) {
+    gs = __ldg(static_gs);
+  } else {
+    float amax = 0.0f;
+    for (int b = lane; b < nblk; b += 32) {
+      float v[16];
+      bf16x16_to_f32(__ldg(xr + 2 * b), __ldg(xr + 2 * b + 1), v);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    }
+    amax = warp_max(amax);
+    gs = nvfp4_global_scale(amax);
   }
-  amax = warp_max(amax);
-  const float gs = nvfp4_global_scale(amax);
 
   pdl_wait();
   int prow[16];
@@ -312,9 +320,10 @@ int grid_for(size_t n, int per_block, int cap = 152 * 16) {
 }  // namespace
 
 cudaError_t launch_act_quant(const void* x, int T, int H, int K, const int32_t* pad_row_of_src, uint8_t* a_codes,
-                             uint8_t* a_sf, float* gs_rows, float* out_acc, cudaStream_t s) {
+                             uint8_t* a_sf, float* gs_rows, float* out_acc, const float* static_gs, cudaStream_t s) {
   return launch_k(act_quant_kernel, dim3((T + 7) / 8), dim3(256), 0, s, true,
-                  reinterpret_cast<const __nv_bfloat16*>(x), T, H, K, pad_row_of_src, a_codes, a_sf, gs_rows, out_acc);
+                  reinterpret_cast<const __nv_bfloat16*>(x), T, H, K, pad_row_of_src, a_codes, a_sf, gs_rows, out_acc,
+                  static_gs);
 }
 
 cudaError_t launch_weight_amax(const void* w, int E, int N, int Kd, uint32_t* amax_bits, cudaStream_t s) {

@@ -491,15 +491,20 @@ __global__ void __launch_bounds__(256) front_small_kernel(const FrontArgs p) {
     const int t = tb0 + i;
     if (t >= T) break;
     const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
-    float amax = 0.0f;
-    for (int b = lane; b < nblk; b += 32) {
-      float v[16];
-      bf16x16_to_f32(__ldg(xr + 2 * b), __ldg(xr + 2 * b + 1), v);
+    float gs;
+    if (p.static_gs) {  // static per-tensor contract: the calibrated scale
+      gs = __ldg(p.static_gs);
+    } else {
+      float amax = 0.0f;
+      for (int b = lane; b < nblk; b += 32) {
+        float v[16];
+        bf16x16_to_f32(__ldg(xr + 2 * b), __ldg(xr + 2 * b + 1), v);
 #pragma unroll
-      for (int q = 0; q < 16; ++q) amax = fmaxf(amax, fabsf(v[q]));
+        for (int q = 0; q < 16; ++q) amax = fmaxf(amax, fabsf(v[q]));
+      }
+      amax = warp_max(amax);
+      gs = nvfp4_global_scale(amax);
     }
-    amax = warp_max(amax);
-    const float gs = nvfp4_global_scale(amax);
     for (int b0 = 0; b0 < nblk; b0 += 32) {  // nblk % 16 == 0: uniform bound
       const int b = b0 + lane;
       uint2 packed = make_uint2(0u, 0u);

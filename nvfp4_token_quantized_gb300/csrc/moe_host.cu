@@ -30,6 +30,8 @@ struct moe_handle {
   int num_sms = 0;      // persistent w2 grid
   int w13_clusters[2] = {0, 0};  // persistent w13 grid (clusters of I/128 CTAs), 64- / 128-row tiles
   bool deterministic = false;
+  bool static_scales = false;   // MOE_FLAG_STATIC_ACT_SCALES
+  bool static_set = false;      // moe_set_static_scales has been called
   bool loaded = false;
   moe_weight_desc w13_desc{}, w2_desc{};
   int last_T = -1;
@@ -51,6 +53,8 @@ struct moe_handle {
   int4* tiles = nullptr;
   int32_t* num_tiles = nullptr;
   uint32_t* front_sync = nullptr;  // completion counters of the small-batch front kernel
+  float* static_x_gs = nullptr;    // static contract: the w13 input's calibrated scale [1]
+  float* static_h_gs = nullptr;    // static contract: the w2 input's calibrated scale per expert [E]
   float* hbuf = nullptr;           // small batches: FP32 SwiGLU rows [E*128][Ipad]
   float* row_amax = nullptr;       // small batches: their row maxima [E*128], zero between forwards
 
@@ -260,6 +264,7 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
       fa.tiles = h->tiles;
       fa.num_tiles = h->num_tiles;
       fa.sync = h->front_sync;
+      fa.static_gs = h->static_scales ? h->static_x_gs : nullptr;
       CK(h, launch_front_small(fa, s));
       for (int i = 1; i <= 4; ++i) CK(h, mark(h, i, s));
     } else {
@@ -272,7 +277,8 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
       CK(h, launch_permute(h->topk_ids, h->counts, T, K, E, tile_rows, po, s));
       CK(h, mark(h, 3, s));
       CK(h, launch_act_quant(x, T, H, K, h->pad_row_of_src, h->a_codes, h->a_sf, h->gs_rows,
-                             h->deterministic ? nullptr : h->out_acc, s));
+                             h->deterministic ? nullptr : h->out_acc, h->static_scales ? h->static_x_gs : nullptr,
+                             s));
       CK(h, mark(h, 4, s));
     }
     // bound on the tile count: one per expert with rows (small batches)
@@ -295,6 +301,7 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
     g.src_of_padrow = h->src_of_padrow;
     g.num_experts = E;
     g.prefetch_units = small ? W13_PREFETCH_UNITS : 0;
+    g.h_gs_static = h->static_scales ? h->static_h_gs : nullptr;
     if (small) {
       // every tile reads the one shared activation tile; no clusters: the
       // units spread over all SMs, and the requantization follows as its own
@@ -304,7 +311,9 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
       g.hbuf = h->hbuf;
       g.row_amax = h->row_amax;
       CK(h, launch_gemm_w13s(g, std::min(h->num_sms, tb * g.w13_pairs), false, s));
-      CK(h, launch_requant_rows(h->hbuf, h->row_amax, h->pad_row_of_src, T * K, h->I, h->Ipad, h->h_codes, h->h_gs,
+      // (with static scales the w13 epilogue has already requantized)
+      if (!h->static_scales)
+        CK(h, launch_requant_rows(h->hbuf, h->row_amax, h->pad_row_of_src, T * K, h->I, h->Ipad, h->h_codes, h->h_gs,
                                 s));
     } else {
       CK(h, launch_gemm_w13(g, h->I / 128, std::min(h->w13_clusters[tile_rows == 128], tb), tile_rows, s));
@@ -393,6 +402,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
   h->tile_cap = std::max(tile_bound(T, K, E, 128), E);
   h->Rpad = h->tile_cap * 128;
   h->deterministic = (cfg->flags & MOE_FLAG_DETERMINISTIC) != 0;
+  h->static_scales = (cfg->flags & MOE_FLAG_STATIC_ACT_SCALES) != 0;
 
   auto fail = [&](moe_status s) {
     moe_destroy(h);
@@ -411,6 +421,10 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
   h->w2_sf = h->w2_codes;
   A(h->gs_w13, sizeof(float) * E);
   A(h->gs_w2, sizeof(float) * E);
+  if (h->static_scales) {
+    A(h->static_x_gs, sizeof(float));
+    A(h->static_h_gs, sizeof(float) * E);
+  }
   A(h->amax_bits, sizeof(uint32_t) * 2 * E);
   A(h->logits, sizeof(float) * (size_t)T * E);
   A(h->topk_ids, sizeof(int32_t) * (size_t)T * K);
@@ -462,6 +476,24 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
     }
   }
   *out = h;
+  return MOE_OK;
+}
+
+moe_status moe_set_static_scales(moe_handle* h, const float* x_gs, const float* h_gs, void* stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  if (!h->static_scales) {
+    set_err(h, "moe_set_static_scales: the handle was not created with MOE_FLAG_STATIC_ACT_SCALES");
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (!x_gs || !h_gs) {
+    set_err(h, "moe_set_static_scales: NULL scale pointer");
+    return MOE_ERR_INVALID_ARG;
+  }
+  DeviceGuard dg(h->cfg.device);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  CK(h, cudaMemcpyAsync(h->static_x_gs, x_gs, sizeof(float), cudaMemcpyDeviceToDevice, s));
+  CK(h, cudaMemcpyAsync(h->static_h_gs, h_gs, sizeof(float) * h->E, cudaMemcpyDeviceToDevice, s));
+  h->static_set = true;
   return MOE_OK;
 }
 
@@ -520,6 +552,10 @@ moe_status moe_forward_ex(moe_handle* h, const void* x, const void* gate_w, cons
   }
   if (!h->loaded) {
     set_err(h, "moe_forward before moe_load_weights");
+    return MOE_ERR_NOT_LOADED;
+  }
+  if (h->static_scales && !h->static_set) {
+    set_err(h, "static activation scales: moe_set_static_scales has not been called");
     return MOE_ERR_NOT_LOADED;
   }
   if (num_tokens < 0) {

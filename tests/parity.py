@@ -106,9 +106,10 @@ def oracle_route(wl, tokens=None):
     return logits, ids, w
 
 
-def oracle_forward(wl, tokens=None):
+def oracle_forward(wl, tokens=None, static_scales=None):
     """Oracle forward for all tokens or a subset; only the experts those tokens
-    route to are quantized."""
+    route to are quantized.  static_scales: (x_gs, h_gs[E]) for the static
+    per-tensor contract, or None for per-token scales."""
     x = omoe.as_f32(wl.x)
     wg = omoe.as_f32(wl.gate_w)
     bias = None if wl.bias is None else wl.bias.numpy()
@@ -116,7 +117,7 @@ def oracle_forward(wl, tokens=None):
     experts = np.unique(ids)
     q13 = quantize_experts(wl.w13, experts)
     q2 = quantize_experts(wl.w2, experts)
-    return omoe.moe_forward(x, wg, q13, q2, wl.shape.K, bias, tokens=tokens)
+    return omoe.moe_forward(x, wg, q13, q2, wl.shape.K, bias, tokens=tokens, static_scales=static_scales)
 
 
 def sample_tokens(T: int, n: int, extra=()):

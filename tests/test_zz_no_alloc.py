@@ -9,6 +9,8 @@ its two halves.  This file is collected last so that it also runs after every
 other test in one process.
 """
 
+import gc
+
 import numpy as np
 import pytest
 import torch
@@ -68,16 +70,24 @@ def test_noalloc_routing_matches_the_forward(name):
         ids.fill_(-1)
         w.fill_(float("nan"))
         torch.cuda.synchronize()
-        allocated = torch.cuda.memory_allocated()
-        free_before = torch.cuda.mem_get_info()[0]
-        moe_route_noalloc(d["x"], d["gate_w"], K, bias=bias, topk_ids=ids, topk_w=w)
-        torch.cuda.synchronize()
+        # no collection of other tests' garbage inside the measured window
+        gc.collect()
+        gc.disable()
+        try:
+            allocated = torch.cuda.memory_allocated()
+            free_before = torch.cuda.mem_get_info()[0]
+            moe_route_noalloc(d["x"], d["gate_w"], K, bias=bias, topk_ids=ids, topk_w=w)
+            torch.cuda.synchronize()
+            allocated_after = torch.cuda.memory_allocated()
+            free_after = torch.cuda.mem_get_info()[0]
+        finally:
+            gc.enable()
+        assert allocated_after == allocated
+        if call == 1:  # the first call on the device has loaded the library's code
+            assert free_after == free_before, "device memory changed during the call"
         assert torch.equal(ids, ids_ref), f"call {call}: top-k ids differ from the forward's routing"
         np.testing.assert_allclose(w.cpu().numpy(), w_ref.cpu().numpy(), rtol=3e-6, atol=1e-7,
                                    err_msg=f"call {call}: routing weights differ")
-        assert torch.cuda.memory_allocated() == allocated
-        if call == 1:  # the first call on the device has loaded the library's code
-            assert torch.cuda.mem_get_info()[0] == free_before, "device memory changed during the call"
 
 
 @gpu
