@@ -33,7 +33,20 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE-layer tokens/s and % of roofline (FP4 tensor-core or HBM) at T=64/256/4096"
 NVFP4_BYTES_PER_ELT = 0.5625      # 4-bit code + one E4M3 scale per 16 elements
 STAGES = ("router", "topk", "permute", "quantize", "gemm_w13", "gemm_w2", "finalize")
-KERNELS_PER_FORWARD = 7
+SMALL_BATCH_TOKENS = 64           # the library's fused small-batch front end and atomic finalize
+
+
+def kernels_per_forward(T):
+    """Kernel launches of one forward: router, top-k, permute, quantize, w13,
+    w2, finalize; up to 64 tokens one fused front end, w13, the row
+    requantization, w2, finalize."""
+    return 5 if T <= SMALL_BATCH_TOKENS else 7
+
+
+def ordered_finalize(s, T):
+    """Whether the forward stores bf16 (token, slot) rows and sums them in slot
+    order (deterministic mode, and every forward above 64 tokens)."""
+    return s.deterministic or T > SMALL_BATCH_TOKENS
 
 
 def parse():
@@ -268,8 +281,9 @@ def stage_alg_bytes(s, T, touched):
         "permute": 4 * T * K + 16 * T * K,
         "quantize": 2 * T * H + q * R * H + 4 * R,
         "gemm_w13": touched * 2 * I * H * q + q * R * H + 4 * R + q * R * I + 4 * R,
-        "gemm_w2": touched * H * I * q + q * R * I + 4 * R + 4 * T * H,
-        "finalize": 4 * T * H + 2 * T * H,
+        # ordered: the bf16 (token, slot) rows; atomic: the FP32 accumulator
+        "gemm_w2": touched * H * I * q + q * R * I + 4 * R + (2 * R * H if ordered_finalize(s, T) else 4 * T * H),
+        "finalize": (2 * R * H + 4 * R if ordered_finalize(s, T) else 4 * T * H) + 2 * T * H,
     }
 
 
@@ -285,7 +299,8 @@ def layer_alg_bytes(s, T, touched):
 def workload_config(s, T, world):
     return {"workload": f"{s.name}: T={T} H={s.H} E={s.E} top-{s.K} I={s.I}, CUDA-graph replay",
             "T": T, "H": s.H, "E": s.E, "top_k": s.K, "I": s.I,
-            "finalize": "ordered (deterministic)" if s.deterministic else "fp32 atomic",
+            "finalize": ("ordered: bf16 (token, slot) rows summed in slot order" if ordered_finalize(s, T)
+                         else "fp32 atomic in the w2 epilogue"),
             "l2": "flushed before every step outside the timed events: a 256 MB write, then a 256 MB read of "
                   "another buffer so the flush's own dirty lines are written back before timing (the weights, "
                   "338 MB at decode, also exceed L2)",
@@ -460,7 +475,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": T * world / (e2e_total / args.steps), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "path": "moe_forward_host (pinned host buffers, eager launches)"},
-        "gpu_launches": KERNELS_PER_FORWARD * args.steps,
+        "gpu_launches": kernels_per_forward(T) * args.steps,
         "clocks": clk,
     }
     layer.close()

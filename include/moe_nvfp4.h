@@ -81,8 +81,13 @@ typedef enum {
 
 /* Deterministic mode: the top-k weighted reduction runs in a fixed order
  * (slot 0, 1, ..., K-1 per token) with no floating-point atomics, so the
- * output is bitwise identical across runs.  Without it, expert rows are
- * accumulated with FP32 atomic adds (the fused finalize). */
+ * output is bitwise identical across runs.  The w2 GEMM stores each
+ * (token, slot) expert output row rounded to bf16, and a finalize kernel sums
+ * a token's K rows in slot order in FP32.  Without the flag, forwards of at
+ * most 64 tokens accumulate the expert rows with FP32 atomic adds in the w2
+ * epilogue (the fused finalize); larger forwards take the ordered path in
+ * either mode, since there the atomic traffic (top_k x the output) bounds
+ * the w2 GEMM. */
 #define MOE_FLAG_DETERMINISTIC 1u
 
 /* Static per-tensor activation scales: the contract "CuTe DSL backend gets

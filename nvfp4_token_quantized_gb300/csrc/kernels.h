@@ -58,7 +58,8 @@ cudaError_t launch_codes_to_tiled(const uint8_t* codes, int rows, int row_bytes,
 
 // ---- finalize (kernels_quant.cu) ----
 cudaError_t launch_finalize_atomic(const float* out_acc, void* out, int T, int H, cudaStream_t s);
-cudaError_t launch_finalize_ordered(const float* ybuf, const float* topk_w, void* out, int T, int H, int K,
+// ybuf: bf16 rows [t * K + j][H] of the weighted-sum operands.
+cudaError_t launch_finalize_ordered(const uint16_t* ybuf, const float* topk_w, void* out, int T, int H, int K,
                                     cudaStream_t s);
 
 // ---- block-scaled FP4 GEMMs (kernels_gemm.cu) ----
@@ -119,7 +120,7 @@ struct GemmArgs {
   const float* topk_w;
   int top_k;
   float* out_acc;             // atomic mode
-  float* ybuf;                // ordered mode
+  uint16_t* ybuf;             // ordered mode: bf16 rows [token * top_k + slot][hidden]
   int hidden;
   // plain epilogue (tests)
   float* d;

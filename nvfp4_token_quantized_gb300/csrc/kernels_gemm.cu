@@ -39,8 +39,10 @@
 //        scale: the per-row NVFP4 input of the w2 GEMM, written without a
 //        round trip of the FP32 intermediate through HBM.
 //   w2   y = acc / (gs_h * gs_w2) scaled by the token's top-k weight and
-//        added into the FP32 output accumulator (atomic mode), or stored per
-//        (token, slot) for the fixed-order finalize (ordered mode).
+//        added into the FP32 output accumulator (atomic mode), or rounded to
+//        bf16 and stored per (token, slot) for the fixed-order finalize
+//        (ordered mode: half the bytes of an FP32 row, and plain stores where
+//        the atomic mode's reductions at large batches saturate L2).
 //   plain FP32 store (tests).
 //
 // The fusion of routing, expandInputRows, activation and finalize around the
@@ -572,11 +574,16 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
                              __fmul_rn(wj, __fmul_rn(a[q + 1], alpha)), __fmul_rn(wj, __fmul_rn(a[q + 2], alpha)),
                              __fmul_rn(wj, __fmul_rn(a[q + 3], alpha)));
               } else if constexpr (MODE == MODE_W2_ORDERED) {
-                float4* dst = reinterpret_cast<float4*>(p.ybuf + (size_t)src * p.hidden + col);
+                // the (token, slot) row of the expert output, rounded to bf16
+                uint4* dst = reinterpret_cast<uint4*>(p.ybuf + (size_t)src * p.hidden + col);
 #pragma unroll
-                for (int q = 0; q < 16; ++q)
-                  dst[q] = make_float4(__fmul_rn(a[4 * q], alpha), __fmul_rn(a[4 * q + 1], alpha),
-                                       __fmul_rn(a[4 * q + 2], alpha), __fmul_rn(a[4 * q + 3], alpha));
+                for (int q = 0; q < 8; ++q) {
+                  uint32_t w[4];
+#pragma unroll
+                  for (int i = 0; i < 4; ++i)
+                    w[i] = pack_bf16x2(__fmul_rn(a[8 * q + 2 * i], alpha), __fmul_rn(a[8 * q + 2 * i + 1], alpha));
+                  dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+                }
               } else {
                 float4* dst = reinterpret_cast<float4*>(p.d + (size_t)prow * p.ldd + col);
 #pragma unroll

@@ -287,26 +287,40 @@ __global__ void __launch_bounds__(256) finalize_atomic_kernel(const float* __res
 }
 
 // out[t][n] = bf16_rn(sum over j ascending of fl32(w[t][j] * y[t*K+j][n])),
-// FP32 partial sums, the first term taken as is.  4 columns per thread.
-__global__ void __launch_bounds__(256) finalize_ordered_kernel(const float* __restrict__ ybuf,
+// y the bf16 rows the w2 epilogue stored; FP32 partial sums, the first term
+// taken as is.  8 columns per thread: the K rows' 16-byte words are all
+// loaded before the sum starts.
+constexpr int FIN_MAX_K = 16;
+__global__ void __launch_bounds__(256) finalize_ordered_kernel(const uint16_t* __restrict__ ybuf,
                                                               const float* __restrict__ topk_w,
                                                               __nv_bfloat16* __restrict__ out, int T, int H, int K) {
   pdl_trigger();
   pdl_wait();
-  const size_t n4 = (size_t)T * H / 4;
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
-    const size_t flat = 4 * i;
-    const int t = (int)(flat / H), n = (int)(flat % H);
-    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < K; ++j) {
-      const float w = topk_w[(size_t)t * K + j];
-      const float4 y = *reinterpret_cast<const float4*>(ybuf + ((size_t)t * K + j) * H + n);
-      const float4 p = make_float4(__fmul_rn(w, y.x), __fmul_rn(w, y.y), __fmul_rn(w, y.z), __fmul_rn(w, y.w));
-      if (j == 0) s = p;
-      else s = make_float4(__fadd_rn(s.x, p.x), __fadd_rn(s.y, p.y), __fadd_rn(s.z, p.z), __fadd_rn(s.w, p.w));
+  const int h8 = H / 8;
+  const size_t n8 = (size_t)T * h8;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / h8), c = (int)(i % h8);
+    const uint4* yr = reinterpret_cast<const uint4*>(ybuf) + (size_t)t * K * h8 + c;
+    uint4 y[FIN_MAX_K];
+#pragma unroll
+    for (int j = 0; j < FIN_MAX_K; ++j)
+      if (j < K) y[j] = __ldcs(yr + (size_t)j * h8);  // read once: streaming
+    float s[8];
+#pragma unroll
+    for (int j = 0; j < FIN_MAX_K; ++j) {
+      if (j < K) {
+        const float w = __ldg(topk_w + (size_t)t * K + j);
+        const uint32_t yw[4] = {y[j].x, y[j].y, y[j].z, y[j].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float p0 = __fmul_rn(w, bf16_lo(yw[q])), p1 = __fmul_rn(w, bf16_hi(yw[q]));
+          s[2 * q] = j == 0 ? p0 : __fadd_rn(s[2 * q], p0);
+          s[2 * q + 1] = j == 0 ? p1 : __fadd_rn(s[2 * q + 1], p1);
+        }
+      }
     }
-    __nv_bfloat162 o[2] = {__floats2bfloat162_rn(s.x, s.y), __floats2bfloat162_rn(s.z, s.w)};
-    *reinterpret_cast<uint2*>(out + flat) = *reinterpret_cast<const uint2*>(o);
+    reinterpret_cast<uint4*>(out)[i] =
+        make_uint4(pack_bf16x2(s[0], s[1]), pack_bf16x2(s[2], s[3]), pack_bf16x2(s[4], s[5]), pack_bf16x2(s[6], s[7]));
   }
 }
 
@@ -378,10 +392,11 @@ cudaError_t launch_finalize_atomic(const float* out_acc, void* out, int T, int H
                   reinterpret_cast<__nv_bfloat16*>(out), n8);
 }
 
-cudaError_t launch_finalize_ordered(const float* ybuf, const float* topk_w, void* out, int T, int H, int K,
+cudaError_t launch_finalize_ordered(const uint16_t* ybuf, const float* topk_w, void* out, int T, int H, int K,
                                     cudaStream_t s) {
-  const size_t n4 = (size_t)T * H / 4;
-  return launch_k(finalize_ordered_kernel, dim3(grid_for(n4, 256)), dim3(256), 0, s, true, ybuf, topk_w,
+  if (K > FIN_MAX_K || H % 8) return cudaErrorInvalidValue;
+  const size_t n8 = (size_t)T * H / 8;
+  return launch_k(finalize_ordered_kernel, dim3(grid_for(n8, 256)), dim3(256), 0, s, true, ybuf, topk_w,
                   reinterpret_cast<__nv_bfloat16*>(out), T, H, K);
 }
 

@@ -61,7 +61,11 @@ struct moe_handle {
   // operands of the two GEMMs
   uint8_t *a_codes = nullptr, *a_sf = nullptr, *h_codes = nullptr, *h_sf = nullptr;
   float *gs_rows = nullptr, *h_gs = nullptr;
-  float *out_acc = nullptr, *ybuf = nullptr;
+  // atomic finalize (small batches): FP32 accumulator [min(Tmax, 64), H];
+  // ordered finalize (deterministic mode, and every batch above 64 tokens):
+  // bf16 rows [Tmax * K, H], one per (token, slot)
+  float* out_acc = nullptr;
+  uint16_t* ybuf = nullptr;
 
   // staging for moe_forward_host
   void *stage_x = nullptr, *stage_gate = nullptr, *stage_out = nullptr;
@@ -238,6 +242,10 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
   if (T > 0) {
     const int tile_rows = tile_rows_for(T);
     const bool small = T <= SMALL_BATCH_TOKENS;
+    // Above the small-batch size the FP32 atomic reduction of R x H partial
+    // rows saturates L2; the ordered finalize (bf16 rows, fixed slot order)
+    // moves half the bytes with plain stores and is deterministic as well.
+    const bool ordered = h->deterministic || !small;
     CK(h, mark(h, 0, s));
     if (small) {
       // one kernel for router, quantization, top-k and grouping; its time is
@@ -255,7 +263,7 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
       fa.topk_w = h->topk_w;
       fa.a_codes = h->a_codes;
       fa.gs_rows = h->gs_rows;
-      fa.out_acc = h->deterministic ? nullptr : h->out_acc;
+      fa.out_acc = ordered ? nullptr : h->out_acc;
       fa.src_of_padrow = h->src_of_padrow;
       fa.expert_offsets = h->expert_offsets;
       fa.src_of_row = h->src_of_row;
@@ -277,7 +285,7 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
       CK(h, launch_permute(h->topk_ids, h->counts, T, K, E, tile_rows, po, s));
       CK(h, mark(h, 3, s));
       CK(h, launch_act_quant(x, T, H, K, h->pad_row_of_src, h->a_codes, h->a_sf, h->gs_rows,
-                             h->deterministic ? nullptr : h->out_acc, h->static_scales ? h->static_x_gs : nullptr,
+                             ordered ? nullptr : h->out_acc, h->static_scales ? h->static_x_gs : nullptr,
                              s));
       CK(h, mark(h, 4, s));
     }
@@ -340,9 +348,9 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
     g2.num_experts = E;
     g2.prefetch_units = small ? W2_PREFETCH_UNITS : 0;
     // units are pairs of 128-column tiles
-    CK(h, launch_gemm_w2(g2, std::min(h->num_sms, tb * g2.n_tiles / 2), h->deterministic, tile_rows, s));
+    CK(h, launch_gemm_w2(g2, std::min(h->num_sms, tb * g2.n_tiles / 2), ordered, tile_rows, s));
     CK(h, mark(h, 6, s));
-    if (h->deterministic) CK(h, launch_finalize_ordered(h->ybuf, h->topk_w, out, T, H, K, s));
+    if (ordered) CK(h, launch_finalize_ordered(h->ybuf, h->topk_w, out, T, H, K, s));
     else CK(h, launch_finalize_atomic(h->out_acc, out, T, H, s));
     CK(h, mark(h, 7, s));
   }
@@ -447,8 +455,8 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
   A(h->h_codes, operand_bytes(Rp, h->Ipad / 2));
   h->h_sf = h->h_codes;
   A(h->h_gs, sizeof(float) * Rp);
-  if (h->deterministic) A(h->ybuf, sizeof(float) * (size_t)h->Rmax * H);
-  else A(h->out_acc, sizeof(float) * (size_t)T * H);
+  if (h->deterministic || T > SMALL_BATCH_TOKENS) A(h->ybuf, sizeof(uint16_t) * (size_t)h->Rmax * H);
+  if (!h->deterministic) A(h->out_acc, sizeof(float) * (size_t)std::min(T, SMALL_BATCH_TOKENS) * H);
   A(h->stage_x, sizeof(uint16_t) * (size_t)T * H);
   A(h->stage_gate, sizeof(uint16_t) * (size_t)H * E);
   A(h->stage_bias, sizeof(float) * E);
