@@ -17,11 +17,14 @@
 //               K=64 MMAs per 256-element stage: N = 256 into the one
 //               256-column accumulator (pairs), or N = 128 into one of two
 //               128-column buffers (plain);
-//   warps 2-5   epilogue, one accumulator row (tensor-memory lane) per thread.
+//   warps 2-9   epilogue, two warps per tensor-memory lane quadrant: warp w
+//               reads lanes [32 (w % 4), +32) and takes column half
+//               (w - 2) / 4 of every accumulator, one row per thread.
 // With two accumulator buffers (plain) the epilogue drains unit u while the
 // tensor cores compute unit u+1; with one 256-column accumulator (pairs) the
-// tensor cores wait only for the epilogue's tensor-memory reads, while the
-// ring keeps streaming weights.
+// tensor cores wait only for the epilogue's tensor-memory reads (each thread
+// moves its 128 columns to registers and releases the accumulator before any
+// arithmetic), while the ring keeps streaming weights.
 //
 // Epilogues:
 //   w13  a unit's 128 columns are 64 gate features and the matching 64 up
@@ -76,8 +79,9 @@ constexpr uint32_t IDESC = idesc_fp4(TILE_M, TILE_N);
 constexpr int TMEM_SF_STAGE_PAIR = 48;       // 16 columns SFA + 32 columns SFB per stage
 constexpr uint32_t IDESC_PAIR = idesc_fp4(TILE_M, 2 * TILE_N);
 constexpr int MAX_STAGES_PAIR = 5;
-constexpr int THREADS = 192;
-constexpr int EPI_WARPS = 4;
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int HALF_MAX_BYTES = 2 * 2 * TILE_M * 4;  // w13: per-half row maxima, two m-tile buffers
 constexpr int CTRL_BYTES = 256;
 constexpr int MAX_SMEM = 232448;
 static_assert(TMEM_SF_BASE + MAX_STAGES * TMEM_SF_STAGE <= TMEM_COLS, "tensor memory overflow");
@@ -115,7 +119,8 @@ __host__ __device__ constexpr int stage_bytes(int a_rows, bool pair = false) {
   return a_slot_bytes(a_rows) + b_slot_bytes(pair);
 }
 __host__ __device__ constexpr int smem_bytes_for(int stages, int nch, int a_rows, bool pair = false) {
-  return stages * stage_bytes(a_rows, pair) + a_tail_bytes(a_rows) + CTRL_BYTES + 2 * nch * TILE_M * 4 + 1024;
+  return stages * stage_bytes(a_rows, pair) + a_tail_bytes(a_rows) + CTRL_BYTES + 2 * nch * TILE_M * 4 +
+         HALF_MAX_BYTES + 1024;
 }
 // Resident activations (the small-batch w13 GEMM, whose tiles all read the
 // same shared activation tile): all K stages of A stay in shared memory for
@@ -123,7 +128,7 @@ __host__ __device__ constexpr int smem_bytes_for(int stages, int nch, int a_rows
 constexpr int ARES_MAX_KS = 8;  // K <= 2048
 __host__ __device__ constexpr int smem_bytes_res(int stages, int nch, int a_rows, bool pair = false) {
   return ARES_MAX_KS * a_slot_bytes(a_rows) + a_tail_bytes(a_rows) + stages * b_slot_bytes(pair) + CTRL_BYTES +
-         2 * nch * TILE_M * 4 + 1024;
+         2 * nch * TILE_M * 4 + HALF_MAX_BYTES + 1024;
 }
 
 // SwiGLU silu(g) * u with sigmoid(g) = 1/2 + tanh(g/2)/2: one special-function
@@ -169,13 +174,16 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
   // [2][nch][128] words: partial row maximum bits (non-negative, so bit 31
   // is free) with bit 31 holding the m-tile tag
   uint32_t* part = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(&c) + CTRL_BYTES);
+  // [2][2][128] w13 row maxima of the two column halves of a CTA (m-tile
+  // buffer i & 1, then half)
+  float* half_max = reinterpret_cast<float*>(part + (MODE == MODE_W13 ? 2 * gridDim.x * TILE_M : 0));
   {
     // The layout above must fit the launch's dynamic shared memory; if the
     // host sized it differently, report and leave before touching any of it
     // (the condition is the same in every CTA of the grid).
     uint32_t dyn;
     asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
-    const uint8_t* end = reinterpret_cast<const uint8_t*>(part) + (MODE == MODE_W13 ? 2 * gridDim.x * TILE_M * 4 : 0);
+    const uint8_t* end = reinterpret_cast<const uint8_t*>(half_max) + HALF_MAX_BYTES;
     if (end > smem_raw + dyn) {
       if (threadIdx.x == 0) report_device_error(p.status, DEV_ERR_BAD_STATE);
       return;
@@ -387,8 +395,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
     }
     __syncwarp();
   } else {
-    // ---------------- epilogue (warps 2..5) ----------------
+    // ---------------- epilogue (warps 2..9) ----------------
     const int quarter = warp & 3;          // tensor-memory lanes [32q, 32q+32)
+    const int half = (warp - 2) >> 2;      // column half of every accumulator
     const int m = quarter * 32 + lane;     // accumulator row of this thread
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     int n = 0;  // units drained by this CTA
@@ -419,9 +428,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
         // expert take no part (their amax counts as 0 in the exchange)
         const bool row_ok = m < un.valid && p.src_of_padrow[prow] >= 0;
         const float alpha = row_ok ? __fdiv_rn(1.0f, __fmul_rn(p.gs_rows[un.arow + m], p.gs_w[un.e])) : 0.0f;
-        float h[128];
+        // this thread's tile of the pair's 128 x 256 accumulator: columns
+        // [128 half, +64) are gate features, the next 64 the matching up
+        // features; h takes the gate values, then the SwiGLU values
+        float h[64], uv[64];
         float amax = 0.0f;
-        // the pair's 128 x 256 accumulator: columns [0, 128) then [128, 256)
         bool ready = mbar_wait_bounded(&c.acc_full[0], i & 1, nullptr);
         if (!ready) {
           c.abort_flag = 1;
@@ -429,29 +440,25 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
         }
         tc_fence_after();
         ready = ready && !c.abort_flag;
+        if (ready && warp_rows) {
+          const uint32_t t = lane_base + half * TILE_N;
+          tmem_ld32(t, h);
+          tmem_ld32(t + 32, h + 32);
+          tmem_ld32(t + 64, uv);
+          tmem_ld32(t + 96, uv + 32);
+          tmem_ld_wait();
+        }
+        release_acc(0);  // everything is in registers: the tensor cores may refill the accumulator
+        if (ready && warp_rows) {
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          if (ready && warp_rows) {
-            const uint32_t t = lane_base + j * TILE_N;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              float gv[32], uv[32];
-              tmem_ld32(t + 32 * half, gv);        // gate features 32*half ..
-              tmem_ld32(t + 64 + 32 * half, uv);   // matching up features
-              tmem_ld_wait();
-#pragma unroll
-              for (int q = 0; q < 32; ++q) {
-                const float hv = swiglu(gv[q], uv[q], alpha);
-                h[64 * j + 32 * half + q] = hv;
-                amax = fmaxf(amax, fabsf(hv));
-              }
-            }
+          for (int q = 0; q < 64; ++q) {
+            h[q] = swiglu(h[q], uv[q], alpha);
+            amax = fmaxf(amax, fabsf(h[q]));
           }
         }
-        release_acc(0);  // the tensor cores may refill the accumulator now
         if (!row_ok) amax = 0.0f;
-        // this CTA's 128 features of the row start at feature f0
-        const int f0 = (MODE == MODE_W13 ? (int)rank : (u >> 1) % nch) * 128;
+        // this thread's 64 features of the row start at feature f0
+        const int f0 = (MODE == MODE_W13 ? (int)rank : (u >> 1) % nch) * 128 + 64 * half;
         float gs_h;
         if (p.h_gs_static) {
           // static per-tensor contract: the expert's calibrated scale, no
@@ -466,20 +473,28 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
               atomicMax(reinterpret_cast<unsigned int*>(p.row_amax) + prow, __float_as_uint(amax));
               float4* dst = reinterpret_cast<float4*>(p.hbuf + (size_t)prow * p.i_pad + f0);
 #pragma unroll
-              for (int q = 0; q < 32; ++q) dst[q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+              for (int q = 0; q < 16; ++q) dst[q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
             }
             continue;
           }
+          // The CTA's two halves first combine their maxima in shared memory
+          // (buffer i & 1: a half can be at most one m-tile ahead, since it
+          // passes the barrier of the next m-tile only with the other half).
+          float* hm = half_max + (size_t)(i & 1) * 2 * TILE_M;
+          hm[half * TILE_M + m] = amax;
+          named_bar_sync(1, EPI_WARPS * 32);
+          const float amax_cta = fmaxf(hm[m], hm[TILE_M + m]);
           // Exchange the row maxima across the cluster.  Slot buffer i & 1;
           // a peer can be at most one m-tile ahead (it needs this CTA's value
           // of its next m-tile first), so two buffers never overwrite a value
           // that has not been read, and the successive uses of a buffer
-          // alternate the tag bit.
+          // alternate the tag bit.  Half 0 stores; both halves read.
           const int b = i & 1;
           const uint32_t tag = ((uint32_t)(i >> 1) & 1u) << 31;
           const uint32_t* slots = part + (size_t)b * nch * TILE_M + m;
-          for (int r = 0; r < nch; ++r)
-            st_shared_cluster_u32(slots + (size_t)rank * TILE_M, (uint32_t)r, tag | __float_as_uint(amax));
+          if (half == 0)
+            for (int r = 0; r < nch; ++r)
+              st_shared_cluster_u32(slots + (size_t)rank * TILE_M, (uint32_t)r, tag | __float_as_uint(amax_cta));
           float amax_row = 0.0f;
           for (int r = 0; r < nch; ++r) {
             const uint32_t* slot = slots + (size_t)r * TILE_M;
@@ -502,9 +517,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
         }
         if (ready && row_ok) {
           const int k16_row = p.i_pad / SF_VEC;
-          uint32_t sf4 = 0;
+          uint32_t sf4 = 0;  // the 4 blocks' scale bytes are consecutive in the row's atom
 #pragma unroll
-          for (int cc = 0; cc < 8; ++cc) {
+          for (int cc = 0; cc < 4; ++cc) {
             float v[16];
 #pragma unroll
             for (int q = 0; q < 16; ++q) v[q] = h[16 * cc + q];
@@ -512,17 +527,16 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
             const uint32_t sf = nvfp4_quant_block16(v, gs_h, packed);
             const int k = f0 + 16 * cc;  // feature index of this block
             *reinterpret_cast<uint2*>(p.h_codes + operand_offset(prow, k / 2, p.i_pad / 2)) = packed;
-            // blocks 4m..4m+3 of the row have consecutive scale bytes
-            sf4 |= sf << (8 * (cc & 3));
-            if ((cc & 3) == 3) {
-              *reinterpret_cast<uint32_t*>(p.h_sf + sf_atom_offset(prow, (k - 48) / SF_VEC, k16_row)) = sf4;
-              sf4 = 0;
-            }
+            sf4 |= sf << (8 * cc);
           }
+          *reinterpret_cast<uint32_t*>(p.h_sf + sf_atom_offset(prow, f0 / SF_VEC, k16_row)) = sf4;
           if (f0 == 0) p.h_gs[prow] = gs_h;
         }
       }
     } else {
+      // pairs: the thread's 128-column tile `half` of the 128 x 256
+      // accumulator; plain: its 64-column half of the 128-column buffer
+      constexpr int COLS = PAIR ? 128 : 64;
       for (int u = first; u < nunits; u = PAIR ? next(next(u)) : next(u), ++n) {
         const Unit un = unit_at(u);
         const bool warp_rows = quarter * 32 < un.valid;
@@ -547,52 +561,43 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
         } else {
           ready = wait_acc(buf, n);
         }
+        float a[COLS];
         if (ready && warp_rows) {
-          float alpha = 0.0f, wj = 0.0f;
-          if (MODE != MODE_PLAIN && row_ok) {
-            alpha = __fdiv_rn(1.0f, __fmul_rn(p.gs_rows[prow], p.gs_w[un.e]));
-            wj = p.topk_w[src];
-          }
-          const int tok = src / (p.top_k > 0 ? p.top_k : 1);
+          const uint32_t t = lane_base + (PAIR ? half * TILE_N : buf * TILE_N + 64 * half);
 #pragma unroll
-          for (int part = 0; part < (PAIR ? 4 : 2); ++part) {  // 64-column parts
-            const int j = part >> 1, half = part & 1;
-            const int n0 = (un.col + j) * TILE_N;
-            const uint32_t t = lane_base + (PAIR ? j : buf) * TILE_N;
-            float a[64];
-            tmem_ld32(t + 64 * half, a);
-            tmem_ld32(t + 64 * half + 32, a + 32);
-            tmem_ld_wait();
-            if (part == (PAIR ? 3 : 1)) release_acc(buf);  // everything is in registers now
-            if (row_ok) {
-              const int col = n0 + 64 * half;
-              if constexpr (MODE == MODE_W2_ATOMIC) {
-                float* dst = p.out_acc + (size_t)tok * p.hidden + col;
+          for (int q = 0; q < COLS; q += 32) tmem_ld32(t + q, a + q);
+          tmem_ld_wait();
+        }
+        release_acc(buf);  // everything is in registers now
+        if (ready && warp_rows && row_ok) {
+          const int col = PAIR ? (un.col + half) * TILE_N : un.col * TILE_N + 64 * half;
+          if constexpr (MODE == MODE_W2_ATOMIC || MODE == MODE_W2_ORDERED) {
+            const float alpha = __fdiv_rn(1.0f, __fmul_rn(p.gs_rows[prow], p.gs_w[un.e]));
+            if constexpr (MODE == MODE_W2_ATOMIC) {
+              const float wj = p.topk_w[src];
+              const int tok = src / (p.top_k > 0 ? p.top_k : 1);
+              float* dst = p.out_acc + (size_t)tok * p.hidden + col;
 #pragma unroll
-                for (int q = 0; q < 64; q += 4)
-                  red_add_v4(dst + q, __fmul_rn(wj, __fmul_rn(a[q], alpha)),
-                             __fmul_rn(wj, __fmul_rn(a[q + 1], alpha)), __fmul_rn(wj, __fmul_rn(a[q + 2], alpha)),
-                             __fmul_rn(wj, __fmul_rn(a[q + 3], alpha)));
-              } else if constexpr (MODE == MODE_W2_ORDERED) {
-                // the (token, slot) row of the expert output, rounded to bf16
-                uint4* dst = reinterpret_cast<uint4*>(p.ybuf + (size_t)src * p.hidden + col);
+              for (int q = 0; q < COLS; q += 4)
+                red_add_v4(dst + q, __fmul_rn(wj, __fmul_rn(a[q], alpha)), __fmul_rn(wj, __fmul_rn(a[q + 1], alpha)),
+                           __fmul_rn(wj, __fmul_rn(a[q + 2], alpha)), __fmul_rn(wj, __fmul_rn(a[q + 3], alpha)));
+            } else {
+              // the (token, slot) row of the expert output, rounded to bf16
+              uint4* dst = reinterpret_cast<uint4*>(p.ybuf + (size_t)src * p.hidden + col);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                  uint32_t w[4];
+              for (int q = 0; q < COLS / 8; ++q) {
+                uint32_t w[4];
 #pragma unroll
-                  for (int i = 0; i < 4; ++i)
-                    w[i] = pack_bf16x2(__fmul_rn(a[8 * q + 2 * i], alpha), __fmul_rn(a[8 * q + 2 * i + 1], alpha));
-                  dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-              } else {
-                float4* dst = reinterpret_cast<float4*>(p.d + (size_t)prow * p.ldd + col);
-#pragma unroll
-                for (int q = 0; q < 16; ++q) dst[q] = make_float4(a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
+                for (int i = 0; i < 4; ++i)
+                  w[i] = pack_bf16x2(__fmul_rn(a[8 * q + 2 * i], alpha), __fmul_rn(a[8 * q + 2 * i + 1], alpha));
+                dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
               }
             }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(p.d + (size_t)prow * p.ldd + col);
+#pragma unroll
+            for (int q = 0; q < COLS / 4; ++q) dst[q] = make_float4(a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
           }
-        } else {
-          release_acc(buf);
         }
       }
     }
