@@ -38,7 +38,7 @@ cudaError_t launch_permute(const int32_t* topk_ids, const int32_t* counts, int T
 // static_gs: nullptr for per-token global scales, else the calibrated
 // per-tensor scale (device scalar) every token uses.
 cudaError_t launch_act_quant(const void* x, int T, int H, int K, const int32_t* pad_row_of_src,
-                             uint8_t* a_codes, uint8_t* a_sf, float* gs_rows, float* out_acc,
+                             uint8_t* a_codes, uint8_t* a_sf, float* gs_rows,
                              const float* static_gs, cudaStream_t s);
 cudaError_t launch_weight_amax(const void* w, int E, int N, int Kd, uint32_t* amax_bits, cudaStream_t s);
 // Weights go to the pair-tile layout (wpair_offset).  interleave: 0 = rows

@@ -16,12 +16,12 @@ namespace {
 // One warp per token.  Lane L owns the 16-element blocks L, L+32, ...
 // The token's codes, block scales and global scale are written to each of its
 // K expanded rows (the rows of its K experts in the padded expert-grouped
-// layout the w13 GEMM reads).  In atomic-finalize mode the token's FP32
-// output accumulator row is cleared here as well.
+// layout the w13 GEMM reads).  (Batches that reach this kernel take the
+// ordered finalize, so no FP32 accumulator needs clearing.)
 __global__ void __launch_bounds__(256, 4) act_quant_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int K,
                                                        const int32_t* __restrict__ pad_row_of_src,
                                                        uint8_t* __restrict__ a_codes, uint8_t* __restrict__ a_sf,
-                                                       float* __restrict__ gs_rows, float* __restrict__ out_acc,
+                                                       float* __restrict__ gs_rows,
                                                        const float* __restrict__ static_gs) {
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -84,10 +84,6 @@ __global__ void __launch_bounds__(256, 4) act_quant_kernel(const __nv_bfloat16* 
     }
   }
   if (lane < K) gs_rows[pad_row_of_src[(size_t)t * K + lane]] = gs;
-  if (out_acc) {
-    float4* o = reinterpret_cast<float4*>(out_acc + (size_t)t * H);
-    for (int i = lane; i < H / 4; i += 32) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
 }
 
 // Requantization of the small-batch w13 output: one warp per expanded row
@@ -334,9 +330,9 @@ int grid_for(size_t n, int per_block, int cap = 152 * 16) {
 }  // namespace
 
 cudaError_t launch_act_quant(const void* x, int T, int H, int K, const int32_t* pad_row_of_src, uint8_t* a_codes,
-                             uint8_t* a_sf, float* gs_rows, float* out_acc, const float* static_gs, cudaStream_t s) {
+                             uint8_t* a_sf, float* gs_rows, const float* static_gs, cudaStream_t s) {
   return launch_k(act_quant_kernel, dim3((T + 7) / 8), dim3(256), 0, s, true,
-                  reinterpret_cast<const __nv_bfloat16*>(x), T, H, K, pad_row_of_src, a_codes, a_sf, gs_rows, out_acc,
+                  reinterpret_cast<const __nv_bfloat16*>(x), T, H, K, pad_row_of_src, a_codes, a_sf, gs_rows,
                   static_gs);
 }
 

@@ -285,7 +285,7 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
       CK(h, launch_permute(h->topk_ids, h->counts, T, K, E, tile_rows, po, s));
       CK(h, mark(h, 3, s));
       CK(h, launch_act_quant(x, T, H, K, h->pad_row_of_src, h->a_codes, h->a_sf, h->gs_rows,
-                             ordered ? nullptr : h->out_acc, h->static_scales ? h->static_x_gs : nullptr,
+                             h->static_scales ? h->static_x_gs : nullptr,
                              s));
       CK(h, mark(h, 4, s));
     }
