@@ -6,6 +6,8 @@
 // quantization and reload", Implementation item 2; the stated reading):
 // gs = 2688 / amax per token (or per expert for weights); per 16-element
 // block sf = E4M3(amax_b * gs / 6); code = E2M1(x * (gs / sf)).
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -284,8 +286,8 @@ __global__ void __launch_bounds__(256) finalize_atomic_kernel(const float* __res
 
 // out[t][n] = bf16_rn(sum over j ascending of fl32(w[t][j] * y[t*K+j][n])),
 // y the bf16 rows the w2 epilogue stored; FP32 partial sums, the first term
-// taken as is.  8 columns per thread: the K rows' 16-byte words are all
-// loaded before the sum starts.
+// taken as is.  One CTA per token row at a time, 8 columns per thread: the K
+// rows' 16-byte words are all loaded before the sum starts.
 constexpr int FIN_MAX_K = 16;
 __global__ void __launch_bounds__(256) finalize_ordered_kernel(const uint16_t* __restrict__ ybuf,
                                                               const float* __restrict__ topk_w,
@@ -293,30 +295,31 @@ __global__ void __launch_bounds__(256) finalize_ordered_kernel(const uint16_t* _
   pdl_trigger();
   pdl_wait();
   const int h8 = H / 8;
-  const size_t n8 = (size_t)T * h8;
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
-    const int t = (int)(i / h8), c = (int)(i % h8);
-    const uint4* yr = reinterpret_cast<const uint4*>(ybuf) + (size_t)t * K * h8 + c;
-    uint4 y[FIN_MAX_K];
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    const uint4* yt = reinterpret_cast<const uint4*>(ybuf) + (size_t)t * K * h8;
+    const float* wt = topk_w + (size_t)t * K;
+    for (int c = threadIdx.x; c < h8; c += blockDim.x) {
+      uint4 y[FIN_MAX_K];
 #pragma unroll
-    for (int j = 0; j < FIN_MAX_K; ++j)
-      if (j < K) y[j] = __ldcs(yr + (size_t)j * h8);  // read once: streaming
-    float s[8];
+      for (int j = 0; j < FIN_MAX_K; ++j)
+        if (j < K) y[j] = __ldcs(yt + (size_t)j * h8 + c);  // read once: streaming
+      float s[8];
 #pragma unroll
-    for (int j = 0; j < FIN_MAX_K; ++j) {
-      if (j < K) {
-        const float w = __ldg(topk_w + (size_t)t * K + j);
-        const uint32_t yw[4] = {y[j].x, y[j].y, y[j].z, y[j].w};
+      for (int j = 0; j < FIN_MAX_K; ++j) {
+        if (j < K) {
+          const float w = __ldg(wt + j);
+          const uint32_t yw[4] = {y[j].x, y[j].y, y[j].z, y[j].w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float p0 = __fmul_rn(w, bf16_lo(yw[q])), p1 = __fmul_rn(w, bf16_hi(yw[q]));
-          s[2 * q] = j == 0 ? p0 : __fadd_rn(s[2 * q], p0);
-          s[2 * q + 1] = j == 0 ? p1 : __fadd_rn(s[2 * q + 1], p1);
+          for (int q = 0; q < 4; ++q) {
+            const float p0 = __fmul_rn(w, bf16_lo(yw[q])), p1 = __fmul_rn(w, bf16_hi(yw[q]));
+            s[2 * q] = j == 0 ? p0 : __fadd_rn(s[2 * q], p0);
+            s[2 * q + 1] = j == 0 ? p1 : __fadd_rn(s[2 * q + 1], p1);
+          }
         }
       }
+      reinterpret_cast<uint4*>(out + (size_t)t * H)[c] =
+          make_uint4(pack_bf16x2(s[0], s[1]), pack_bf16x2(s[2], s[3]), pack_bf16x2(s[4], s[5]), pack_bf16x2(s[6], s[7]));
     }
-    reinterpret_cast<uint4*>(out)[i] =
-        make_uint4(pack_bf16x2(s[0], s[1]), pack_bf16x2(s[2], s[3]), pack_bf16x2(s[4], s[5]), pack_bf16x2(s[6], s[7]));
   }
 }
 
@@ -391,8 +394,8 @@ cudaError_t launch_finalize_atomic(const float* out_acc, void* out, int T, int H
 cudaError_t launch_finalize_ordered(const uint16_t* ybuf, const float* topk_w, void* out, int T, int H, int K,
                                     cudaStream_t s) {
   if (K > FIN_MAX_K || H % 8) return cudaErrorInvalidValue;
-  const size_t n8 = (size_t)T * H / 8;
-  return launch_k(finalize_ordered_kernel, dim3(grid_for(n8, 256)), dim3(256), 0, s, true, ybuf, topk_w,
+  // one token row per CTA and pass; up to 8 resident CTAs per SM
+  return launch_k(finalize_ordered_kernel, dim3(std::min(T, 152 * 8)), dim3(256), 0, s, true, ybuf, topk_w,
                   reinterpret_cast<__nv_bfloat16*>(out), T, H, K);
 }
 

@@ -482,6 +482,13 @@ __global__ void __launch_bounds__(256) front_small_kernel(const FrontArgs p) {
   // The w13 GEMM may launch now and stage weights; it reads this kernel's
   // outputs only after its dependency wait.
   pdl_trigger();
+  // Padded row e*128 + t of this CTA's experts and tokens starts as "not
+  // routed here"; the top-k phase marks the K chosen ones after this CTA's
+  // release of the token block's counter.
+  if (threadIdx.x < EB * TOK) {
+    const int e = blockIdx.y * EB + threadIdx.x / TOK, t = tb0 + threadIdx.x % TOK;
+    if (t < T) p.src_of_padrow[e * 128 + t] = -1;
+  }
   router_tile<TB, EB, false, XSMEM>(x, reinterpret_cast<const __nv_bfloat16*>(p.gate_w), p.bias, p.logits, T, H,
                                      E);
 
@@ -543,14 +550,7 @@ __global__ void __launch_bounds__(256) front_small_kernel(const FrontArgs p) {
       if (lane < K) {
         p.topk_ids[(size_t)t * K + lane] = e_lane;
         p.topk_w[(size_t)t * K + lane] = w;
-      }
-      for (int base = 0; base < E; base += 32) {  // every expert's padded row t
-        const int e = base + lane;
-        int src = -1;
-#pragma unroll 1
-        for (int j = 0; j < K; ++j)
-          if (__shfl_sync(0xffffffffu, e_lane, j) == e) src = t * K + j;
-        if (e < E) p.src_of_padrow[e * 128 + t] = src;
+        p.src_of_padrow[e_lane * 128 + t] = t * K + lane;  // the other experts' rows hold -1
       }
     }
     if (threadIdx.x == 0) p.sync[blockIdx.x] = 0;
