@@ -289,9 +289,13 @@ __global__ void __launch_bounds__(256) finalize_atomic_kernel(const float* __res
 // taken as is.  One CTA per token row at a time, 8 columns per thread: the K
 // rows' 16-byte words are all loaded before the sum starts.
 constexpr int FIN_MAX_K = 16;
-__global__ void __launch_bounds__(256) finalize_ordered_kernel(const uint16_t* __restrict__ ybuf,
-                                                              const float* __restrict__ topk_w,
-                                                              __nv_bfloat16* __restrict__ out, int T, int H, int K) {
+// KMAX bounds K at compile time: the K rows' words live in registers, so a
+// small bound (top-k <= 8) leaves room for more resident CTAs.
+template <int KMAX>
+__global__ void __launch_bounds__(256, KMAX <= 8 ? 4 : 2) finalize_ordered_kernel(const uint16_t* __restrict__ ybuf,
+                                                                                  const float* __restrict__ topk_w,
+                                                                                  __nv_bfloat16* __restrict__ out, int T,
+                                                                                  int H, int K) {
   pdl_trigger();
   pdl_wait();
   const int h8 = H / 8;
@@ -299,13 +303,13 @@ __global__ void __launch_bounds__(256) finalize_ordered_kernel(const uint16_t* _
     const uint4* yt = reinterpret_cast<const uint4*>(ybuf) + (size_t)t * K * h8;
     const float* wt = topk_w + (size_t)t * K;
     for (int c = threadIdx.x; c < h8; c += blockDim.x) {
-      uint4 y[FIN_MAX_K];
+      uint4 y[KMAX];
 #pragma unroll
-      for (int j = 0; j < FIN_MAX_K; ++j)
+      for (int j = 0; j < KMAX; ++j)
         if (j < K) y[j] = __ldcs(yt + (size_t)j * h8 + c);  // read once: streaming
       float s[8];
 #pragma unroll
-      for (int j = 0; j < FIN_MAX_K; ++j) {
+      for (int j = 0; j < KMAX; ++j) {
         if (j < K) {
           const float w = __ldg(wt + j);
           const uint32_t yw[4] = {y[j].x, y[j].y, y[j].z, y[j].w};
@@ -394,9 +398,12 @@ cudaError_t launch_finalize_atomic(const float* out_acc, void* out, int T, int H
 cudaError_t launch_finalize_ordered(const uint16_t* ybuf, const float* topk_w, void* out, int T, int H, int K,
                                     cudaStream_t s) {
   if (K > FIN_MAX_K || H % 8) return cudaErrorInvalidValue;
-  // one token row per CTA and pass; up to 8 resident CTAs per SM
-  return launch_k(finalize_ordered_kernel, dim3(std::min(T, 152 * 8)), dim3(256), 0, s, true, ybuf, topk_w,
-                  reinterpret_cast<__nv_bfloat16*>(out), T, H, K);
+  // one token row per CTA and pass
+  if (K <= 8)
+    return launch_k(finalize_ordered_kernel<8>, dim3(std::min(T, 152 * 8)), dim3(256), 0, s, true, ybuf, topk_w,
+                    reinterpret_cast<__nv_bfloat16*>(out), T, H, K);
+  return launch_k(finalize_ordered_kernel<FIN_MAX_K>, dim3(std::min(T, 152 * 8)), dim3(256), 0, s, true, ybuf,
+                  topk_w, reinterpret_cast<__nv_bfloat16*>(out), T, H, K);
 }
 
 }  // namespace moe
