@@ -45,6 +45,21 @@ design notes):
   with FP32 partial sums, the first term taken as is.
 * rows [0, I) of w13[e] are the gate projection, rows [I, 2I) the up
   projection.
+
+Optional shared expert ("SM10X Command-A-Plus decode 2.3x faster, BCG capture
+memory -78%", the Cohere2MoE sparse-block listing: the shared experts read the
+same post-norm input as the routed experts, their output is added to the
+routed output, and the 'average' combination strategy halves the sum):
+
+* the shared expert is one more NVFP4 SwiGLU MLP (w13s [2Is, H], w2s [H, Is],
+  one global scale per tensor) on every token, with the same per-token
+  quantized input as the routed experts and the same requantization of its
+  intermediate (the pages do not say how it is quantized; this reading keeps
+  one activation contract for the layer);
+* combination in FP32 with one bf16 rounding at the end:
+  out = bf16( fl32(routed + shared) ), or bf16( fl32(fl32(routed + shared)
+  * 0.5) ) for 'average' (the pages add two bf16 tensors; the reading keeps
+  FP32 until the single rounding the layer output needs).
 """
 
 from __future__ import annotations
@@ -253,9 +268,24 @@ class ForwardResult:
     y2: dict                    # (t, j) -> float32 [H]
 
 
+def shared_expert_rows(x_codes, x_sf, x_gs, w13s: QuantWeights, w2s: QuantWeights) -> np.ndarray:
+    """The shared expert on every token's quantized input: the FP32 w2
+    output [n, H] of its NVFP4 SwiGLU MLP (one expert, weight 1)."""
+    return expert_rows(x_codes, x_sf, x_gs, w13s, w2s, 0)["y2"]
+
+
+def combine_shared(routed_f32: np.ndarray, shared_f32: np.ndarray, average: bool) -> np.ndarray:
+    """fl32(routed + shared), halved (one more FP32 rounding) for 'average'."""
+    s = (np.asarray(routed_f32, np.float32) + np.asarray(shared_f32, np.float32)).astype(np.float32)
+    if average:
+        s = (s * np.float32(0.5)).astype(np.float32)
+    return s
+
+
 def moe_forward(x: np.ndarray, wg: np.ndarray, w13: QuantWeights, w2: QuantWeights,
                 top_k: int, bias: Optional[np.ndarray] = None,
-                tokens: Optional[Sequence[int]] = None, static_scales=None) -> ForwardResult:
+                tokens: Optional[Sequence[int]] = None, static_scales=None,
+                shared=None, shared_average: bool = False) -> ForwardResult:
     """Forward of the routed MoE layer for all tokens, or for ``tokens`` only.
 
     Tokens are independent in this layer, so a subset gives the same rows as
@@ -269,6 +299,10 @@ def moe_forward(x: np.ndarray, wg: np.ndarray, w13: QuantWeights, w2: QuantWeigh
     Summary and Implementation item 2): one calibrated FP32 global scale for
     the first GEMM's input, and one per expert (``h_gs`` [E]) for the second
     GEMM's input.
+
+    ``shared``: None, or a pair (w13s, w2s) of single-expert QuantWeights for
+    the shared expert, combined with the routed output by sum or, with
+    ``shared_average``, by the average (see the module notes).
     """
     x = np.asarray(x, dtype=np.float32)
     tok = np.arange(x.shape[0]) if tokens is None else np.asarray(tokens, dtype=np.int64)
@@ -293,6 +327,9 @@ def moe_forward(x: np.ndarray, wg: np.ndarray, w13: QuantWeights, w2: QuantWeigh
             h_gs[(int(tok[t]), int(j))] = r["h_gs"][i]
             y2_map[(int(tok[t]), int(j))] = r["y2"][i]
     out_f32 = finalize(y_rows, weights) if n else np.zeros((0, H), np.float32)
+    if shared is not None and n:
+        out_f32 = combine_shared(out_f32, shared_expert_rows(x_codes, x_sf, x_gs, shared[0], shared[1]),
+                                 shared_average)
     bits = nvfp4.bf16_round(out_f32)
     return ForwardResult(out_bits=bits, out=nvfp4.bf16_to_f32(bits), out_f32=out_f32,
                          logits=logits, ids=ids, weights=weights, x_codes=x_codes,
