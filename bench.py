@@ -36,11 +36,12 @@ STAGES = ("router", "topk", "permute", "quantize", "gemm_w13", "gemm_w2", "final
 SMALL_BATCH_TOKENS = 64           # the library's fused small-batch front end and atomic finalize
 
 
-def kernels_per_forward(s, T):
+def kernels_per_forward(s, T, shared_inter=0):
     """Kernel launches of one forward: router, top-k, permute, quantize, w13,
     w2, finalize.  Up to 64 tokens: one fused front end, w13, the row
-    requantization, w2, finalize (the bench runs per-token scales)."""
-    return 7 if T > SMALL_BATCH_TOKENS else 5
+    requantization, w2, finalize (the bench runs per-token scales).  A shared
+    expert adds four on its own stream: tile list, quantize, w13, w2."""
+    return (7 if T > SMALL_BATCH_TOKENS else 5) + (4 if shared_inter else 0)
 
 
 def ordered_finalize(s, T):
@@ -59,6 +60,10 @@ def parse():
     p.add_argument("--tokens", type=int, default=None, help="override T of the workload")
     p.add_argument("--cpu-sample", type=int, default=4, help="tokens per oracle step")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--shared-inter", type=int, default=0,
+                   help="add a shared expert of this intermediate width (0: routed experts only)")
+    p.add_argument("--shared-average", action="store_true",
+                   help="combine routed and shared outputs by their average instead of their sum")
     p.add_argument("--oracle-worker", action="store_true", help=argparse.SUPPRESS)
     return p.parse_args()
 
@@ -92,10 +97,15 @@ def oracle_worker(args):
     for e in experts:
         q13.codes[e], q13.sf[e], q13.gs[e] = onv.quantize_tensor(omoe.as_f32(wl.w13[e]))
         q2.codes[e], q2.sf[e], q2.gs[e] = onv.quantize_tensor(omoe.as_f32(wl.w2[e]))
+    shared = None
+    if args.shared_inter:
+        w13s, w2s = synthetic.make_shared_weights(s, args.shared_inter)
+        shared = (omoe.quantize_weights(omoe.as_f32(w13s)[None]), omoe.quantize_weights(omoe.as_f32(w2s)[None]))
     times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        omoe.moe_forward(x, wg, q13, q2, s.K, bias, tokens=tokens)
+        omoe.moe_forward(x, wg, q13, q2, s.K, bias, tokens=tokens, shared=shared,
+                         shared_average=args.shared_average)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             times.append(dt)
@@ -109,6 +119,8 @@ def run_oracle(args, steps, warmup):
            "--steps", str(steps), "--warmup", str(warmup), "--cpu-sample", str(args.cpu_sample)]
     if args.tokens:
         cmd += ["--tokens", str(args.tokens)]
+    if args.shared_inter:
+        cmd += ["--shared-inter", str(args.shared_inter)] + (["--shared-average"] if args.shared_average else [])
     r = subprocess.run(cmd, capture_output=True, text=True, env=env)
     if r.returncode != 0:
         raise RuntimeError(f"oracle worker failed: {r.stderr[-2000:]}")
@@ -287,18 +299,26 @@ def stage_alg_bytes(s, T, touched):
     }
 
 
-def layer_alg_bytes(s, T, touched):
-    # x in, out, router weight, and the NVFP4 weights of the experts that got rows
-    return 2 * T * s.H + 2 * T * s.H + 2 * s.H * s.E + touched * 3 * s.I * s.H * NVFP4_BYTES_PER_ELT
+def layer_alg_bytes(s, T, touched, shared_inter=0):
+    # x in, out, router weight, and the NVFP4 weights of the experts that got
+    # rows (and of the shared expert)
+    return (2 * T * s.H + 2 * T * s.H + 2 * s.H * s.E
+            + (touched * 3 * s.I + 3 * shared_inter) * s.H * NVFP4_BYTES_PER_ELT)
 
 
 # --------------------------------------------------------------------------
 # Our implementation
 # --------------------------------------------------------------------------
 
-def workload_config(s, T, world):
-    return {"workload": f"{s.name}: T={T} H={s.H} E={s.E} top-{s.K} I={s.I}, CUDA-graph replay",
-            "T": T, "H": s.H, "E": s.E, "top_k": s.K, "I": s.I,
+def workload_config(s, T, world, shared_inter=0, shared_average=False):
+    extra = {}
+    shared_desc = ""
+    if shared_inter:
+        combine = "average" if shared_average else "sum"
+        extra = {"shared_inter": shared_inter, "shared_combine": combine}
+        shared_desc = f" + shared expert Is={shared_inter} ({combine}, second stream)"
+    return {"workload": f"{s.name}: T={T} H={s.H} E={s.E} top-{s.K} I={s.I}{shared_desc}, CUDA-graph replay",
+            "T": T, "H": s.H, "E": s.E, "top_k": s.K, "I": s.I, **extra,
             "finalize": ("ordered: bf16 (token, slot) rows summed in slot order" if ordered_finalize(s, T)
                          else "fp32 atomic in the w2 epilogue"),
             "l2": "flushed before every step outside the timed events: a 256 MB write, then a 256 MB read of "
@@ -338,8 +358,13 @@ def run_ours(args, rank, world, local_rank):
     wl = synthetic.make_workload(args.config, T=args.tokens)
     s = wl.shape
     T = wl.T
-    layer = MoE.from_shape(s, device=local_rank)
+    Is = args.shared_inter
+    layer = MoE(s.H, s.I, s.E, s.K, s.max_num_tokens, device=local_rank, deterministic=s.deterministic,
+                shared_inter=Is, shared_average=args.shared_average)
     layer.load_weights(wl.w13.to(dev), wl.w2.to(dev))
+    if Is:
+        w13s, w2s = synthetic.make_shared_weights(s, Is)
+        layer.load_shared_weights(w13s.to(dev), w2s.to(dev))
     x = wl.x.to(dev)
     gate_w = wl.gate_w.to(dev)
     bias = None if wl.bias is None else wl.bias.to(dev)
@@ -448,7 +473,7 @@ def run_ours(args, rank, world, local_rank):
     alg = stage_alg_bytes(s, T, touched)
     peak, peak_kind = measured_peaks()
     achieved = alg[dom] / (mean_stage[dom] / 1e3) / 1e9
-    layer_bytes = layer_alg_bytes(s, T, touched)
+    layer_bytes = layer_alg_bytes(s, T, touched, Is)
     layer_gbs = layer_bytes / (ms_per_step / 1e3) / 1e9
     result = {
         "metric": METRIC,
@@ -463,7 +488,7 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "nvfp4 (e2m1 x e2m1 with e4m3 block scales, fp32 accumulate)",
         "data": "synthetic (seeded bf16 N(0,1) activations, N(0,0.02) router/expert weights)",
-        "config": workload_config(s, T, world),
+        "config": workload_config(s, T, world, Is, args.shared_average),
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs",
                      "alg_bytes_per_launch": alg[dom], "launch_ms": mean_stage[dom],
@@ -475,7 +500,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": T * world / (e2e_total / args.steps), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "path": "moe_forward_host (pinned host buffers, eager launches)"},
-        "gpu_launches": kernels_per_forward(s, T) * args.steps,
+        "gpu_launches": kernels_per_forward(s, T, Is) * args.steps,
         "clocks": clk,
     }
     layer.close()
@@ -500,7 +525,8 @@ def main():
         line = {"impl": "reference", "metric": METRIC, "value": r["value"], "unit": "tokens/s", "n_gpus": 1,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["seconds_per_step"] * 1e3,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
-                "data": "synthetic", "config": workload_config(s, s.T if args.tokens is None else args.tokens, 1),
+                "data": "synthetic", "config": workload_config(s, s.T if args.tokens is None else args.tokens, 1,
+                                                          args.shared_inter, args.shared_average),
                 "cpu_baseline": {k: r[k] for k in ("value", "unit", "cores", "kind", "sample")},
                 "e2e": {"value": r["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))

@@ -100,6 +100,13 @@ typedef enum {
  * the scale exceeds 2688 saturate (block scale 448, codes +-6). */
 #define MOE_FLAG_STATIC_ACT_SCALES 2u
 
+/* Shared-expert combination: with a shared expert (moe_config.shared_inter
+ * > 0) the layer output is routed + shared by default; with this flag it is
+ * (routed + shared) / 2, the 'average' combination strategy of the
+ * Cohere2MoE sparse block in "SM10X Command-A-Plus decode 2.3x faster, BCG
+ * capture memory -78%" (its key source listing). */
+#define MOE_FLAG_SHARED_AVERAGE 4u
+
 typedef struct {
   int hidden;          /* H: model width (K dim of w13, N dim of w2) */
   int inter;           /* I: expert intermediate width */
@@ -108,6 +115,9 @@ typedef struct {
   int max_num_tokens;  /* worst-case tokens of one forward; fixes all buffer sizes */
   int device;          /* CUDA device ordinal */
   unsigned flags;      /* MOE_FLAG_* */
+  int shared_inter;    /* Is: intermediate width of the shared expert, 0 = none
+                          (a multiple of 128, at most 2048; not with
+                          MOE_FLAG_STATIC_ACT_SCALES) */
 } moe_config;
 
 typedef enum { MOE_DTYPE_BF16 = 1 } moe_dtype;
@@ -148,6 +158,26 @@ MOE_API moe_status moe_load_weights(moe_handle* h, const void* w13, const moe_we
  * graph would then need to be recaptured).  Never reallocates. */
 MOE_API moe_status moe_refresh_scales_inplace(moe_handle* h, const void* w13, const moe_weight_desc* w13_desc,
                                       const void* w2, const moe_weight_desc* w2_desc, void* stream);
+
+/* Shared expert ("SM10X Command-A-Plus decode 2.3x faster, BCG capture
+ * memory -78%", the Cohere2MoE sparse block of its key source listing: the
+ * shared experts read the same input as the routed experts, on a second
+ * stream while the routed experts run, and their output is added to the
+ * routed output).  Online NVFP4 conversion of its bf16 weights, as
+ * moe_load_weights does for one expert:
+ *   w13s: [1, 2*Is, H] bf16 (gate rows [0, Is), up rows [Is, 2*Is));
+ *   w2s:  [1, H, Is] bf16.
+ * Calling it again requantizes into the same buffers (a captured graph stays
+ * valid).  MOE_ERR_INVALID_ARG if the handle has no shared expert or a shape
+ * differs.  With a shared expert, moe_forward returns MOE_ERR_NOT_LOADED
+ * until this has been called.  Every forward then quantizes x per token once
+ * more on the handle's second stream (forked from and joined back into the
+ * caller's stream, so capture works as for moe_forward), runs the shared
+ * expert's two GEMMs there, and the finalize adds (or averages, with
+ * MOE_FLAG_SHARED_AVERAGE) its bf16 output rows into the routed sum in FP32
+ * before the single bf16 rounding of the output. */
+MOE_API moe_status moe_load_shared_weights(moe_handle* h, const void* w13s, const moe_weight_desc* w13s_desc,
+                                           const void* w2s, const moe_weight_desc* w2s_desc, void* stream);
 
 /* Calibrated global scales of the static contract, copied on `stream` into
  * handle-owned buffers (the same buffers every time, so a captured graph
@@ -296,6 +326,15 @@ MOE_API moe_status moe_debug_weight_quant(moe_handle* h, int which, uint8_t* cod
  * h_sf uint8 [R, I/16], h_gs f32 [R], indexed by src = t*K + j. */
 MOE_API moe_status moe_debug_intermediate(moe_handle* h, uint8_t* h_codes, uint8_t* h_sf, float* h_gs,
                                   void* stream);
+
+/* The shared expert's part of the last forward (handles with a shared expert
+ * only): rows bf16 [T, H], its w2 output for token t before the combination;
+ * h_codes uint8 [T, Is/2], h_sf uint8 [T, Is/16], h_gs f32 [T], its
+ * requantized intermediate.  Device pointers; rows may be NULL, and the
+ * other three are all given or all NULL.  MOE_ERR_INVALID_ARG without a
+ * shared expert, MOE_ERR_NOT_LOADED before the first forward. */
+MOE_API moe_status moe_debug_shared(moe_handle* h, uint16_t* rows, uint8_t* h_codes, uint8_t* h_sf, float* h_gs,
+                                    void* stream);
 
 /* Addresses of every device buffer the handle owns (weights, scales,
  * workspace), for checking that load/refresh never moves them.  On entry *n

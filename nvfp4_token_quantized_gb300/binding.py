@@ -27,6 +27,7 @@ MOE_ERR_DEVICE_TIMEOUT = 7
 MOE_ERR_UNSUPPORTED = 8
 MOE_FLAG_DETERMINISTIC = 1
 MOE_FLAG_STATIC_ACT_SCALES = 2
+MOE_FLAG_SHARED_AVERAGE = 4
 MOE_DTYPE_BF16 = 1
 
 EXPORTED = (
@@ -35,7 +36,8 @@ EXPORTED = (
     "moe_status_string", "moe_get_status", "moe_debug_routing", "moe_debug_logits",
     "moe_debug_act_quant", "moe_debug_weight_quant", "moe_debug_intermediate", "moe_debug_buffer_ptrs",
     "moe_debug_convert", "moe_debug_block_scaled_gemm", "moe_set_stage_timing", "moe_get_stage_times",
-    "moe_stage_name", "moe_route_noalloc", "moe_set_static_scales",
+    "moe_stage_name", "moe_route_noalloc", "moe_set_static_scales", "moe_load_shared_weights",
+    "moe_debug_shared",
 )
 MOE_ROUTE_NOALLOC_MAX_LOGITS = 1 << 20
 MOE_NUM_STAGES = 7
@@ -44,7 +46,7 @@ MOE_NUM_STAGES = 7
 class moe_config(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int), ("inter", ctypes.c_int), ("num_experts", ctypes.c_int),
                 ("top_k", ctypes.c_int), ("max_num_tokens", ctypes.c_int), ("device", ctypes.c_int),
-                ("flags", ctypes.c_uint)]
+                ("flags", ctypes.c_uint), ("shared_inter", ctypes.c_int)]
 
 
 class moe_weight_desc(ctypes.Structure):
@@ -78,6 +80,8 @@ def load_library() -> ctypes.CDLL:
         "moe_create": (I, [ctypes.POINTER(moe_config), ctypes.POINTER(P)]),
         "moe_destroy": (I, [P]),
         "moe_load_weights": (I, [P, P, ctypes.POINTER(moe_weight_desc), P, ctypes.POINTER(moe_weight_desc), P]),
+        "moe_load_shared_weights": (I, [P, P, ctypes.POINTER(moe_weight_desc), P, ctypes.POINTER(moe_weight_desc),
+                                        P]),
         "moe_refresh_scales_inplace": (I, [P, P, ctypes.POINTER(moe_weight_desc), P,
                                            ctypes.POINTER(moe_weight_desc), P]),
         "moe_forward": (I, [P, P, P, P, I, P]),
@@ -100,6 +104,7 @@ def load_library() -> ctypes.CDLL:
         "moe_stage_name": (ctypes.c_char_p, [I]),
         "moe_route_noalloc": (I, [P, P, P, I, I, I, I, P, P, P]),
         "moe_set_static_scales": (I, [P, P, P, P]),
+        "moe_debug_shared": (I, [P, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -148,9 +153,9 @@ def _wdesc(t: torch.Tensor) -> moe_weight_desc:
 # ---- functions with the C names (handles are ctypes c_void_p) ----
 
 def moe_create(hidden: int, inter: int, num_experts: int, top_k: int, max_num_tokens: int, device: int = 0,
-               flags: int = 0) -> ctypes.c_void_p:
+               flags: int = 0, shared_inter: int = 0) -> ctypes.c_void_p:
     lib = load_library()
-    cfg = moe_config(hidden, inter, num_experts, top_k, max_num_tokens, device, flags)
+    cfg = moe_config(hidden, inter, num_experts, top_k, max_num_tokens, device, flags, shared_inter)
     h = ctypes.c_void_p()
     st = lib.moe_create(ctypes.byref(cfg), ctypes.byref(h))
     if st != MOE_OK:
@@ -172,6 +177,15 @@ def moe_load_weights(h, w13: torch.Tensor, w2: torch.Tensor, stream=None) -> Non
     d13, d2 = _wdesc(w13), _wdesc(w2)
     _raise(h, load_library().moe_load_weights(h, _ptr(w13), ctypes.byref(d13), _ptr(w2), ctypes.byref(d2),
                                               _stream(stream)))
+
+
+def moe_load_shared_weights(h, w13s: torch.Tensor, w2s: torch.Tensor, stream=None) -> None:
+    """The shared expert's bf16 weights: w13s [2*Is, H] (gate rows, then up rows), w2s [H, Is]."""
+    w13s = w13s.unsqueeze(0) if w13s.dim() == 2 else w13s
+    w2s = w2s.unsqueeze(0) if w2s.dim() == 2 else w2s
+    d13, d2 = _wdesc(w13s), _wdesc(w2s)
+    _raise(h, load_library().moe_load_shared_weights(h, _ptr(w13s), ctypes.byref(d13), _ptr(w2s), ctypes.byref(d2),
+                                                     _stream(stream)))
 
 
 def moe_refresh_scales_inplace(h, w13: torch.Tensor, w2: torch.Tensor, stream=None) -> None:
@@ -260,13 +274,16 @@ class MoE:
     """Owner of one library handle: a routed-MoE layer with fixed sizes."""
 
     def __init__(self, hidden: int, inter: int, num_experts: int, top_k: int, max_num_tokens: int,
-                 device: int = 0, deterministic: bool = False, static_scales: bool = False):
+                 device: int = 0, deterministic: bool = False, static_scales: bool = False,
+                 shared_inter: int = 0, shared_average: bool = False):
         self.H, self.I, self.E, self.K, self.Tmax = hidden, inter, num_experts, top_k, max_num_tokens
         self.device = device
         self.deterministic = deterministic
         self.static_scales = static_scales
+        self.shared_inter, self.shared_average = shared_inter, shared_average
         flags = (MOE_FLAG_DETERMINISTIC if deterministic else 0) | (MOE_FLAG_STATIC_ACT_SCALES if static_scales else 0)
-        self._h = moe_create(hidden, inter, num_experts, top_k, max_num_tokens, device, flags)
+        flags |= MOE_FLAG_SHARED_AVERAGE if shared_average else 0
+        self._h = moe_create(hidden, inter, num_experts, top_k, max_num_tokens, device, flags, shared_inter)
         self.last_T = None
 
     @classmethod
@@ -295,6 +312,9 @@ class MoE:
 
     def load_weights(self, w13: torch.Tensor, w2: torch.Tensor, stream=None):
         moe_load_weights(self._h, w13, w2, stream)
+
+    def load_shared_weights(self, w13s: torch.Tensor, w2s: torch.Tensor, stream=None):
+        moe_load_shared_weights(self._h, w13s, w2s, stream)
 
     def refresh_scales_inplace(self, w13: torch.Tensor, w2: torch.Tensor, stream=None):
         moe_refresh_scales_inplace(self._h, w13, w2, stream)
@@ -372,6 +392,19 @@ class MoE:
         _raise(self._h, load_library().moe_debug_intermediate(self._h, _ptr(codes), _ptr(sf), _ptr(gs),
                                                               _stream(stream)))
         return codes, sf, gs
+
+    def debug_shared(self, stream=None):
+        """The shared expert's bf16 rows [T, H] and requantized intermediate
+        (codes [T, Is/2], block scales [T, Is/16], global scales [T]) of the
+        last forward."""
+        T = self.last_T or 0
+        rows = self._dev((T, self.H), torch.bfloat16)
+        codes = self._dev((T, self.shared_inter // 2), torch.uint8)
+        sf = self._dev((T, self.shared_inter // 16), torch.uint8)
+        gs = self._dev((T,), torch.float32)
+        _raise(self._h, load_library().moe_debug_shared(self._h, _ptr(rows), _ptr(codes), _ptr(sf), _ptr(gs),
+                                                        _stream(stream)))
+        return rows, codes, sf, gs
 
     def set_stage_timing(self, enable: bool = True):
         _raise(self._h, load_library().moe_set_stage_timing(self._h, int(enable)))

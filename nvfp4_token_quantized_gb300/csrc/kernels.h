@@ -57,10 +57,17 @@ cudaError_t launch_sf_to_atoms(const uint8_t* sf, int rows, int k16, uint8_t* at
 cudaError_t launch_codes_to_tiled(const uint8_t* codes, int rows, int row_bytes, uint8_t* tiled, cudaStream_t s);
 
 // ---- finalize (kernels_quant.cu) ----
-cudaError_t launch_finalize_atomic(const float* out_acc, void* out, int T, int H, cudaStream_t s);
+// shared: nullptr, or bf16 rows [T][H] of a shared expert added to the
+// routed sum in FP32 and the sum scaled by shared_scale before the bf16
+// rounding.
+cudaError_t launch_finalize_atomic(const float* out_acc, const uint16_t* shared, float shared_scale, void* out, int T,
+                                   int H, cudaStream_t s);
 // ybuf: bf16 rows [t * K + j][H] of the weighted-sum operands.
-cudaError_t launch_finalize_ordered(const uint16_t* ybuf, const float* topk_w, void* out, int T, int H, int K,
-                                    cudaStream_t s);
+cudaError_t launch_finalize_ordered(const uint16_t* ybuf, const float* topk_w, const uint16_t* shared,
+                                    float shared_scale, void* out, int T, int H, int K, cudaStream_t s);
+// The shared expert's tile list: ceil(T/128) tiles of expert 0 over rows
+// 0..T-1 ({0, 128 i, valid rows, 128 i}).
+cudaError_t launch_shared_tiles(int T, int4* tiles, int32_t* num_tiles, cudaStream_t s);
 
 // ---- block-scaled FP4 GEMMs (kernels_gemm.cu) ----
 // Small batches (T <= SMALL_BATCH_TOKENS): router logits, per-token

@@ -253,8 +253,22 @@ __global__ void sf_to_atoms_kernel(const uint8_t* __restrict__ sf, int rows, int
   }
 }
 
-// out = bf16_rn(acc), 8 elements per thread.
+// The shared expert's contribution to 8 consecutive outputs: the FP32 routed
+// sums v[0..8) become fl32(fl32(v + shared) * scale) (scale 1: the sum; 0.5:
+// the average), from the shared expert's bf16 output word `sh` (8 values).
+__device__ __forceinline__ void add_shared8(float (&v)[8], const uint4& sh, float scale) {
+  const uint32_t w[4] = {sh.x, sh.y, sh.z, sh.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    v[2 * q] = __fmul_rn(__fadd_rn(v[2 * q], bf16_lo(w[q])), scale);
+    v[2 * q + 1] = __fmul_rn(__fadd_rn(v[2 * q + 1], bf16_hi(w[q])), scale);
+  }
+}
+
+// out = bf16_rn(acc), 8 elements per thread; with a shared expert,
+// bf16_rn(fl32(acc + shared) * scale).
 __global__ void __launch_bounds__(256) finalize_atomic_kernel(const float* __restrict__ acc,
+                                                             const uint16_t* __restrict__ shared, float shared_scale,
                                                              __nv_bfloat16* __restrict__ out, size_t n8) {
   pdl_trigger();
   pdl_wait();
@@ -276,9 +290,10 @@ __global__ void __launch_bounds__(256) finalize_atomic_kernel(const float* __res
     for (int q = 0; q < FIN_ILP; ++q) {
       const size_t i = base + (size_t)q * blockDim.x;
       if (i < n8) {
-        __nv_bfloat162 o[4] = {__floats2bfloat162_rn(a[q].x, a[q].y), __floats2bfloat162_rn(a[q].z, a[q].w),
-                               __floats2bfloat162_rn(b[q].x, b[q].y), __floats2bfloat162_rn(b[q].z, b[q].w)};
-        reinterpret_cast<uint4*>(out)[i] = *reinterpret_cast<const uint4*>(o);
+        float v[8] = {a[q].x, a[q].y, a[q].z, a[q].w, b[q].x, b[q].y, b[q].z, b[q].w};
+        if (shared) add_shared8(v, reinterpret_cast<const uint4*>(shared)[i], shared_scale);
+        reinterpret_cast<uint4*>(out)[i] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                                      pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
       }
     }
   }
@@ -291,9 +306,13 @@ __global__ void __launch_bounds__(256) finalize_atomic_kernel(const float* __res
 constexpr int FIN_MAX_K = 16;
 // KMAX bounds K at compile time: the K rows' words live in registers, so a
 // small bound (top-k <= 8) leaves room for more resident CTAs.
+// With a shared expert, its bf16 row t is added to the FP32 sum and the
+// result scaled (add_shared8) before the rounding.
 template <int KMAX>
 __global__ void __launch_bounds__(256, KMAX <= 8 ? 4 : 2) finalize_ordered_kernel(const uint16_t* __restrict__ ybuf,
                                                                                   const float* __restrict__ topk_w,
+                                                                                  const uint16_t* __restrict__ shared,
+                                                                                  float shared_scale,
                                                                                   __nv_bfloat16* __restrict__ out, int T,
                                                                                   int H, int K) {
   pdl_trigger();
@@ -321,10 +340,18 @@ __global__ void __launch_bounds__(256, KMAX <= 8 ? 4 : 2) finalize_ordered_kerne
           }
         }
       }
+      if (shared) add_shared8(s, reinterpret_cast<const uint4*>(shared + (size_t)t * H)[c], shared_scale);
       reinterpret_cast<uint4*>(out + (size_t)t * H)[c] =
           make_uint4(pack_bf16x2(s[0], s[1]), pack_bf16x2(s[2], s[3]), pack_bf16x2(s[4], s[5]), pack_bf16x2(s[6], s[7]));
     }
   }
+}
+
+// The shared expert's tile list: rows 0..T-1 of expert 0 in 128-row tiles.
+__global__ void shared_tiles_kernel(int T, int4* __restrict__ tiles, int32_t* __restrict__ num_tiles) {
+  const int n = (T + 127) / 128;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) tiles[i] = make_int4(0, 128 * i, min(128, T - 128 * i), 128 * i);
+  if (threadIdx.x == 0) *num_tiles = n;
 }
 
 int grid_for(size_t n, int per_block, int cap = 152 * 16) {
@@ -389,21 +416,29 @@ cudaError_t launch_requant_rows(const float* hbuf, float* row_amax, const int32_
                   n_rows, I, i_pad, h_codes, h_gs);
 }
 
-cudaError_t launch_finalize_atomic(const float* out_acc, void* out, int T, int H, cudaStream_t s) {
+cudaError_t launch_finalize_atomic(const float* out_acc, const uint16_t* shared, float shared_scale, void* out, int T,
+                                   int H, cudaStream_t s) {
   const size_t n8 = (size_t)T * H / 8;
-  return launch_k(finalize_atomic_kernel, dim3(grid_for(n8, 256 * 4)), dim3(256), 0, s, true, out_acc,
-                  reinterpret_cast<__nv_bfloat16*>(out), n8);
+  // after the join of the shared expert's stream: plain stream order
+  return launch_k(finalize_atomic_kernel, dim3(grid_for(n8, 256 * 4)), dim3(256), 0, s, !shared, out_acc, shared,
+                  shared_scale, reinterpret_cast<__nv_bfloat16*>(out), n8);
 }
 
-cudaError_t launch_finalize_ordered(const uint16_t* ybuf, const float* topk_w, void* out, int T, int H, int K,
-                                    cudaStream_t s) {
+cudaError_t launch_finalize_ordered(const uint16_t* ybuf, const float* topk_w, const uint16_t* shared,
+                                    float shared_scale, void* out, int T, int H, int K, cudaStream_t s) {
   if (K > FIN_MAX_K || H % 8) return cudaErrorInvalidValue;
-  // one token row per CTA and pass
+  // one token row per CTA and pass; plain stream order after a shared join
   if (K <= 8)
-    return launch_k(finalize_ordered_kernel<8>, dim3(std::min(T, 152 * 8)), dim3(256), 0, s, true, ybuf, topk_w,
-                    reinterpret_cast<__nv_bfloat16*>(out), T, H, K);
-  return launch_k(finalize_ordered_kernel<FIN_MAX_K>, dim3(std::min(T, 152 * 8)), dim3(256), 0, s, true, ybuf,
-                  topk_w, reinterpret_cast<__nv_bfloat16*>(out), T, H, K);
+    return launch_k(finalize_ordered_kernel<8>, dim3(std::min(T, 152 * 8)), dim3(256), 0, s, !shared, ybuf, topk_w,
+                    shared, shared_scale, reinterpret_cast<__nv_bfloat16*>(out), T, H, K);
+  return launch_k(finalize_ordered_kernel<FIN_MAX_K>, dim3(std::min(T, 152 * 8)), dim3(256), 0, s, !shared, ybuf,
+                  topk_w, shared, shared_scale, reinterpret_cast<__nv_bfloat16*>(out), T, H, K);
+}
+
+cudaError_t launch_shared_tiles(int T, int4* tiles, int32_t* num_tiles, cudaStream_t s) {
+  if (T <= 0) return cudaErrorInvalidValue;
+  // first kernel of the shared stream after the fork: ordinary stream order
+  return launch_k(shared_tiles_kernel, dim3(1), dim3(128), 0, s, false, T, tiles, num_tiles);
 }
 
 }  // namespace moe

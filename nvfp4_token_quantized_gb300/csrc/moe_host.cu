@@ -53,6 +53,21 @@ struct moe_handle {
   int4* tiles = nullptr;
   int32_t* num_tiles = nullptr;
   uint32_t* front_sync = nullptr;  // completion counters of the small-batch front kernel
+  // Shared expert (Is > 0): its NVFP4 weights, the token-ordered activation
+  // and intermediate operands (row t = token t, 128-row tiles), the
+  // identity row map, its tile list, its bf16 output rows, and the second
+  // stream with the fork / join events.
+  int Is = 0, Ipad_s = 0, Tpad_s = 0;
+  bool shared_loaded = false;
+  uint8_t *sw13_codes = nullptr, *sw2_codes = nullptr, *s_a_codes = nullptr, *s_h_codes = nullptr;
+  float *gs_sw13 = nullptr, *gs_sw2 = nullptr, *s_gs_rows = nullptr, *s_h_gs = nullptr;
+  uint32_t* s_amax_bits = nullptr;
+  int32_t *s_ident = nullptr, *s_num_tiles = nullptr;
+  int4* s_tiles = nullptr;
+  uint16_t* s_ybuf = nullptr;
+  int s_clusters[2] = {0, 0};
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   float* static_x_gs = nullptr;    // static contract: the w13 input's calibrated scale [1]
   float* static_h_gs = nullptr;    // static contract: the w2 input's calibrated scale per expert [E]
   float* hbuf = nullptr;           // small batches: FP32 SwiGLU rows [E*128][Ipad]
@@ -236,12 +251,67 @@ cudaError_t mark(moe_handle* h, int i, cudaStream_t s) {
   return cudaEventRecord(h->events[i], s);
 }
 
+// The shared expert on the handle's second stream, forked from `s`: x
+// quantized per token into token-ordered rows (the same arithmetic as the
+// routed experts' input), the w13 GEMM with the fused SwiGLU and
+// requantization epilogue on clusters of Is/128 CTAs, the w2 GEMM storing
+// bf16 rows; the join event is recorded at the end ("SM10X Command-A-Plus
+// decode 2.3x faster, BCG capture memory -78%", key source listing: the
+// shared experts on the 'alt' stream while gate, top-k and the routed
+// experts stay on the main stream).
+moe_status shared_branch(moe_handle* h, const void* x, int T, cudaStream_t s) {
+  const int H = h->H;
+  const int ntiles = (T + 127) / 128;
+  const int a_rows = T <= SMALL_BATCH_TOKENS ? 64 : 128;
+  CK(h, cudaEventRecord(h->ev_fork, s));
+  CK(h, cudaStreamWaitEvent(h->side, h->ev_fork, 0));
+  CK(h, launch_shared_tiles(T, h->s_tiles, h->s_num_tiles, h->side));
+  CK(h, launch_act_quant(x, T, H, 1, h->s_ident, h->s_a_codes, h->s_a_codes, h->s_gs_rows, nullptr, h->side));
+  GemmArgs g{};
+  g.status = h->status_dev;
+  g.tiles = h->s_tiles;
+  g.num_tiles = h->s_num_tiles;
+  g.a_codes = h->s_a_codes;
+  g.b_codes = h->sw13_codes;
+  g.k_stages = H / STAGE_K;
+  g.b_rows_per_expert = 2 * h->Is;
+  g.gs_rows = h->s_gs_rows;
+  g.gs_w = h->gs_sw13;
+  g.h_codes = h->s_h_codes;
+  g.h_sf = h->s_h_codes;
+  g.h_gs = h->s_h_gs;
+  g.i_pad = h->Ipad_s;
+  g.src_of_padrow = h->s_ident;  // row t is token t
+  g.num_experts = 1;
+  CK(h, launch_gemm_w13(g, h->Is / 128, std::min(h->s_clusters[a_rows == 128], ntiles), a_rows, h->side));
+  GemmArgs g2{};
+  g2.status = h->status_dev;
+  g2.tiles = h->s_tiles;
+  g2.num_tiles = h->s_num_tiles;
+  g2.a_codes = h->s_h_codes;
+  g2.b_codes = h->sw2_codes;
+  g2.k_stages = h->Ipad_s / STAGE_K;
+  g2.b_rows_per_expert = H;
+  g2.gs_rows = h->s_h_gs;
+  g2.gs_w = h->gs_sw2;
+  g2.src_of_padrow = h->s_ident;
+  g2.top_k = 1;
+  g2.ybuf = h->s_ybuf;  // (ordered epilogue: row t of the shared output)
+  g2.hidden = H;
+  g2.n_tiles = H / TILE_N;
+  g2.num_experts = 1;
+  CK(h, launch_gemm_w2(g2, std::min(h->num_sms, ntiles * g2.n_tiles / 2), true, a_rows, h->side));
+  CK(h, cudaEventRecord(h->ev_join, h->side));
+  return MOE_OK;
+}
+
 moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const float* bias, void* out, int T,
                         cudaStream_t s) {
   const int H = h->H, E = h->E, K = h->K;
   if (T > 0) {
     const int tile_rows = tile_rows_for(T);
     const bool small = T <= SMALL_BATCH_TOKENS;
+    if (h->Is > 0) TRY(shared_branch(h, x, T, s));
     // Above the small-batch size the FP32 atomic reduction of R x H partial
     // rows saturates L2; the ordered finalize (bf16 rows, fixed slot order)
     // moves half the bytes with plain stores and is deterministic as well.
@@ -350,8 +420,16 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
     // units are pairs of 128-column tiles
     CK(h, launch_gemm_w2(g2, std::min(h->num_sms, tb * g2.n_tiles / 2), ordered, tile_rows, s));
     CK(h, mark(h, 6, s));
-    if (ordered) CK(h, launch_finalize_ordered(h->ybuf, h->topk_w, out, T, H, K, s));
-    else CK(h, launch_finalize_atomic(h->out_acc, out, T, H, s));
+    // the shared expert's rows join here (its stream's work is done)
+    const uint16_t* shared = nullptr;
+    float shared_scale = 1.0f;
+    if (h->Is > 0) {
+      CK(h, cudaStreamWaitEvent(s, h->ev_join, 0));
+      shared = h->s_ybuf;
+      shared_scale = (h->cfg.flags & MOE_FLAG_SHARED_AVERAGE) ? 0.5f : 1.0f;
+    }
+    if (ordered) CK(h, launch_finalize_ordered(h->ybuf, h->topk_w, shared, shared_scale, out, T, H, K, s));
+    else CK(h, launch_finalize_atomic(h->out_acc, shared, shared_scale, out, T, H, s));
     CK(h, mark(h, 7, s));
   }
   h->last_T = T;
@@ -385,6 +463,9 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
   const int H = cfg->hidden, I = cfg->inter, E = cfg->num_experts, K = cfg->top_k, T = cfg->max_num_tokens;
   if (H <= 0 || I <= 0 || E <= 0 || K <= 0 || T <= 0) return MOE_ERR_INVALID_ARG;
   if (H % 256 || I % 128 || E % 8 || E > 256 || K > E || K > 16 || I / 128 > 16) return MOE_ERR_UNSUPPORTED;
+  const int Is = cfg->shared_inter;
+  if (Is < 0 || Is % 128 || Is / 128 > 16) return MOE_ERR_UNSUPPORTED;
+  if (Is > 0 && (cfg->flags & MOE_FLAG_STATIC_ACT_SCALES)) return MOE_ERR_UNSUPPORTED;
   if ((long)T * K > (1L << 30)) return MOE_ERR_UNSUPPORTED;
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess || cfg->device < 0 || cfg->device >= ndev) {
@@ -446,6 +527,32 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
   A(h->tiles, sizeof(int4) * (size_t)h->tile_cap);
   A(h->num_tiles, sizeof(int32_t) * 4);
   A(h->front_sync, sizeof(uint32_t) * FRONT_SYNC_WORDS);
+  if (Is > 0) {
+    h->Is = Is;
+    h->Ipad_s = (Is + 255) / 256 * 256;
+    h->Tpad_s = (T + 127) / 128 * 128;
+    const size_t Ts = h->Tpad_s;
+    A(h->sw13_codes, operand_bytes((size_t)2 * Is, H / 2));
+    A(h->sw2_codes, operand_bytes((size_t)H, h->Ipad_s / 2));
+    A(h->gs_sw13, sizeof(float));
+    A(h->gs_sw2, sizeof(float));
+    A(h->s_amax_bits, sizeof(uint32_t) * 2);
+    A(h->s_a_codes, operand_bytes(Ts, H / 2));
+    A(h->s_gs_rows, sizeof(float) * Ts);
+    A(h->s_h_codes, operand_bytes(Ts, h->Ipad_s / 2));
+    A(h->s_h_gs, sizeof(float) * Ts);
+    A(h->s_ident, sizeof(int32_t) * Ts);
+    A(h->s_tiles, sizeof(int4) * (Ts / 128));
+    A(h->s_num_tiles, sizeof(int32_t));
+    A(h->s_ybuf, sizeof(uint16_t) * (size_t)T * H);
+    std::vector<int32_t> ident(Ts);
+    for (size_t i = 0; i < Ts; ++i) ident[i] = (int32_t)i;
+    cudaError_t e = cudaMemcpy(h->s_ident, ident.data(), sizeof(int32_t) * Ts, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming);
+    if (e != cudaSuccess) return fail(cuda_fail(h, e, "shared-expert set-up"));
+  }
   // small batches: FP32 SwiGLU rows and row maxima of the expert blocks
   A(h->hbuf, sizeof(float) * (size_t)E * 128 * h->Ipad);
   A(h->row_amax, sizeof(float) * (size_t)E * 128);
@@ -478,6 +585,16 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
     h->num_sms = prop.multiProcessorCount;
     h->w13_clusters[0] = gemm_w13_max_clusters(I / 128, 64);
     h->w13_clusters[1] = gemm_w13_max_clusters(I / 128, 128);
+    if (h->Is > 0) {
+      e = gemm_setup_attributes(h->Is / 128);
+      if (e != cudaSuccess) return fail(cuda_fail(h, e, "cudaFuncSetAttribute(shared)"));
+      h->s_clusters[0] = gemm_w13_max_clusters(h->Is / 128, 64);
+      h->s_clusters[1] = gemm_w13_max_clusters(h->Is / 128, 128);
+      if (h->s_clusters[0] <= 0 || h->s_clusters[1] <= 0) {
+        set_err(h, "no thread-block cluster of %d CTAs fits on the device", h->Is / 128);
+        return fail(MOE_ERR_UNSUPPORTED);
+      }
+    }
     if (h->w13_clusters[0] <= 0 || h->w13_clusters[1] <= 0) {
       set_err(h, "no thread-block cluster of %d CTAs fits on the device", I / 128);
       return fail(MOE_ERR_UNSUPPORTED);
@@ -513,8 +630,36 @@ moe_status moe_destroy(moe_handle* h) {
   if (h->status_host) cudaFreeHost(h->status_host);
   for (cudaEvent_t ev : h->events)
     if (ev) cudaEventDestroy(ev);
+  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+  if (h->ev_join) cudaEventDestroy(h->ev_join);
+  if (h->side) cudaStreamDestroy(h->side);
   cudaGetLastError();
   delete h;
+  return MOE_OK;
+}
+
+moe_status moe_load_shared_weights(moe_handle* h, const void* w13s, const moe_weight_desc* w13s_desc,
+                                   const void* w2s, const moe_weight_desc* w2s_desc, void* stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  if (h->Is <= 0) {
+    set_err(h, "the handle was created without a shared expert (shared_inter = 0)");
+    return MOE_ERR_INVALID_ARG;
+  }
+  DeviceGuard dg(h->cfg.device);
+  TRY(check_weight_desc(h, w13s_desc, w13s, 1, 2 * h->Is, h->H, "w13s"));
+  TRY(check_weight_desc(h, w2s_desc, w2s, 1, h->H, h->Is, "w2s"));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // one expert: the routed experts' conversion (gate / up rows interleaved
+  // in chunks of 64 for the w13 epilogue), into the same buffers every time
+  CK(h, cudaMemsetAsync(h->s_amax_bits, 0, sizeof(uint32_t) * 2, s));
+  CK(h, launch_weight_amax(w13s, 1, 2 * h->Is, h->H, h->s_amax_bits, s));
+  CK(h, launch_weight_amax(w2s, 1, h->H, h->Is, h->s_amax_bits + 1, s));
+  CK(h, launch_weight_quant(w13s, 1, 2 * h->Is, h->H, h->H, 1, h->s_amax_bits, h->sw13_codes, h->sw13_codes,
+                            h->gs_sw13, s));
+  CK(h, launch_weight_quant(w2s, 1, h->H, h->Is, h->Ipad_s, 0, h->s_amax_bits + 1, h->sw2_codes, h->sw2_codes,
+                            h->gs_sw2, s));
+  h->shared_loaded = true;
+  h->err.clear();
   return MOE_OK;
 }
 
@@ -564,6 +709,10 @@ moe_status moe_forward_ex(moe_handle* h, const void* x, const void* gate_w, cons
   }
   if (h->static_scales && !h->static_set) {
     set_err(h, "static activation scales: moe_set_static_scales has not been called");
+    return MOE_ERR_NOT_LOADED;
+  }
+  if (h->Is > 0 && !h->shared_loaded) {
+    set_err(h, "shared expert: moe_load_shared_weights has not been called");
     return MOE_ERR_NOT_LOADED;
   }
   if (num_tokens < 0) {
@@ -736,6 +885,26 @@ moe_status moe_debug_intermediate(moe_handle* h, uint8_t* h_codes, uint8_t* h_sf
   if (h->last_T == 0) return MOE_OK;
   CK(h, launch_export_rows(h->h_codes, h->h_sf, h->h_gs, h->last_T * h->K, h->I, h->Ipad, h->pad_row_of_src, 1, 0,
                            0, 0, h_codes, h_sf, h_gs, reinterpret_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+moe_status moe_debug_shared(moe_handle* h, uint16_t* rows, uint8_t* h_codes, uint8_t* h_sf, float* h_gs,
+                            void* stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  if (h->Is <= 0) {
+    set_err(h, "the handle was created without a shared expert (shared_inter = 0)");
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (h->last_T < 0) return MOE_ERR_NOT_LOADED;
+  if (!h_codes != !h_sf || !h_codes != !h_gs) return MOE_ERR_INVALID_ARG;
+  DeviceGuard dg(h->cfg.device);
+  const int T = h->last_T;
+  if (T == 0) return MOE_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (rows) CK(h, cudaMemcpyAsync(rows, h->s_ybuf, sizeof(uint16_t) * (size_t)T * h->H, cudaMemcpyDeviceToDevice, s));
+  if (h_codes && h_sf && h_gs)
+    CK(h, launch_export_rows(h->s_h_codes, h->s_h_codes, h->s_h_gs, T, h->Is, h->Ipad_s, h->s_ident, 1, 0, 0, 0,
+                             h_codes, h_sf, h_gs, s));
   return MOE_OK;
 }
 

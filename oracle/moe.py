@@ -226,12 +226,19 @@ def expert_rows(a_codes, a_sf, a_gs, w13: QuantWeights, w2: QuantWeights, e: int
         h_codes, h_sf, h_gs = nvfp4.quantize_rows(h)
     else:
         h_codes, h_sf, h_gs = nvfp4.quantize_rows_static(h, h_gs_static)
+    y2 = expert_w2(h_codes, h_sf, h_gs, w2, e)
+    return dict(y1=y1, h=h, h_codes=h_codes, h_sf=h_sf, h_gs=h_gs, y2=y2)
+
+
+def expert_w2(h_codes, h_sf, h_gs, w2: QuantWeights, e: int) -> np.ndarray:
+    """The second GEMM of expert ``e`` on quantized intermediate rows (codes
+    [n, I], block scales [n, I/16], global scales [n]): the FP32 output
+    [n, H], from FP64 sums over the exactly decoded operands."""
     A2 = nvfp4.decode_scaled(h_codes, h_sf)                      # [n, I]
     B2 = nvfp4.decode_scaled(w2.codes[e], w2.sf[e])              # [H, I]
     acc2 = A2 @ B2.T
-    scale2 = 1.0 / (h_gs.astype(np.float64)[:, None] * np.float64(w2.gs[e]))
-    y2 = (acc2 * scale2).astype(np.float32)
-    return dict(y1=y1, h=h, h_codes=h_codes, h_sf=h_sf, h_gs=h_gs, y2=y2)
+    scale2 = 1.0 / (np.asarray(h_gs, np.float64)[:, None] * np.float64(w2.gs[e]))
+    return (acc2 * scale2).astype(np.float32)
 
 
 def finalize(y_rows: np.ndarray, weights: np.ndarray) -> np.ndarray:

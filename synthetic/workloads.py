@@ -20,6 +20,7 @@ import torch
 
 # One generator stream per tensor kind.
 _TAG_X, _TAG_GATE, _TAG_W13, _TAG_W2, _TAG_BIAS, _TAG_ROWS = 1, 2, 3, 4, 5, 6
+_TAG_SW13, _TAG_SW2 = 7, 8
 
 
 def _gen(seed: int, tag: int) -> torch.Generator:
@@ -135,6 +136,15 @@ def make_weights(shape: MoEShape, seed: int = 0) -> Tuple[torch.Tensor, torch.Te
         w13[e] = (torch.randn(2 * I, H, generator=g13, dtype=torch.float32) * 0.02).to(torch.bfloat16)
         w2[e] = (torch.randn(H, I, generator=g2, dtype=torch.float32) * 0.02).to(torch.bfloat16)
     return w13, w2
+
+
+def make_shared_weights(shape: MoEShape, shared_inter: int, seed: int = 0) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Shared-expert weights w13s bf16 [2*Is, H] (gate rows, then up rows) and
+    w2s bf16 [H, Is], N(0, 0.02), from streams of their own."""
+    H, Is = shape.H, shared_inter
+    w13s = (torch.randn(2 * Is, H, generator=_gen(seed, _TAG_SW13), dtype=torch.float32) * 0.02).to(torch.bfloat16)
+    w2s = (torch.randn(H, Is, generator=_gen(seed, _TAG_SW2), dtype=torch.float32) * 0.02).to(torch.bfloat16)
+    return w13s, w2s
 
 
 @dataclasses.dataclass

@@ -61,6 +61,12 @@ def test_argument_checks_without_gpu(lib):
     assert not h.value
     neg = moe_config(2048, 768, 128, 8, 0, 0, 0)                         # no tokens
     assert lib.moe_create(ctypes.byref(neg), ctypes.byref(h)) == 1
+    odd_shared = moe_config(2048, 768, 128, 8, 64, 0, 0, 100)            # Is not a multiple of 128
+    assert lib.moe_create(ctypes.byref(odd_shared), ctypes.byref(h)) == 8
+    static_shared = moe_config(2048, 768, 128, 8, 64, 0, 2, 256)         # shared expert with static scales
+    assert lib.moe_create(ctypes.byref(static_shared), ctypes.byref(h)) == 8
+    assert not h.value
+    assert lib.moe_load_shared_weights(None, None, None, None, None, None) == 1
     assert lib.moe_forward(None, None, None, None, 4, None) == 1
     assert lib.moe_destroy(None) == 0
     assert lib.moe_get_workspace_bytes(None) == 0
