@@ -40,8 +40,10 @@ def kernels_per_forward(s, T, shared_inter=0):
     """Kernel launches of one forward: router, top-k, permute, quantize, w13,
     w2, finalize.  Up to 64 tokens: one fused front end, w13, the row
     requantization, w2, finalize (the bench runs per-token scales).  A shared
-    expert adds four on its own stream: tile list, quantize, w13, w2."""
-    return (7 if T > SMALL_BATCH_TOKENS else 5) + (4 if shared_inter else 0)
+    expert adds its own stream's tile list, quantize, w13, w2, and up to 64
+    tokens the row requantization between them."""
+    shared = (5 if T <= SMALL_BATCH_TOKENS else 4) if shared_inter else 0
+    return (7 if T > SMALL_BATCH_TOKENS else 5) + shared
 
 
 def ordered_finalize(s, T):

@@ -65,6 +65,7 @@ struct moe_handle {
   int32_t *s_ident = nullptr, *s_num_tiles = nullptr;
   int4* s_tiles = nullptr;
   uint16_t* s_ybuf = nullptr;
+  float *s_hbuf = nullptr, *s_row_amax = nullptr;  // small batches: FP32 SwiGLU rows [128][Ipad_s], row maxima
   int s_clusters[2] = {0, 0};
   cudaStream_t side = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
@@ -259,6 +260,10 @@ cudaError_t mark(moe_handle* h, int i, cudaStream_t s) {
 // decode 2.3x faster, BCG capture memory -78%", key source listing: the
 // shared experts on the 'alt' stream while gate, top-k and the routed
 // experts stay on the main stream).
+// CTAs of the shared expert's GEMMs up to 64 tokens: its w13 column pairs,
+// or its w2 column-tile pairs, whichever is more.
+int shared_gemm_ctas(const moe_handle* h) { return std::max(h->Is / 128, h->H / 256); }
+
 moe_status shared_branch(moe_handle* h, const void* x, int T, cudaStream_t s) {
   const int H = h->H;
   const int ntiles = (T + 127) / 128;
@@ -283,7 +288,19 @@ moe_status shared_branch(moe_handle* h, const void* x, int T, cudaStream_t s) {
   g.i_pad = h->Ipad_s;
   g.src_of_padrow = h->s_ident;  // row t is token t
   g.num_experts = 1;
-  CK(h, launch_gemm_w13(g, h->Is / 128, std::min(h->s_clusters[a_rows == 128], ntiles), a_rows, h->side));
+  if (T <= SMALL_BATCH_TOKENS) {
+    // one 64-row tile: column pairs spread over single CTAs (no cluster has
+    // to find SMs of one GPC free next to the routed GEMMs), then the row
+    // requantization
+    g.w13_pairs = h->Is / 128;
+    g.hbuf = h->s_hbuf;
+    g.row_amax = h->s_row_amax;
+    CK(h, launch_gemm_w13s(g, std::min(h->num_sms, g.w13_pairs), false, h->side));
+    CK(h, launch_requant_rows(h->s_hbuf, h->s_row_amax, h->s_ident, T, h->Is, h->Ipad_s, h->s_h_codes, h->s_h_gs,
+                              h->side));
+  } else {
+    CK(h, launch_gemm_w13(g, h->Is / 128, std::min(h->s_clusters[a_rows == 128], ntiles), a_rows, h->side));
+  }
   GemmArgs g2{};
   g2.status = h->status_dev;
   g2.tiles = h->s_tiles;
@@ -316,6 +333,11 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
     // rows saturates L2; the ordered finalize (bf16 rows, fixed slot order)
     // moves half the bytes with plain stores and is deterministic as well.
     const bool ordered = h->deterministic || !small;
+    // Up to 64 tokens the routed GEMMs are persistent with one CTA per SM
+    // and start early; with a shared expert they leave its GEMM CTAs SMs of
+    // their own so that the two streams overlap instead of queueing.
+    const int gemm_sms = (h->Is > 0 && small) ? std::max(h->num_sms / 2, h->num_sms - shared_gemm_ctas(h))
+                                              : h->num_sms;
     CK(h, mark(h, 0, s));
     if (small) {
       // one kernel for router, quantization, top-k and grouping; its time is
@@ -388,7 +410,7 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
       g.w13_pairs = h->I / 128;
       g.hbuf = h->hbuf;
       g.row_amax = h->row_amax;
-      CK(h, launch_gemm_w13s(g, std::min(h->num_sms, tb * g.w13_pairs), false, s));
+      CK(h, launch_gemm_w13s(g, std::min(gemm_sms, tb * g.w13_pairs), false, s));
       // (with static scales the w13 epilogue has already requantized)
       if (!h->static_scales)
         CK(h, launch_requant_rows(h->hbuf, h->row_amax, h->pad_row_of_src, T * K, h->I, h->Ipad, h->h_codes, h->h_gs,
@@ -418,7 +440,7 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
     g2.num_experts = E;
     g2.prefetch_units = small ? W2_PREFETCH_UNITS : 0;
     // units are pairs of 128-column tiles
-    CK(h, launch_gemm_w2(g2, std::min(h->num_sms, tb * g2.n_tiles / 2), ordered, tile_rows, s));
+    CK(h, launch_gemm_w2(g2, std::min(gemm_sms, tb * g2.n_tiles / 2), ordered, tile_rows, s));
     CK(h, mark(h, 6, s));
     // the shared expert's rows join here (its stream's work is done)
     const uint16_t* shared = nullptr;
@@ -545,6 +567,8 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
     A(h->s_tiles, sizeof(int4) * (Ts / 128));
     A(h->s_num_tiles, sizeof(int32_t));
     A(h->s_ybuf, sizeof(uint16_t) * (size_t)T * H);
+    A(h->s_hbuf, sizeof(float) * 128 * (size_t)h->Ipad_s);
+    A(h->s_row_amax, sizeof(float) * 128);
     std::vector<int32_t> ident(Ts);
     for (size_t i = 0; i < Ts; ++i) ident[i] = (int32_t)i;
     cudaError_t e = cudaMemcpy(h->s_ident, ident.data(), sizeof(int32_t) * Ts, cudaMemcpyHostToDevice);
