@@ -246,39 +246,61 @@ __device__ __forceinline__ bool topk_before(float av, int ae, float bv, int be) 
   return av > bv || (av == bv && ae < be);
 }
 
-// Top-k of one token's logits by one warp: K rounds of a warp argmax over
-// the remaining candidates (lane holds experts lane, lane + 32, ...; E <= 256)
-// by (logit desc, expert asc); softmax over all E experts (lane sums in
-// ascending order, then the xor tree), chosen probabilities renormalised in
-// slot order.  The round loop is kept rolled: its body stays in the
-// instruction cache (fully unrolled, the selection ran from cold instruction
-// fetches).  Lane j < K returns slot j: its expert in e_lane and its weight in
-// w_lane.  Logits are read through L2 (another CTA of the same grid may have
-// written them).  All 32 lanes must call it.
-__device__ __forceinline__ void topk_warp(const float* __restrict__ lrow, int E, int K, int lane, int& e_lane,
-                                          float& w_lane) {
-  constexpr int NE = 8;
-  float l[NE], cand[NE];
+// Compare-exchange of two candidates: the one first in topk_before order
+// ends up in slot a.
+__device__ __forceinline__ void topk_cas(float& va, int& ea, float& vb, int& eb) {
+  if (topk_before(vb, eb, va, ea)) {
+    const float tv = va;
+    const int te = ea;
+    va = vb;
+    ea = eb;
+    vb = tv;
+    eb = te;
+  }
+}
+
+// Top-k of one token's logits by one warp.  Lane l holds the NE candidates
+// l, l + 32, ... (E <= 32 NE) and sorts them by (logit desc, expert asc), a
+// total order since expert ids are unique; each of the K rounds takes the
+// best lane head over the warp (a butterfly argmax in the same order) and
+// the lane that held it moves on to its next candidate.  Softmax over all E
+// experts (each lane sums its raw logits in ascending expert order, then the
+// xor tree), chosen probabilities renormalised in slot order.  Lane j < K
+// returns slot j: its expert in e_lane and its weight in w_lane.  Logits are
+// read through L2 (another CTA of the same grid may have written them).  All
+// 32 lanes must call it.
+template <int NE>
+__device__ __forceinline__ void topk_warp_n(const float* __restrict__ lrow, int E, int K, int lane, int& e_lane,
+                                            float& w_lane) {
+  float raw[NE], v[NE];
+  int id[NE];
 #pragma unroll
   for (int i = 0; i < NE; ++i) {
     const int e = lane + 32 * i;
-    l[i] = e < E ? __ldcg(lrow + e) : -INFINITY;
-    cand[i] = l[i];
+    raw[i] = e < E ? __ldcg(lrow + e) : -INFINITY;
+    v[i] = raw[i];
+    id[i] = e < E ? e : 0x7fffffff;  // padding sorts last
   }
-  float l_lane = -INFINITY;
+  // sorting network: 5 exchanges for 4 candidates, 19 for 8
+  if constexpr (NE == 4) {
+    topk_cas(v[0], id[0], v[1], id[1]);
+    topk_cas(v[2], id[2], v[3], id[3]);
+    topk_cas(v[0], id[0], v[2], id[2]);
+    topk_cas(v[1], id[1], v[3], id[3]);
+    topk_cas(v[1], id[1], v[2], id[2]);
+  } else {
+    static_assert(NE == 8, "4 or 8 candidates per lane");
+    constexpr int net[19][2] = {{0, 2}, {1, 3}, {4, 6}, {5, 7}, {0, 4}, {1, 5}, {2, 6}, {3, 7}, {0, 1}, {2, 3},
+                                {4, 5}, {6, 7}, {2, 4}, {3, 5}, {1, 4}, {3, 6}, {1, 2}, {3, 4}, {5, 6}};
+#pragma unroll
+    for (int c = 0; c < 19; ++c) topk_cas(v[net[c][0]], id[net[c][0]], v[net[c][1]], id[net[c][1]]);
+  }
+  float l_lane = -INFINITY, m = 0.0f, s = 0.0f;
   e_lane = 0;
 #pragma unroll 1
   for (int j = 0; j < K; ++j) {
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < NE; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && topk_before(cand[i], e, bv, be)) {
-        bv = cand[i];
-        be = e;
-      }
-    }
+    float bv = v[0];
+    int be = id[0];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
@@ -288,27 +310,40 @@ __device__ __forceinline__ void topk_warp(const float* __restrict__ lrow, int E,
         be = oe;
       }
     }
+    if (j == 0) {
+      // the maximum logit: the softmax denominator over all experts
+      m = bv;
+#pragma unroll
+      for (int i = 0; i < NE; ++i)
+        if (lane + 32 * i < E) s += expf(raw[i] - m);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    }
     if (lane == j) {
       l_lane = bv;
       e_lane = be;
     }
+    if (id[0] == be) {  // this lane's head was taken
 #pragma unroll
-    for (int i = 0; i < NE; ++i)
-      if (lane + 32 * i == be) cand[i] = -INFINITY;
+      for (int i = 0; i + 1 < NE; ++i) {
+        v[i] = v[i + 1];
+        id[i] = id[i + 1];
+      }
+      v[NE - 1] = -INFINITY;
+      id[NE - 1] = 0x7fffffff;
+    }
   }
-  // softmax over all experts, then renormalise the chosen probabilities
-  const float m = __shfl_sync(0xffffffffu, l_lane, 0);
-  float s = 0.0f;
-#pragma unroll
-  for (int i = 0; i < NE; ++i)
-    if (lane + 32 * i < E) s += expf(l[i] - m);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   const float pj = lane < K ? expf(l_lane - m) / s : 0.0f;
   float psum = 0.0f;
 #pragma unroll 1
   for (int j = 0; j < K; ++j) psum += __shfl_sync(0xffffffffu, pj, j);
   w_lane = pj / psum;
+}
+
+__device__ __forceinline__ void topk_warp(const float* __restrict__ lrow, int E, int K, int lane, int& e_lane,
+                                          float& w_lane) {
+  if (E <= 128) topk_warp_n<4>(lrow, E, K, lane, e_lane, w_lane);
+  else topk_warp_n<8>(lrow, E, K, lane, e_lane, w_lane);
 }
 
 // One warp per token: the top-k choice and weights, and the per-expert row

@@ -121,3 +121,28 @@ def test_zero_tokens_give_zero_rows_on_gpu():
     assert torch.count_nonzero(o[2]) == 0 and torch.count_nonzero(o[11]) == 0
     assert torch.count_nonzero(o[0]) > 0
     layer.close()
+
+
+@pytest.mark.parametrize("E,K,T", [(16, 4, 16), (16, 4, 100), (256, 12, 24), (256, 12, 100), (136, 8, 70)])
+def test_tied_logits_take_the_lower_expert(E, K, T):
+    """Router columns duplicated in pairs give every token's logits in exact
+    pairs (the canonical FP32 order computes both the same way), so the top-k
+    meets a tie at every step: the lower expert id must come first, as in the
+    oracle.  Covers both per-lane candidate counts of the warp top-k (E <= 128
+    and above) on the fused small-batch front end and on the top-k kernel."""
+    shape = synthetic.MoEShape(name="ties", T=T, H=256, E=E, K=K, I=128, max_num_tokens=128)
+    wl = synthetic.make_workload(shape, T=T, seed=11)
+    gate = wl.gate_w.clone()
+    gate[:, 1::2] = gate[:, 0::2]
+    layer = _layer(shape)
+    layer.load_weights(wl.w13.cuda(), wl.w2.cuda())
+    layer.forward(wl.x.cuda(), gate.cuda())
+    torch.cuda.synchronize()
+    logits = omoe.router_logits(omoe.as_f32(wl.x), omoe.as_f32(gate))
+    assert np.array_equal(logits[:, 0::2], logits[:, 1::2])
+    ids, weights = omoe.topk_route(logits, K)
+    r = layer.debug_routing()
+    got = r["topk_ids"].cpu().numpy()
+    assert np.array_equal(got, ids), "tie order differs from the oracle"
+    np.testing.assert_allclose(r["topk_w"].cpu().numpy(), weights, rtol=1e-5, atol=1e-7)
+    layer.close()
