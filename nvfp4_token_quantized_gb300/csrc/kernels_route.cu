@@ -429,21 +429,41 @@ __global__ void __launch_bounds__(PERM_THREADS) permute_kernel(const int32_t* __
   const int tbase = block_sum_int(n_lt, red);
   const int cnt = counts[e];
 
+  // Pass over PERM_THREADS * PERM_TPT tokens: warp w takes the block's
+  // tokens [w * 32 * PERM_TPT, +32 * PERM_TPT), lane l the tokens l, l + 32,
+  // ... of them, so one load instruction covers 32 consecutive token rows.
+  // A row's rank among the expert's rows (token order) is: the rows of the
+  // earlier passes (carry), of the earlier warps (a scan over the warps'
+  // counts), of the warp's earlier 32-token groups, and of the lower lanes
+  // of its own group (ballots).
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned lanes_below = (1u << lane) - 1u;
   int carry = 0;
   for (int base = 0; base < T; base += PERM_THREADS * PERM_TPT) {
-    const int tb = base + threadIdx.x * PERM_TPT;
+    const int wbase = base + warp * 32 * PERM_TPT;
     int slot[PERM_TPT];
-    int n = 0;
+    unsigned bal[PERM_TPT];
+    int wcount = 0;
 #pragma unroll
     for (int i = 0; i < PERM_TPT; ++i) {
       slot[i] = -1;
-      const int t = tb + i;
+      const int t = wbase + 32 * i + lane;
       if (t < T) {
-        // the token's K <= 16 ids into registers first (8-byte loads when K
-        // is even), then the comparisons: all loads are in flight together
+        // the token's K <= 16 ids into registers first (16- or 8-byte loads
+        // when K allows), then the comparisons
         int id[16];
         const int32_t* row = topk_ids + (size_t)t * K;
-        if ((K & 1) == 0) {
+        if ((K & 3) == 0) {
+#pragma unroll
+          for (int j = 0; j < 16; j += 4)
+            if (j < K) {
+              const int4 v = __ldg(reinterpret_cast<const int4*>(row + j));
+              id[j] = v.x;
+              id[j + 1] = v.y;
+              id[j + 2] = v.z;
+              id[j + 3] = v.w;
+            }
+        } else if ((K & 1) == 0) {
 #pragma unroll
           for (int j = 0; j < 16; j += 2)
             if (j < K) {
@@ -460,22 +480,34 @@ __global__ void __launch_bounds__(PERM_THREADS) permute_kernel(const int32_t* __
         for (int j = 0; j < 16; ++j)
           if (j < K && id[j] == e) slot[i] = j;
       }
-      n += slot[i] >= 0;
+      bal[i] = __ballot_sync(0xffffffffu, slot[i] >= 0);
+      wcount += __popc(bal[i]);
     }
-    int tot;
-    int pos = carry + block_excl_scan(n, red, &tot);
+    // exclusive scan of the warps' counts
+    __syncthreads();  // red[] is free again (previous pass or block sums)
+    if (lane == 0) red[warp] = wcount;
+    __syncthreads();
+    int wpre = 0, tot = 0;
+    for (int w = 0; w < PERM_THREADS / 32; ++w) {
+      const int c = red[w];
+      wpre += w < warp ? c : 0;
+      tot += c;
+    }
+    int pos = carry + wpre;
 #pragma unroll
     for (int i = 0; i < PERM_TPT; ++i) {
       if (slot[i] >= 0) {
-        const int src = (tb + i) * K + slot[i];
-        const int r = off + pos;
-        const int pr = poff + (pos >> tile_shift) * 128 + (pos & (tile_rows - 1));
+        const int t = wbase + 32 * i + lane;
+        const int src = t * K + slot[i];
+        const int rank = pos + __popc(bal[i] & lanes_below);
+        const int r = off + rank;
+        const int pr = poff + (rank >> tile_shift) * 128 + (rank & (tile_rows - 1));
         o.src_of_row[r] = src;
         o.row_of_src[src] = r;
         o.pad_row_of_src[src] = pr;
         o.src_of_padrow[pr] = src;
-        ++pos;
       }
+      pos += __popc(bal[i]);
     }
     carry += tot;
   }
