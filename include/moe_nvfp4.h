@@ -7,7 +7,12 @@
  *   router logits -> top-k -> expert permutation (expand) -> per-token NVFP4
  *   quantization -> block-scaled FP4 grouped GEMM on w13 with SwiGLU and
  *   per-row requantization in its epilogue -> block-scaled FP4 grouped GEMM on
- *   w2 with the top-k weighted reduction in its epilogue -> bf16 output.
+ *   w2 -> top-k weighted finalize -> bf16 output.  Up to 64 tokens the w2
+ *   epilogue adds the weighted rows into an FP32 accumulator; in
+ *   deterministic mode and above 64 tokens it stores one bf16 row per
+ *   (token, slot), summed in slot order by the finalize.  An optional shared
+ *   expert runs on a second stream forked from and joined back into the
+ *   caller's.
  *
  * Where each operation is defined (the pages' titles and sections):
  *   - "CuTe DSL backend gets per-token NVFP4 online quantization and reload",
@@ -23,7 +28,9 @@
  *   - "SM10X Command-A-Plus decode 2.3x faster, BCG capture memory -78%",
  *     Motivation and Implementation item 2: routing, expandInputRows,
  *     activation and finalize fused around the expert GEMMs; the routed
- *     output must not alias its input.
+ *     output must not alias its input.  Its code snippets (the Cohere2MoE
+ *     sparse block): shared experts on an alternate stream next to the
+ *     routed experts, outputs added, halved under the 'average' strategy.
  *
  * Numeric rules (the pages print no formula; these are the library's stated
  * readings):
