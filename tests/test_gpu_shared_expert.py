@@ -19,7 +19,8 @@ through the C ABI against the oracle with ``shared=(w13s, w2s)``:
 * deterministic mode gives the same bits on every run, and a CUDA graph
   capture of the forked forward replays to the eager output;
 * a handle with a shared expert refuses to run before its shared weights
-  are loaded.
+  are loaded;
+* the widest shapes (I = Is = 2048, top-16) above 64 tokens.
 """
 
 import numpy as np
@@ -172,3 +173,17 @@ def test_shared_weights_required():
     with pytest.raises(MoEError):
         plain.load_shared_weights(w13s.cuda(), w2s.cuda())
     plain.close()
+
+
+@pytest.mark.parametrize("T", [100])
+def test_maximum_widths(T):
+    """The widest supported layer shapes in one handle, above 64 tokens:
+    I = 2048 (w13 clusters of 16 CTAs exchanging row maxima), top-16 (the
+    wide finalize variant), and a 2048-wide shared expert (its own 16-CTA
+    clusters)."""
+    shape = synthetic.MoEShape(name="max_widths", T=T, H=256, E=32, K=16, I=2048, max_num_tokens=128)
+    layer, _, out, ref, routed, q2s, q13s = _run(shape, T, 2048, False)
+    r = layer.debug_routing()
+    assert np.array_equal(r["topk_ids"].cpu().numpy(), ref.ids)
+    _check(layer, out, ref, routed, q2s, q13s, False, f"maximum widths, T={T}")
+    layer.close()
