@@ -114,6 +114,17 @@ typedef enum {
  * capture memory -78%" (its key source listing). */
 #define MOE_FLAG_SHARED_AVERAGE 4u
 
+/* SwiGLU sigmoid form.  The pages do not fix how the activation between the
+ * expert GEMMs is evaluated.  By default the w13 epilogue forms
+ * sigmoid(g) = 1/2 + tanh(g/2)/2 with the hardware tanh approximation (one
+ * special-function operation per element, relative error about 2^-11);
+ * with this flag it forms sigmoid(g) = 1 / (1 + expf(-g)) with an IEEE
+ * division.  Either way the requantized intermediate is not a bit-exact
+ * target: its codes depend on FP32 accumulation in the tensor cores.  The
+ * accurate form moves fewer of its near-tie rounding decisions away from an
+ * FP64 evaluation. */
+#define MOE_FLAG_ACCURATE_SIGMOID 8u
+
 typedef struct {
   int hidden;          /* H: model width (K dim of w13, N dim of w2) */
   int inter;           /* I: expert intermediate width */
@@ -266,7 +277,11 @@ MOE_API const char* moe_stage_name(int i);
  * per-expert row counters live in one fixed array in the library's device
  * code: MOE_ROUTE_NOALLOC_MAX_LOGITS floats of logits plus 256 counters
  * (about 4 MiB per device, reserved when the library's device code is loaded
- * on that device).  Nothing is allocated by this call, by CUDA or otherwise.
+ * on that device).  After the first call on a device, nothing is allocated by
+ * a call, by CUDA or otherwise.  Under CUDA's default lazy module loading the
+ * device code (and with it the array) is loaded on a device by the first call
+ * there, so that first call reserves the 4 MiB: make it before a memory pool
+ * takes the device's free memory, as well as before any stream capture.
  *
  * Computes exactly the routing of moe_forward_ex on the same inputs (the same
  * kernels): FP32 router logits in the canonical order, plus gate_bias if not
@@ -289,9 +304,10 @@ MOE_API const char* moe_stage_name(int i);
  * batch); NULL or misaligned pointers MOE_ERR_INVALID_ARG; a device other
  * than sm_103 MOE_ERR_UNSUPPORTED; num_tokens == 0 does nothing.
  *
- * The first call on each device does that device's set-up (looks up the
- * array's device address and raises the router kernel's launch limits), so
- * make one call on each device before any stream capture.  The array is
+ * The first call on each device does that device's set-up (loads the device
+ * code there if it is not loaded yet, looks up the array's device address and
+ * raises the router kernel's launch limits), so make one call on each device
+ * before any stream capture and before a pool reserves its free memory.  The array is
  * shared by every call on the device: calls whose device work overlaps
  * (different streams, or threads without ordering between them) race on it
  * and corrupt each other's results; order them on one stream.
@@ -342,6 +358,13 @@ MOE_API moe_status moe_debug_intermediate(moe_handle* h, uint8_t* h_codes, uint8
  * shared expert, MOE_ERR_NOT_LOADED before the first forward. */
 MOE_API moe_status moe_debug_shared(moe_handle* h, uint16_t* rows, uint8_t* h_codes, uint8_t* h_sf, float* h_gs,
                                     void* stream);
+
+/* The shared expert's own per-token quantization of x in the last forward
+ * (its second stream quantizes the tokens into token-ordered rows, with the
+ * same per-token rules as the routed experts' input): codes uint8 [T, H/2],
+ * sf uint8 [T, H/16], gs f32 [T], device pointers, all three required.
+ * Errors as moe_debug_shared. */
+MOE_API moe_status moe_debug_shared_act_quant(moe_handle* h, uint8_t* codes, uint8_t* sf, float* gs, void* stream);
 
 /* Addresses of every device buffer the handle owns (weights, scales,
  * workspace), for checking that load/refresh never moves them.  On entry *n

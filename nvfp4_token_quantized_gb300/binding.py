@@ -28,6 +28,7 @@ MOE_ERR_UNSUPPORTED = 8
 MOE_FLAG_DETERMINISTIC = 1
 MOE_FLAG_STATIC_ACT_SCALES = 2
 MOE_FLAG_SHARED_AVERAGE = 4
+MOE_FLAG_ACCURATE_SIGMOID = 8
 MOE_DTYPE_BF16 = 1
 
 EXPORTED = (
@@ -37,7 +38,7 @@ EXPORTED = (
     "moe_debug_act_quant", "moe_debug_weight_quant", "moe_debug_intermediate", "moe_debug_buffer_ptrs",
     "moe_debug_convert", "moe_debug_block_scaled_gemm", "moe_set_stage_timing", "moe_get_stage_times",
     "moe_stage_name", "moe_route_noalloc", "moe_set_static_scales", "moe_load_shared_weights",
-    "moe_debug_shared",
+    "moe_debug_shared", "moe_debug_shared_act_quant",
 )
 MOE_ROUTE_NOALLOC_MAX_LOGITS = 1 << 20
 MOE_NUM_STAGES = 7
@@ -105,6 +106,7 @@ def load_library() -> ctypes.CDLL:
         "moe_route_noalloc": (I, [P, P, P, I, I, I, I, P, P, P]),
         "moe_set_static_scales": (I, [P, P, P, P]),
         "moe_debug_shared": (I, [P, P, P, P, P, P]),
+        "moe_debug_shared_act_quant": (I, [P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -252,14 +254,35 @@ def moe_route_noalloc(x: torch.Tensor, gate_w: torch.Tensor, top_k: int, bias: O
     """Routing (logits, top-k, renormalised weights) with no handle and no
     device allocation inside the library call.  ``topk_ids`` (int32 [T, K])
     and ``topk_w`` (float32 [T, K]) may be passed in to be filled; otherwise
-    they are created here, before the call.  The current CUDA device must be
-    the one holding the tensors."""
+    they are created here, before the call.  Every tensor must be contiguous
+    and on x's device, which must be the current CUDA device (the library
+    launches there); anything else raises before the library is called."""
+    if not isinstance(x, torch.Tensor) or x.dim() != 2:
+        raise ValueError("x must be a 2-D tensor [num_tokens, hidden]")
+    if x.device.type != "cuda":
+        raise ValueError("x must be a CUDA tensor")
+    dev = x.device.index
+    if dev != torch.cuda.current_device():
+        raise ValueError(f"x is on cuda:{dev} but the current device is cuda:{torch.cuda.current_device()}")
+    _check_dev(x, torch.bfloat16, "x", dev)
+    _check_dev(gate_w, torch.bfloat16, "gate_w", dev)
     T, H = x.shape
+    if gate_w.dim() != 2 or gate_w.shape[0] != H:
+        raise ValueError(f"gate_w must be [hidden={H}, num_experts], got {tuple(gate_w.shape)}")
     E = gate_w.shape[1]
+    if bias is not None:
+        _check_dev(bias, torch.float32, "bias", dev)
+        if tuple(bias.shape) != (E,):
+            raise ValueError(f"bias must be [{E}], got {tuple(bias.shape)}")
     if topk_ids is None:
         topk_ids = torch.empty(T, top_k, dtype=torch.int32, device=x.device)
     if topk_w is None:
         topk_w = torch.empty(T, top_k, dtype=torch.float32, device=x.device)
+    _check_dev(topk_ids, torch.int32, "topk_ids", dev)
+    _check_dev(topk_w, torch.float32, "topk_w", dev)
+    for name, t in (("topk_ids", topk_ids), ("topk_w", topk_w)):
+        if tuple(t.shape) != (T, top_k):
+            raise ValueError(f"{name} must be [{T}, {top_k}], got {tuple(t.shape)}")
     st = load_library().moe_route_noalloc(_ptr(x), _ptr(gate_w), _ptr(bias), T, H, E, top_k, _ptr(topk_ids),
                                           _ptr(topk_w), _stream(stream))
     if st != MOE_OK:
@@ -275,7 +298,7 @@ class MoE:
 
     def __init__(self, hidden: int, inter: int, num_experts: int, top_k: int, max_num_tokens: int,
                  device: int = 0, deterministic: bool = False, static_scales: bool = False,
-                 shared_inter: int = 0, shared_average: bool = False):
+                 shared_inter: int = 0, shared_average: bool = False, accurate_sigmoid: bool = False):
         self.H, self.I, self.E, self.K, self.Tmax = hidden, inter, num_experts, top_k, max_num_tokens
         self.device = device
         self.deterministic = deterministic
@@ -283,14 +306,17 @@ class MoE:
         self.shared_inter, self.shared_average = shared_inter, shared_average
         flags = (MOE_FLAG_DETERMINISTIC if deterministic else 0) | (MOE_FLAG_STATIC_ACT_SCALES if static_scales else 0)
         flags |= MOE_FLAG_SHARED_AVERAGE if shared_average else 0
+        flags |= MOE_FLAG_ACCURATE_SIGMOID if accurate_sigmoid else 0
+        self.accurate_sigmoid = accurate_sigmoid
         self._h = moe_create(hidden, inter, num_experts, top_k, max_num_tokens, device, flags, shared_inter)
         self.last_T = None
 
     @classmethod
     def from_shape(cls, shape, device: int = 0, deterministic: Optional[bool] = None, max_num_tokens=None,
-                   static_scales: bool = False):
+                   static_scales: bool = False, accurate_sigmoid: bool = False):
         return cls(shape.H, shape.I, shape.E, shape.K, max_num_tokens or shape.max_num_tokens, device,
-                   shape.deterministic if deterministic is None else deterministic, static_scales)
+                   shape.deterministic if deterministic is None else deterministic, static_scales,
+                   accurate_sigmoid=accurate_sigmoid)
 
     def set_static_scales(self, x_gs: torch.Tensor, h_gs: torch.Tensor, stream=None):
         moe_set_static_scales(self._h, x_gs, h_gs, stream)
@@ -405,6 +431,17 @@ class MoE:
         _raise(self._h, load_library().moe_debug_shared(self._h, _ptr(rows), _ptr(codes), _ptr(sf), _ptr(gs),
                                                         _stream(stream)))
         return rows, codes, sf, gs
+
+    def debug_shared_act_quant(self, stream=None):
+        """The shared expert's per-token quantization of x in the last
+        forward: codes [T, H/2], block scales [T, H/16], global scales [T]."""
+        T = self.last_T or 0
+        codes = self._dev((T, self.H // 2), torch.uint8)
+        sf = self._dev((T, self.H // 16), torch.uint8)
+        gs = self._dev((T,), torch.float32)
+        _raise(self._h, load_library().moe_debug_shared_act_quant(self._h, _ptr(codes), _ptr(sf), _ptr(gs),
+                                                                  _stream(stream)))
+        return codes, sf, gs
 
     def set_stage_timing(self, enable: bool = True):
         _raise(self._h, load_library().moe_set_stage_timing(self._h, int(enable)))

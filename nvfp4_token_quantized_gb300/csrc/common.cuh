@@ -3,7 +3,6 @@
 // NVFP4 block quantizer.
 #pragma once
 
-#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -188,15 +187,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 // ---------------------------------------------------------------------------
 // TMA and bulk copies (global -> shared, completion on an mbarrier)
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x,
-                                            int y, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
-      : "memory");
-}
-
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -209,22 +199,6 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint
 // into L2 without a destination or completion.
 __device__ __forceinline__ void prefetch_l2_bulk(const void* gsrc, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
-__device__ __forceinline__ uint64_t policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
 }
 
 // ---------------------------------------------------------------------------
@@ -278,19 +252,6 @@ __device__ __forceinline__ void tc_mma_fp4(uint32_t d_tmem, uint64_t a_desc, uin
       "}\n" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
-}
-
-// 16 consecutive FP32 columns of this thread's tensor-memory lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // 32 consecutive FP32 columns of this thread's tensor-memory lane.
@@ -363,11 +324,6 @@ __device__ __forceinline__ uint32_t cluster_map(const void* local_smem, uint32_t
   return remote;
 }
 
-// Store v at the same shared-memory offset in CTA `rank` of the cluster.
-__device__ __forceinline__ void st_shared_cluster_f32(const void* local_smem, uint32_t rank, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_map(local_smem, rank)), "f"(v) : "memory");
-}
-
 // Store a 32-bit word at the same shared-memory offset in CTA `rank` (one
 // single-copy-atomic access).
 __device__ __forceinline__ void st_shared_cluster_u32(const void* local_smem, uint32_t rank, uint32_t v) {
@@ -380,43 +336,6 @@ __device__ __forceinline__ uint32_t ld_shared_relaxed_u32(const void* local_smem
   asm volatile("ld.relaxed.cluster.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(local_smem)) : "memory");
   return v;
 }
-
-// Arrive (release, cluster scope) on the mbarrier at the same offset in CTA `rank`.
-__device__ __forceinline__ void mbar_arrive_remote(uint64_t* local_bar, uint32_t rank) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_map(local_bar, rank))
-               : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n"
-      ".reg .pred p;\n"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
-      "selp.u32 %0, 1, 0, p;\n"
-      "}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait with cluster-scope acquire (for barriers that CTAs of the
-// cluster arrive on remotely).
-__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                                          uint64_t timeout_ns = 2000000000ull) {
-  if (mbar_try_wait_acq_cluster(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait_acq_cluster(bar, parity)) return true;
-    if ((it & 255u) == 0) {
-      if (abort != nullptr && *abort) return false;
-      if (global_timer_ns() - t0 > timeout_ns) return false;
-    }
-  }
-}
-
-__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
 
 // Arrival on a grid-wide completion counter: an atomic add with
 // acquire-release semantics at GPU scope.  Called by one thread right after a
@@ -432,14 +351,6 @@ __device__ __forceinline__ uint32_t arrive_acq_rel_gpu(uint32_t* counter) {
 // Barrier among `nthreads` threads (whole warps) on hardware barrier `id`.
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-__device__ __forceinline__ float ld_shared_cluster_f32(const void* local_smem, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local_smem)), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-  return v;
 }
 
 // ---------------------------------------------------------------------------

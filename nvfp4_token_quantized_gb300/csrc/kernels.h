@@ -2,7 +2,6 @@
 // between the C ABI in moe_host.cu and the kernel translation units).
 #pragma once
 
-#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -149,6 +148,9 @@ struct GemmArgs {
   // static per-tensor contract: the w2 input's calibrated global scale per
   // expert (the w13 epilogue requantizes with it directly), or nullptr
   const float* h_gs_static;
+  // SwiGLU sigmoid: 0 = 1/2 + tanh.approx(g/2)/2, 1 = 1 / (1 + expf(-g))
+  // with an IEEE division
+  int accurate_sigmoid;
 };
 
 cudaError_t gemm_setup_attributes(int w13_chunks);

@@ -131,20 +131,21 @@ __host__ __device__ constexpr int smem_bytes_res(int stages, int nch, int a_rows
          2 * nch * TILE_M * 4 + HALF_MAX_BYTES + 1024;
 }
 
-// SwiGLU silu(g) * u with sigmoid(g) = 1/2 + tanh(g/2)/2: one special-function
-// operation per element (the hardware tanh, relative error about 2^-11, far
-// below the FP4 requantization that follows).  With an exponential and a
-// reciprocal per element, the w13 epilogue was bound by the special-function
-// units at full 128-row tiles.
+// SwiGLU silu(g) * u.  Default sigmoid(g) = 1/2 + tanh(g/2)/2: one
+// special-function operation per element (the hardware tanh, relative error
+// about 2^-11, below the FP4 requantization that follows).  With
+// `accurate`, sigmoid(g) = 1 / (1 + expf(-g)) with CUDA's expf and an IEEE
+// division (a few ulp): fewer of the requantization's near-tie decisions
+// differ from an FP64 evaluation.
 __device__ __forceinline__ float tanh_approx(float x) {
   float y;
   asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-__device__ __forceinline__ float swiglu(float g_acc, float u_acc, float alpha) {
+__device__ __forceinline__ float swiglu(float g_acc, float u_acc, float alpha, bool accurate) {
   const float g = __fmul_rn(g_acc, alpha);
   const float u = __fmul_rn(u_acc, alpha);
-  const float sig = fmaf(0.5f, tanh_approx(0.5f * g), 0.5f);
+  const float sig = accurate ? __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-g))) : fmaf(0.5f, tanh_approx(0.5f * g), 0.5f);
   return __fmul_rn(__fmul_rn(g, u), sig);
 }
 
@@ -450,10 +451,18 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
         }
         release_acc(0);  // everything is in registers: the tensor cores may refill the accumulator
         if (ready && warp_rows) {
+          if (p.accurate_sigmoid) {
+#pragma unroll 8
+            for (int q = 0; q < 64; ++q) {
+              h[q] = swiglu(h[q], uv[q], alpha, true);
+              amax = fmaxf(amax, fabsf(h[q]));
+            }
+          } else {
 #pragma unroll
-          for (int q = 0; q < 64; ++q) {
-            h[q] = swiglu(h[q], uv[q], alpha);
-            amax = fmaxf(amax, fabsf(h[q]));
+            for (int q = 0; q < 64; ++q) {
+              h[q] = swiglu(h[q], uv[q], alpha, false);
+              amax = fmaxf(amax, fabsf(h[q]));
+            }
           }
         }
         if (!row_ok) amax = 0.0f;

@@ -288,6 +288,7 @@ moe_status shared_branch(moe_handle* h, const void* x, int T, cudaStream_t s) {
   g.i_pad = h->Ipad_s;
   g.src_of_padrow = h->s_ident;  // row t is token t
   g.num_experts = 1;
+  g.accurate_sigmoid = (h->cfg.flags & MOE_FLAG_ACCURATE_SIGMOID) != 0;
   if (T <= SMALL_BATCH_TOKENS) {
     // one 64-row tile: column pairs spread over single CTAs (no cluster has
     // to find SMs of one GPC free next to the routed GEMMs), then the row
@@ -402,6 +403,7 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
     g.num_experts = E;
     g.prefetch_units = small ? W13_PREFETCH_UNITS : 0;
     g.h_gs_static = h->static_scales ? h->static_h_gs : nullptr;
+    g.accurate_sigmoid = (h->cfg.flags & MOE_FLAG_ACCURATE_SIGMOID) != 0;
     if (small) {
       // every tile reads the one shared activation tile; no clusters: the
       // units spread over all SMs, and the requantization follows as its own
@@ -929,6 +931,22 @@ moe_status moe_debug_shared(moe_handle* h, uint16_t* rows, uint8_t* h_codes, uin
   if (h_codes && h_sf && h_gs)
     CK(h, launch_export_rows(h->s_h_codes, h->s_h_codes, h->s_h_gs, T, h->Is, h->Ipad_s, h->s_ident, 1, 0, 0, 0,
                              h_codes, h_sf, h_gs, s));
+  return MOE_OK;
+}
+
+moe_status moe_debug_shared_act_quant(moe_handle* h, uint8_t* codes, uint8_t* sf, float* gs, void* stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  if (h->Is <= 0) {
+    set_err(h, "the handle was created without a shared expert (shared_inter = 0)");
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (h->last_T < 0) return MOE_ERR_NOT_LOADED;
+  if (!codes || !sf || !gs) return MOE_ERR_INVALID_ARG;
+  DeviceGuard dg(h->cfg.device);
+  if (h->last_T == 0) return MOE_OK;
+  // token t is row t of the shared expert's activation operand
+  CK(h, launch_export_rows(h->s_a_codes, h->s_a_codes, h->s_gs_rows, h->last_T, h->H, h->H, h->s_ident, 1, 0, 0, 0,
+                           codes, sf, gs, reinterpret_cast<cudaStream_t>(stream)));
   return MOE_OK;
 }
 

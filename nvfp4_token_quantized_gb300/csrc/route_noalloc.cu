@@ -1,15 +1,20 @@
 // route_noalloc.cu - moe_route_noalloc: router logits, top-k selection and
 // renormalised routing weights without a handle and without allocating.
 //
-// The routing arithmetic is the forward's own (the same two kernels), so the
-// result is bit-identical to the routing moe_forward computes.  The only
+// The routing arithmetic is the forward's own: the same router-tile and top-k
+// device functions (moe_forward runs them as router_logits_kernel and
+// topk_kernel above 64 tokens, and inside front_small_kernel at or below), so
+// the result is bit-identical to the routing moe_forward computes.  The only
 // difference is where the intermediate lives: the FP32 logits [T, E] and the
 // per-expert row counters go to one file-scope device array of fixed size
 // instead of a handle's workspace.
 //
 // The first call on a device does the set-up for that device (looks the
-// array's address up and raises the router kernel's shared-memory cap) and
-// should come before any stream capture.  Calls whose work overlaps on one
+// array's address up and raises the router kernel's shared-memory cap).  With
+// CUDA's lazy module loading, that look-up is also what loads this file's
+// device code on the device and so reserves the array there; the first call
+// should therefore come before any stream capture, and before a memory pool
+// claims the device's free memory.  Calls whose work overlaps on one
 // device share the array and race: order them on one stream.
 #include <mutex>
 

@@ -120,6 +120,57 @@ def oracle_forward(wl, tokens=None, static_scales=None):
     return omoe.moe_forward(x, wg, q13, q2, wl.shape.K, bias, tokens=tokens, static_scales=static_scales)
 
 
+def _bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def oracle_forward_parallel(wl, tokens):
+    """``oracle_forward(wl, tokens)`` (per-token scales) computed expert by
+    expert in worker processes: routing, per-token quantization and the
+    finalize here, each expert's weight quantization and GEMMs in a worker
+    (``tests/oracle_jobs.py``).  Returns (out float32 [n, H] - the bf16
+    output widened, ids [n, K], h_gs {(token, slot): float32})."""
+    from tests import oracle_jobs
+
+    tok = np.asarray(tokens, dtype=np.int64)
+    K = wl.shape.K
+    _, ids, w = oracle_route(wl, tok)
+    xs = omoe.as_f32(wl.x)[tok]
+    codes, sf, gs = onv.quantize_rows(xs)
+    jobs, where = [], []
+    for e in np.unique(ids):
+        sel_t, sel_j = np.nonzero(ids == e)          # token-ascending, as the oracle's forward
+        jobs.append((_bf16_bits(wl.w13[int(e)]), _bf16_bits(wl.w2[int(e)]), codes[sel_t], sf[sel_t], gs[sel_t]))
+        where.append((sel_t, sel_j))
+    results = list(_pool().map(oracle_jobs.expert_job, jobs)) if len(jobs) > 1 else \
+        [oracle_jobs.expert_job(j) for j in jobs]
+    y_rows = np.zeros((len(tok), K, wl.shape.H), np.float32)
+    h_gs = {}
+    for (sel_t, sel_j), (y2, hg) in zip(where, results):
+        y_rows[sel_t, sel_j] = y2
+        for i, (t, j) in enumerate(zip(sel_t, sel_j)):
+            h_gs[(int(tok[t]), int(j))] = hg[i]
+    out = onv.bf16_to_f32(onv.bf16_round(omoe.finalize(y_rows, w)))
+    return out, ids, h_gs
+
+
+def tile_covering_tokens(ids: np.ndarray, num_experts: int, tile_rows: int = 128):
+    """Tokens whose rows include the first and the last row of every
+    tile_rows-row GEMM tile of every expert with rows (each expert's ragged
+    last tile included), in the expert-grouped, token-ordered row order of
+    the permutation; ids int [T, K] is the whole batch's top-k choice."""
+    ids = np.asarray(ids)
+    K = ids.shape[1]
+    off, src, _ = omoe.permute(ids, num_experts)
+    toks = set()
+    for e in range(num_experts):
+        n = int(off[e + 1] - off[e])
+        for r0 in range(0, n, tile_rows):
+            for r in (r0, min(r0 + tile_rows, n) - 1):
+                toks.add(int(src[off[e] + r]) // K)
+    return np.array(sorted(toks), dtype=np.int64)
+
+
 def sample_tokens(T: int, n: int, extra=()):
     """n evenly spread token indices (always the first and last) plus extras."""
     base = np.linspace(0, T - 1, min(n, T)).astype(np.int64)

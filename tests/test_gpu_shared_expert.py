@@ -8,6 +8,7 @@ with the fused requantization, w2 GEMM into bf16 rows) and joins it before
 the finalize, which adds the shared row to the routed FP32 sum.  Checked
 through the C ABI against the oracle with ``shared=(w13s, w2s)``:
 
+* the shared branch's own per-token quantization of x, bit for bit;
 * the shared rows and the layer output against the oracle, with the
   shared intermediate's rare near-tie requantization decisions taken from
   the GPU on both sides (see _check);
@@ -41,7 +42,7 @@ def _bf16(a):
     return onv.bf16_to_f32(onv.bf16_round(np.asarray(a, dtype=np.float32)))
 
 
-def _run(shape, T, Is, average, deterministic=False, seed=3):
+def _run(shape, T, Is, average, deterministic=False, seed=3, accurate=False):
     from nvfp4_token_quantized_gb300 import MoE
 
     built()
@@ -49,7 +50,7 @@ def _run(shape, T, Is, average, deterministic=False, seed=3):
     w13s, w2s = synthetic.make_shared_weights(shape, Is, seed=seed)
     d = to_dev(wl)
     layer = MoE(shape.H, shape.I, shape.E, shape.K, shape.max_num_tokens, device=0, deterministic=deterministic,
-                shared_inter=Is, shared_average=average)
+                shared_inter=Is, shared_average=average, accurate_sigmoid=accurate)
     layer.load_weights(d["w13"], d["w2"])
     layer.load_shared_weights(w13s.cuda(), w2s.cuda())
     out = layer.forward(d["x"], d["gate_w"])
@@ -79,6 +80,11 @@ def _check(layer, out, ref, routed, q2s, q13s, average, what):
     both sides), and every row whose intermediate matches exactly equals the
     oracle's full forward."""
     T = out.shape[0]
+    # the shared branch quantizes x itself: bit for bit the per-token rules
+    ac, asf, ags = (t.cpu().numpy() for t in layer.debug_shared_act_quant())
+    assert np.array_equal(ags.view(np.uint32), ref.x_gs.view(np.uint32)), f"{what}: shared input global scales"
+    assert np.array_equal(asf, ref.x_sf), f"{what}: shared input block scales"
+    assert np.array_equal(ac, onv.pack_e2m1(ref.x_codes)), f"{what}: shared input codes"
     rows, hc, hsf, hgs = (t.cpu() for t in layer.debug_shared())
     sr = omoe.expert_rows(ref.x_codes, ref.x_sf, ref.x_gs, q13s, q2s, 0)
     hgs = hgs.numpy()
@@ -187,3 +193,46 @@ def test_maximum_widths(T):
     assert np.array_equal(r["topk_ids"].cpu().numpy(), ref.ids)
     _check(layer, out, ref, routed, q2s, q13s, False, f"maximum widths, T={T}")
     layer.close()
+
+
+FLIP = synthetic.MoEShape(name="flip_rate", T=2048, H=2048, E=8, K=1, I=128, max_num_tokens=2048)
+
+
+@pytest.mark.parametrize("T", [64, 2048])
+def test_sigmoid_forms_flip_rate(T):
+    """How often the SwiGLU's sigmoid form moves a requantization decision of
+    the intermediate away from the oracle's FP64 evaluation: the shared
+    expert (weight one, 1536 features per row) of T tokens, once with the
+    hardware-tanh sigmoid (the default) and once with the accurate one
+    (MOE_FLAG_ACCURATE_SIGMOID).  T = 64 runs the small-batch w13 GEMM and the
+    row requantization kernel, T = 2048 the cluster GEMM with the fused
+    requantization.  The counts are printed for the record; the accurate
+    form must not flip more blocks."""
+    from nvfp4_token_quantized_gb300 import MoE
+
+    built()
+    Is = 1536
+    wl = synthetic.make_workload(FLIP, T=T, seed=11)
+    w13s, w2s = synthetic.make_shared_weights(FLIP, Is, seed=11)
+    q13s = omoe.quantize_weights(omoe.as_f32(w13s)[None])
+    q2s = omoe.quantize_weights(omoe.as_f32(w2s)[None])
+    xc, xs, xg = onv.quantize_rows(omoe.as_f32(wl.x))
+    sr = omoe.expert_rows(xc, xs, xg, q13s, q2s, 0)
+    d = to_dev(wl)
+    counts = {}
+    for accurate in (False, True):
+        layer = MoE(FLIP.H, FLIP.I, FLIP.E, FLIP.K, FLIP.max_num_tokens, device=0, shared_inter=Is,
+                    accurate_sigmoid=accurate)
+        layer.load_weights(d["w13"], d["w2"])
+        layer.load_shared_weights(w13s.cuda(), w2s.cuda())
+        layer.forward(d["x"], d["gate_w"])
+        torch.cuda.synchronize()
+        _, hc, hsf, hgs = (t.cpu().numpy() for t in layer.debug_shared())
+        layer.close()
+        np.testing.assert_allclose(hgs, sr["h_gs"], rtol=1e-4)
+        codes = np.stack([hc & 0xF, hc >> 4], -1).reshape(T, -1)
+        blk = (codes != sr["h_codes"]).reshape(T, -1, 16).any(2) | (hsf != sr["h_sf"])
+        counts[accurate] = (int(blk.any(1).sum()), int(blk.sum()), blk.size)
+    print(f"\nflip rate T={T}: tanh.approx rows {counts[False][0]}/{T}, blocks {counts[False][1]}/"
+          f"{counts[False][2]}; accurate rows {counts[True][0]}/{T}, blocks {counts[True][1]}/{counts[True][2]}")
+    assert counts[True][1] <= counts[False][1]

@@ -176,3 +176,16 @@ def test_swapped_gate_up_would_be_detected():
     rms = np.sqrt(np.mean(good.out.astype(np.float64) ** 2))
     err = np.abs(bad.out - good.out)
     assert np.any(err > 2e-2 * rms + 5e-2 * np.abs(good.out))
+
+
+def test_silu_hand_values():
+    """silu(g) = g * sigmoid(g) at points worked out on paper: sigmoid(0) = 1/2;
+    e^(-ln 3) = 1/3 gives sigmoid(ln 3) = 3/4 and sigmoid(-ln 3) = 1/4;
+    e^(-ln 4) = 1/4 gives sigmoid(ln 4) = 4/5.  Large negative gates vanish,
+    large positive gates pass through."""
+    ln3, ln4 = math.log(3.0), math.log(4.0)
+    got = moe.silu(np.array([0.0, ln3, -ln3, ln4, -ln4, -60.0, 60.0]))
+    want = np.array([0.0, 0.75 * ln3, -0.25 * ln3, 0.8 * ln4, -0.2 * ln4, 0.0, 60.0])
+    np.testing.assert_allclose(got, want, rtol=1e-15, atol=1e-24)
+    assert got[0] == 0.0
+    assert abs(got[5]) < 1e-24  # -60 * e^-60

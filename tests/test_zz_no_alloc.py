@@ -83,11 +83,14 @@ def test_noalloc_routing_matches_the_forward(name):
         finally:
             gc.enable()
         assert allocated_after == allocated
-        if call == 1:  # the first call on the device has loaded the library's code
+        # Call 0 may be the first on this device when the file runs alone: it
+        # loads the library's device code there (lazy module loading), which
+        # reserves the fixed scratch array.  Every later call allocates nothing.
+        if call == 1:
             assert free_after == free_before, "device memory changed during the call"
         assert torch.equal(ids, ids_ref), f"call {call}: top-k ids differ from the forward's routing"
-        np.testing.assert_allclose(w.cpu().numpy(), w_ref.cpu().numpy(), rtol=3e-6, atol=1e-7,
-                                   err_msg=f"call {call}: routing weights differ")
+        # the same device functions on the same inputs: the weights agree bit for bit
+        assert torch.equal(w.view(torch.int32), w_ref.view(torch.int32)), f"call {call}: routing weights differ"
 
 
 @gpu
