@@ -149,6 +149,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// Add `bytes` to the transaction count of the current phase without
+// arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
@@ -346,6 +353,28 @@ __device__ __forceinline__ uint32_t arrive_acq_rel_gpu(uint32_t* counter) {
   uint32_t old;
   asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
   return old;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Wait until *counter >= target (acquire, GPU scope), for at most
+// ~timeout_ns; gives up early once `abort` is raised.  False if it gave up.
+__device__ __forceinline__ bool wait_counter_acquire(const uint32_t* counter, uint32_t target, volatile int* abort,
+                                                     uint64_t timeout_ns = 2000000000ull) {
+  if (ld_acquire_gpu_u32(counter) >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(32);
+    if (ld_acquire_gpu_u32(counter) >= target) return true;
+    if ((it & 63u) == 0) {
+      if (abort != nullptr && *abort) return false;
+      if (global_timer_ns() - t0 > timeout_ns) return false;
+    }
+  }
 }
 
 // Barrier among `nthreads` threads (whole warps) on hardware barrier `id`.

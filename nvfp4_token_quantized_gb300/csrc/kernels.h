@@ -2,6 +2,7 @@
 // between the C ABI in moe_host.cu and the kernel translation units).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -76,6 +77,11 @@ cudaError_t launch_shared_tiles(int T, int4* tiles, int32_t* num_tiles, cudaStre
 // e is padded row e*128 + t.
 constexpr int SMALL_BATCH_TOKENS = 64;
 struct FrontArgs {
+  // tensor map of the router weight viewed as [H/8][8][E] bf16 whose box
+  // reaches one row and 8 columns past the data (zeros): the staged rows and
+  // 8-row chunks come out padded (see launch_front_small)
+  CUtensorMap wg_map;
+  int wg_map_ok;              // 0: stage rows with plain bulk copies instead
   const void* x;              // [T, H] bf16
   const void* gate_w;         // [H, E] bf16
   const float* bias;          // [E] or nullptr
@@ -95,10 +101,25 @@ struct FrontArgs {
   int32_t* num_tiles;
   uint32_t* sync;             // FRONT_SYNC_WORDS counters, zero between launches
   const float* static_gs;     // calibrated per-tensor scale (static contract), or nullptr
+  // The GEMMs run the all-experts schedule and do not wait for the grouping
+  // (expert_offsets, src_of_row, row_of_src, pad_row_of_src, tiles): the
+  // requantization kernel derives it instead.
+  int all_experts;
+  int* status;                // device status word (a bounded wait that ran out)
 };
 constexpr int FRONT_SYNC_WORDS = 64;
+// Words of the front kernel's sync block used by the all-experts small-batch
+// path (returned to zero by the requantization kernel): front CTAs that
+// quantized their tokens, front CTAs that routed their tokens, and the
+// dynamic work counter of the w13 GEMM.
+constexpr int FRONT_SYNC_A_READY = 0;
+constexpr int FRONT_SYNC_ROUTED = 1;
+constexpr int FRONT_SYNC_WORK = 2;
+// CTAs of the front kernel's grid for T tokens and E experts.
+int front_ctas(int T, int E);
 cudaError_t front_setup(int H, int E);
-cudaError_t launch_front_small(const FrontArgs& a, cudaStream_t s);
+// Fills a.wg_map / a.wg_map_ok for a.gate_w, then launches.
+cudaError_t launch_front_small(FrontArgs& a, cudaStream_t s);
 
 struct GemmArgs {
   const uint8_t* a_codes;     // A operand (codes and block scales), operand layout
@@ -148,6 +169,16 @@ struct GemmArgs {
   // static per-tensor contract: the w2 input's calibrated global scale per
   // expert (the w13 epilogue requantizes with it directly), or nullptr
   const float* h_gs_static;
+  // Small batches in which nearly every expert has rows (w13s and w2): the
+  // units are every expert's tile in expert order (tile i = expert i, padded
+  // rows i*128 .. i*128 + small_T - 1), independent of the tile list, so the
+  // kernel streams weights into its ring before the dependency wait.
+  int all_experts;
+  int small_T;
+  // all-experts small-batch w13 only: the front kernel's sync words and its
+  // grid size (dynamic schedule, no dependency wait); nullptr otherwise
+  uint32_t* front_sync;
+  int front_ctas;
   // SwiGLU sigmoid: 0 = 1/2 + tanh.approx(g/2)/2, 1 = 1 / (1 + expf(-g))
   // with an IEEE division
   int accurate_sigmoid;
@@ -167,7 +198,17 @@ cudaError_t launch_gemm_w13(const GemmArgs& a, int n_chunks, int n_clusters, int
 // FP32 output into the w2 operand.  resident keeps the shared activation tile
 // in shared memory for the whole kernel (K <= 2048).
 cudaError_t launch_gemm_w13s(const GemmArgs& a, int n_ctas, bool resident, cudaStream_t s);
-cudaError_t launch_requant_rows(const float* hbuf, float* row_amax, const int32_t* pad_row_of_src, int n_rows,
+// The row of expanded row i (token * K + slot) is row_map[i], or with topk_ids
+// given the small-batch padded row topk_ids[i] * 128 + i / K.  grouping: when
+// not null, one extra CTA derives the small batch's expert grouping from
+// topk_ids (T = n_rows / K tokens, E experts) while the others requantize.
+struct SmallGroupOut;
+// front_sync (with grouping): the all-experts path's sync words, returned to
+// zero, and the rows of tokens that did not route to an expert have their
+// maxima cleared (the dynamic w13 GEMM may have formed them).
+cudaError_t launch_requant_rows(const float* hbuf, float* row_amax, const int32_t* row_map,
+                                const int32_t* topk_ids, int K, int E, const SmallGroupOut* grouping,
+                                uint32_t* front_sync, const int32_t* src_of_padrow, int n_rows,
                                 int I, int i_pad, uint8_t* h_codes, float* h_gs, cudaStream_t s);
 cudaError_t launch_gemm_w2(const GemmArgs& a, int n_ctas, bool ordered, int a_rows, cudaStream_t s);
 cudaError_t launch_gemm_plain(const GemmArgs& a, int n_ctas, cudaStream_t s);

@@ -98,14 +98,22 @@ enum Mode { MODE_W13 = 0, MODE_W2_ATOMIC = 1, MODE_W2_ORDERED = 2, MODE_PLAIN = 
 // layout and the host's launch size both use.
 __host__ __device__ constexpr bool pair_mode(int mode) { return mode != MODE_PLAIN; }
 
+constexpr int UNIT_QUEUE = 4;  // dynamic schedule: units published ahead by the producer
+
 struct Ctrl {
   uint64_t full[MAX_STAGES];
   uint64_t empty[MAX_STAGES];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t a_full;  // resident activations loaded (resident-A kernels)
+  // dynamic schedule: unit n of the CTA is q_unit[n % UNIT_QUEUE], published
+  // by the producer (q_full) and released by the MMA thread and the 8
+  // epilogue warps (q_empty)
+  uint64_t q_full[UNIT_QUEUE];
+  uint64_t q_empty[UNIT_QUEUE];
   uint32_t tmem_base;
   int abort_flag;
+  int q_unit[UNIT_QUEUE];
 };
 static_assert(sizeof(Ctrl) <= CTRL_BYTES, "control block too large");
 
@@ -227,16 +235,72 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
       r.e = ti.x; r.row0 = ti.y; r.valid = ti.z; r.col = 2 * (int)rank + (u & 1); r.arow = ti.w;
     } else if constexpr (MODE == MODE_W13S) {
       const int pair = u >> 1;
-      const int4 ti = p.tiles[pair / nch];
-      r.e = ti.x; r.row0 = ti.y; r.valid = ti.z; r.col = 2 * (pair % nch) + (u & 1); r.arow = ti.w;
+      const int tile = pair / nch;
+      r.col = 2 * (pair % nch) + (u & 1);
+      if (p.all_experts) {  // tile i is expert i: padded rows i*128 + t, the shared activation tile
+        r.e = tile; r.row0 = tile * TILE_M; r.valid = p.small_T; r.arow = 0;
+      } else {
+        const int4 ti = p.tiles[tile];
+        r.e = ti.x; r.row0 = ti.y; r.valid = ti.z; r.arow = ti.w;
+      }
     } else if constexpr (MODE == MODE_PLAIN) {
       r.e = 0; r.row0 = (u / p.n_tiles) * TILE_M; r.valid = TILE_M; r.col = u % p.n_tiles; r.arow = r.row0;
     } else {
-      const int4 ti = p.tiles[u / p.n_tiles];
+      const int tile = u / p.n_tiles;
+      r.col = u % p.n_tiles;
+      if (p.all_experts) {
+        r.e = tile; r.row0 = tile * TILE_M; r.valid = p.small_T;
+      } else {
+        const int4 ti = p.tiles[tile];
+        r.e = ti.x; r.row0 = ti.y; r.valid = ti.z;
+      }
       // the w2 GEMM's activations are the intermediate rows at the padded rows
-      r.e = ti.x; r.row0 = ti.y; r.valid = ti.z; r.col = u % p.n_tiles; r.arow = ti.y;
+      r.arow = r.row0;
     }
     return r;
+  };
+  // Work units of the launch.  With all_experts (small batches in which
+  // nearly every expert has rows) the list is every expert in order and is
+  // known before the previous kernels finish; otherwise it is the tile list
+  // they write, read only after the dependency wait.
+  auto count_units = [&]() -> int {
+    if constexpr (MODE == MODE_W13) return 2 * (*p.num_tiles);
+    else if constexpr (MODE == MODE_W13S) return 2 * nch * (p.all_experts ? p.num_experts : *p.num_tiles);
+    else if constexpr (MODE == MODE_PLAIN) return p.m_tiles * p.n_tiles;
+    else return (p.all_experts ? p.num_experts : *p.num_tiles) * p.n_tiles;
+  };
+  // Dynamic schedule (the small-batch w13 GEMM over all experts, launched
+  // while the front kernel still runs): the CTAs take unit pairs from a
+  // global counter, so that CTAs which start late - on the front kernel's
+  // SMs - take fewer.  Instead of a dependency wait the kernel reads the
+  // front kernel's counters: the producer waits until every front CTA has
+  // quantized its tokens before it loads activations; the epilogue treats
+  // every row as routed until every front CTA has routed its tokens; and no
+  // CTA finishes before routing has finished (so later kernels, which wait
+  // for this one, see it).
+  const bool dyn = !ARES && MODE == MODE_W13S && p.all_experts && p.front_sync != nullptr;
+  const uint32_t front_n = (uint32_t)p.front_ctas;
+  auto static_unit = [&](int n) -> int {
+    const int u = first + n * stride;
+    return u < count_units() ? u : -1;
+  };
+  // consumer side of the queue: unit n, or -1 when the CTA is done (or gave up)
+  auto queued_unit = [&](int n, bool single_thread) -> int {
+    const int q = n % UNIT_QUEUE;
+    bool ok = true;
+    if (single_thread || lane == 0) ok = mbar_wait_bounded(&c.q_full[q], (n / UNIT_QUEUE) & 1, &c.abort_flag);
+    if (!single_thread) ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (!ok) {
+      if (single_thread || lane == 0) {
+        c.abort_flag = 1;
+        report_device_error(p.status, DEV_ERR_TIMEOUT);
+      }
+      return -1;
+    }
+    const int u = *reinterpret_cast<volatile int*>(&c.q_unit[q]);
+    if (!single_thread) __syncwarp();
+    if (single_thread || lane == 0) mbar_arrive(&c.q_empty[q]);
+    return u;
   };
 
   if (threadIdx.x == 0) {
@@ -249,6 +313,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
       mbar_init(&c.acc_empty[b], EPI_WARPS);
     }
     mbar_init(&c.a_full, 1);
+    for (int q = 0; q < UNIT_QUEUE; ++q) {
+      mbar_init(&c.q_full[q], 1);
+      mbar_init(&c.q_empty[q], 1 + EPI_WARPS);
+    }
     c.abort_flag = 0;
     if (MODE == MODE_W13)
       for (int i = 0; i < 2 * nch * TILE_M; ++i) part[i] = 0x80000000u;  // tag of no first use
@@ -264,29 +332,65 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
   tc_fence_after();
   const uint32_t tmem = c.tmem_base;
   const int KS = p.k_stages;
-  if (MODE != MODE_PLAIN && warp == 0 && lane == 0 && p.prefetch_units > 0) {
-    // Weights do not depend on the previous kernels: stream the expected
-    // first units' weight tiles into L2 while those kernels still run.
-    int u = first;
-    for (int k = 0; k < p.prefetch_units; ++k, u = next(u)) {
-      const int tile = (MODE == MODE_W13) ? (u >> 1) : (MODE == MODE_W13S ? (u >> 1) / nch : u / p.n_tiles);
-      if (tile >= p.num_experts) break;
-      const int col = (MODE == MODE_W13)    ? 2 * (int)rank + (u & 1)
-                      : (MODE == MODE_W13S) ? 2 * ((u >> 1) % nch) + (u & 1)
-                                            : u % p.n_tiles;
-      if (u & 1) continue;  // the pair block of an even unit holds both tiles
-      const int brow0 = tile * p.b_rows_per_expert + col * TILE_N;
-      const uint8_t* b_src = p.b_codes + (size_t)(brow0 >> 8) * KS * WPAIR_BYTES;
-      for (int ks = 0; ks < KS; ++ks) prefetch_l2_bulk(b_src + (size_t)ks * WPAIR_BYTES, WPAIR_BYTES);
+  // Stages of the ring whose weight tile the producer issued before the
+  // dependency wait (their activation tiles follow after it).
+  constexpr bool PRE_ISSUE = !ARES && (MODE == MODE_W13S || MODE == MODE_W2_ATOMIC || MODE == MODE_W2_ORDERED);
+  uint32_t g_pre = 0;
+  int u_first = -1;  // dynamic schedule: the producer's first unit
+  // producer side of the queue: fetch the CTA's unit n from the global counter
+  auto fetch_unit = [&](int n) -> int {
+    const int q = n % UNIT_QUEUE;
+    if (!mbar_wait_bounded(&c.q_empty[q], ((n / UNIT_QUEUE) & 1) ^ 1, &c.abort_flag)) {
+      c.abort_flag = 1;
+      report_device_error(p.status, DEV_ERR_TIMEOUT);
+      return -1;
+    }
+    const int pair = (int)atomicAdd(p.front_sync + FRONT_SYNC_WORK, 1u);
+    const int u = pair < count_units() / 2 ? 2 * pair : -1;
+    c.q_unit[q] = u;
+    mbar_arrive(&c.q_full[q]);
+    return u;
+  };
+  if (MODE != MODE_PLAIN && warp == 0 && lane == 0) {
+    if (p.prefetch_units > 0 && !dyn) {
+      // Weights do not depend on the previous kernels: stream the expected
+      // first units' weight tiles into L2 while those kernels still run.
+      int u = first;
+      for (int k = 0; k < p.prefetch_units; ++k, u = next(u)) {
+        const int tile = (MODE == MODE_W13) ? (u >> 1) : (MODE == MODE_W13S ? (u >> 1) / nch : u / p.n_tiles);
+        if (tile >= p.num_experts) break;
+        const int col = (MODE == MODE_W13)    ? 2 * (int)rank + (u & 1)
+                        : (MODE == MODE_W13S) ? 2 * ((u >> 1) % nch) + (u & 1)
+                                              : u % p.n_tiles;
+        if (u & 1) continue;  // the pair block of an even unit holds both tiles
+        const int brow0 = tile * p.b_rows_per_expert + col * TILE_N;
+        const uint8_t* b_src = p.b_codes + (size_t)(brow0 >> 8) * KS * WPAIR_BYTES;
+        for (int ks = 0; ks < KS; ++ks) prefetch_l2_bulk(b_src + (size_t)ks * WPAIR_BYTES, WPAIR_BYTES);
+      }
+    }
+    if (PRE_ISSUE && p.all_experts) {
+      // The unit list does not depend on the previous kernels: fill the
+      // ring's weight slots now.  Each slot's barrier first expects only the
+      // weight bytes; the producer arrives (and adds the activation bytes)
+      // when it issues the activation tile, once the activations are ready.
+      if (dyn) u_first = fetch_unit(0);
+      for (int n = 0; g_pre < (uint32_t)STAGES; ++n) {
+        const int u = dyn ? (n == 0 ? u_first : -1) : static_unit(n);
+        if (u < 0) break;
+        const Unit un = unit_at(u);
+        const int brow0 = un.e * p.b_rows_per_expert + un.col * TILE_N;
+        for (int ks = 0; ks < KS && g_pre < (uint32_t)STAGES; ++ks, ++g_pre) {
+          mbar_expect_tx(&c.full[g_pre], BS);
+          bulk_load(sB + g_pre * BS, p.b_codes + ((size_t)(brow0 >> 8) * KS + ks) * WPAIR_BYTES, WPAIR_BYTES,
+                    &c.full[g_pre]);
+        }
+      }
     }
   }
   // Everything above overlaps the previous kernel's tail; its outputs (the
   // tile list, operands, scales) are read only from here on.
-  pdl_wait();
-  int nunits;
-  if constexpr (MODE == MODE_W13) nunits = 2 * (*p.num_tiles);
-  else if constexpr (MODE == MODE_W13S) nunits = 2 * nch * (*p.num_tiles);
-  else nunits = (MODE == MODE_PLAIN ? p.m_tiles : *p.num_tiles) * p.n_tiles;
+  if (!dyn) pdl_wait();
+  const int nunits = count_units();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -303,7 +407,19 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
           bulk_load(sA + ks * A_SLOT, a_src + (size_t)ks * OPERAND_TILE_BYTES, a_bytes, &c.a_full);
         a_issued = true;
       }
-      for (int u = first; u < nunits && !c.abort_flag; u = PAIR ? next(next(u)) : next(u)) {
+      if (dyn) {
+        // the activations: every front CTA has quantized its tokens (bounded)
+        bool ok = wait_counter_acquire(p.front_sync + FRONT_SYNC_A_READY, front_n, &c.abort_flag);
+        if (!ok) {
+          c.abort_flag = 1;
+          report_device_error(p.status, DEV_ERR_TIMEOUT);
+        }
+        // they were written by another kernel's generic stores; the bulk
+        // copies below read them through the async proxy
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
+      int u = dyn ? u_first : static_unit(0);
+      for (int n = 0; u >= 0 && !c.abort_flag;) {
         const Unit un = unit_at(u);
         const int brow0 = (MODE == MODE_PLAIN ? 0 : un.e * p.b_rows_per_expert) + un.col * TILE_N;
         // scales + valid rows, in whole 8-row swizzle groups
@@ -313,6 +429,12 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
         const uint8_t* b_src = p.b_codes + (size_t)(brow0 >> 7) * KS * OPERAND_TILE_BYTES;
         for (int ks = 0; ks < KS; ++ks, ++g) {
           const int s = g % STAGES;
+          if (PRE_ISSUE && g < g_pre) {
+            // the weight tile of this (first) use of the slot is in flight
+            mbar_arrive_expect_tx(&c.full[s], a_bytes);
+            bulk_load(sA + s * A_SLOT, a_src + (size_t)ks * OPERAND_TILE_BYTES, a_bytes, &c.full[s]);
+            continue;
+          }
           if (!mbar_wait_bounded(&c.empty[s], ((g / STAGES) & 1) ^ 1, &c.abort_flag)) {
             c.abort_flag = 1;
             report_device_error(p.status, DEV_ERR_TIMEOUT);
@@ -329,6 +451,15 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
             bulk_load(slot_b, b_src + (size_t)ks * OPERAND_TILE_BYTES, B_SLOT, &c.full[s]);
           }
         }
+        ++n;
+        u = dyn ? fetch_unit(n) : static_unit(n);
+      }
+      if (PRE_ISSUE) {
+        // After an abort the loop above may stop before it reached every
+        // stage whose weight tile was issued before the dependency wait: arrive
+        // on those barriers so that they complete once the weight bytes land,
+        // and wait for them below.  (Without an abort g >= g_pre here.)
+        for (; g < g_pre; ++g) mbar_arrive(&c.full[g]);
       }
       if (c.abort_flag) {
         // Unwinding: let the copies already issued land before the CTA's
@@ -348,8 +479,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
         c.abort_flag = 1;
         report_device_error(p.status, DEV_ERR_TIMEOUT);
       }
-      for (int u = first; u < nunits; u = PAIR ? next(next(u)) : next(u), ++n) {
-        if (c.abort_flag) break;
+      for (;; ++n) {
+        const int u = dyn ? queued_unit(n, true) : static_unit(n);
+        if (u < 0 || c.abort_flag) break;
         // column pairs: one accumulator (buffer 0), used by every pair
         const int buf = PAIR ? 0 : n & 1;
         const uint32_t acc_parity = PAIR ? ((n & 1) ^ 1) : (((n >> 1) & 1) ^ 1);
@@ -420,14 +552,28 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
     };
 
     if constexpr (W13L) {
-      int i = 0;  // m-tiles (w13s: unit pairs) processed
-      for (int u = first; u < nunits; u = next(next(u)), ++i) {
+      bool a_seen = !dyn;  // dynamic schedule: the activation scales acquired
+      // i: m-tiles (w13s: unit pairs) processed
+      for (int i = 0;; ++i) {
+        const int u = dyn ? queued_unit(i, false) : static_unit(i);
+        if (u < 0) break;
+        if (!a_seen) {
+          if (!wait_counter_acquire(p.front_sync + FRONT_SYNC_A_READY, front_n, &c.abort_flag)) {
+            c.abort_flag = 1;
+            report_device_error(p.status, DEV_ERR_TIMEOUT);
+          }
+          a_seen = true;
+        }
         const Unit un = unit_at(u);
         const bool warp_rows = quarter * 32 < un.valid;  // warp-uniform
         const int prow = un.row0 + m;
         // rows of the shared small-batch tile whose token did not pick this
-        // expert take no part (their amax counts as 0 in the exchange)
-        const bool row_ok = m < un.valid && p.src_of_padrow[prow] >= 0;
+        // expert take no part (their amax counts as 0 in the exchange);
+        // dynamic schedule: until the routing is known every row of the tile
+        // is formed (the requantization reads only the routed ones)
+        const bool routed =
+            !dyn || ld_acquire_gpu_u32(p.front_sync + FRONT_SYNC_ROUTED) >= front_n;
+        const bool row_ok = m < un.valid && (!routed || p.src_of_padrow[prow] >= 0);
         const float alpha = row_ok ? __fdiv_rn(1.0f, __fmul_rn(p.gs_rows[un.arow + m], p.gs_w[un.e])) : 0.0f;
         // this thread's tile of the pair's 128 x 256 accumulator: columns
         // [128 half, +64) are gate features, the next 64 the matching up
@@ -451,8 +597,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
         }
         release_acc(0);  // everything is in registers: the tensor cores may refill the accumulator
         if (ready && warp_rows) {
+          // (both loops fully unrolled: h and uv must stay in registers)
           if (p.accurate_sigmoid) {
-#pragma unroll 8
+#pragma unroll
             for (int q = 0; q < 64; ++q) {
               h[q] = swiglu(h[q], uv[q], alpha, true);
               amax = fmaxf(amax, fabsf(h[q]));
@@ -542,6 +689,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
           if (f0 == 0) p.h_gs[prow] = gs_h;
         }
       }
+      if (dyn && warp == 2 && lane == 0 &&
+          !wait_counter_acquire(p.front_sync + FRONT_SYNC_ROUTED, front_n, nullptr))
+        report_device_error(p.status, DEV_ERR_TIMEOUT);
     } else {
       // pairs: the thread's 128-column tile `half` of the 128 x 256
       // accumulator; plain: its 64-column half of the 128-column buffer

@@ -9,6 +9,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "grouping.cuh"
 #include "kernels.h"
 
 namespace moe {
@@ -89,20 +90,46 @@ __global__ void __launch_bounds__(256, 4) act_quant_kernel(const __nv_bfloat16* 
 }
 
 // Requantization of the small-batch w13 output: one warp per expanded row
-// (token * K + slot), at its padded row pad_row_of_src[row].  Row maximum ->
-// global scale -> block scales and codes, the same arithmetic as the fused
-// w13 epilogue; returns the row's maximum word to zero.
+// (token * K + slot), at its padded row: topk_ids[row] * 128 + row / K in the
+// small-batch layout, or row_map[row].  Row maximum -> global scale -> block
+// scales and codes, the same arithmetic as the fused w13 epilogue; returns
+// the row's maximum word to zero.  With do_group the last CTA instead derives
+// the batch's expert grouping from topk_ids (the GEMMs of the all-experts
+// schedule do not need it; the parity exports read it).
 __global__ void __launch_bounds__(256) requant_rows_kernel(const float* __restrict__ hbuf,
                                                           float* __restrict__ row_amax,
-                                                          const int32_t* __restrict__ pad_row_of_src, int n_rows,
+                                                          const int32_t* __restrict__ row_map,
+                                                          const int32_t* __restrict__ topk_ids, int K, int E,
+                                                          const SmallGroupOut grp, int do_group,
+                                                          uint32_t* __restrict__ front_sync,
+                                                          const int32_t* __restrict__ src_of_padrow, int n_rows,
                                                           int I, int i_pad, uint8_t* __restrict__ h_codes,
                                                           float* __restrict__ h_gs) {
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   pdl_trigger();
   pdl_wait();
+  if (front_sync) {
+    // The all-experts path: the w13 GEMM (complete now) may have formed the
+    // rows of tokens that did not route to an expert; their maxima return to
+    // zero here (a routed row's own warp clears its word below).  Then the
+    // front kernel's counters and the GEMM's work counter return to zero.
+    const int T = n_rows / K;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < E * T; i += gridDim.x * blockDim.x) {
+      const int prow = (i / T) * 128 + i % T;
+      if (src_of_padrow[prow] < 0) row_amax[prow] = 0.0f;
+    }
+    if (blockIdx.x == 0 && threadIdx.x < 3) front_sync[threadIdx.x] = 0;
+  }
+  if (do_group && blockIdx.x == gridDim.x - 1) {
+    __shared__ unsigned long long tok_mask[256];
+    __shared__ int offs[256];
+    __shared__ int red[8];
+    small_grouping(topk_ids, n_rows / K, K, E, grp, tok_mask, offs, red);
+    return;
+  }
   if (row >= n_rows) return;
-  const int prow = pad_row_of_src[row];
+  const int prow = topk_ids ? __ldg(topk_ids + row) * 128 + row / K : row_map[row];
   const float amax = row_amax[prow];
   const float gs = nvfp4_global_scale(amax);
   const float* hr = hbuf + (size_t)prow * i_pad;
@@ -410,10 +437,16 @@ cudaError_t launch_sf_to_atoms(const uint8_t* sf, int rows, int k16, uint8_t* at
   return cudaGetLastError();
 }
 
-cudaError_t launch_requant_rows(const float* hbuf, float* row_amax, const int32_t* pad_row_of_src, int n_rows,
+cudaError_t launch_requant_rows(const float* hbuf, float* row_amax, const int32_t* row_map,
+                                const int32_t* topk_ids, int K, int E, const SmallGroupOut* grouping,
+                                uint32_t* front_sync, const int32_t* src_of_padrow, int n_rows,
                                 int I, int i_pad, uint8_t* h_codes, float* h_gs, cudaStream_t s) {
-  return launch_k(requant_rows_kernel, dim3((n_rows + 7) / 8), dim3(256), 0, s, true, hbuf, row_amax, pad_row_of_src,
-                  n_rows, I, i_pad, h_codes, h_gs);
+  if (grouping && (!topk_ids || E > 256 || n_rows / K > 64)) return cudaErrorInvalidValue;
+  if (front_sync && (!topk_ids || !src_of_padrow)) return cudaErrorInvalidValue;
+  const SmallGroupOut g = grouping ? *grouping : SmallGroupOut{};
+  const unsigned grid = (n_rows + 7) / 8 + (grouping ? 1 : 0);
+  return launch_k(requant_rows_kernel, dim3(grid), dim3(256), 0, s, true, hbuf, row_amax, row_map, topk_ids, K, E,
+                  g, grouping ? 1 : 0, front_sync, src_of_padrow, n_rows, I, i_pad, h_codes, h_gs);
 }
 
 cudaError_t launch_finalize_atomic(const float* out_acc, const uint16_t* shared, float shared_scale, void* out, int T,

@@ -12,6 +12,7 @@
 #include <type_traits>
 
 #include "common.cuh"
+#include "grouping.cuh"
 #include "kernels.h"
 
 namespace moe {
@@ -53,7 +54,7 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
 // memory round trip; H <= 2048), for small token counts where latency rules.
 // Ends with a __syncthreads-free store of the logits; the caller may reuse
 // the shared memory only after its own barrier.
-template <int TB, int EB, bool XALL, bool XSMEM = false>
+template <int TB, int EB, bool XALL>
 __device__ __forceinline__ void router_tile(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ wg,
                                             const float* __restrict__ bias, float* __restrict__ logits, int T,
                                             int H, int E) {
@@ -76,22 +77,6 @@ __device__ __forceinline__ void router_tile(const __nv_bfloat16* __restrict__ x,
       asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + 16 * u) : "memory");
     }
   }
-  // XSMEM: the CTA's activation rows [8*TB tokens][H] are staged after the
-  // weight slice (rows past T are zero), so all operands arrive in one round
-  // trip and the round loop below can stay rolled.
-  uint4* sx = sw + (size_t)H * EB * 2 / 16;
-  if constexpr (XSMEM) {
-    const int cpr = H / 8;  // 16-byte chunks per row
-    const int tb0 = blockIdx.x * ROUTER_WARPS * TB;
-    for (int idx = threadIdx.x; idx < ROUTER_WARPS * TB * cpr; idx += 256) {
-      const int r = idx / cpr, c = idx - r * cpr;
-      const int tok = tb0 + r;
-      const uint32_t dst = smem_u32(&sx[idx]);
-      const __nv_bfloat16* src = x + (size_t)(tok < T ? tok : 0) * H + 8 * c;
-      const int nbytes = tok < T ? 16 : 0;  // zero fill
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(nbytes) : "memory");
-    }
-  }
   asm volatile("cp.async.commit_group;" ::: "memory");
 
   auto load_x = [&](int j, uint4 (&xv)[TB]) {
@@ -104,8 +89,7 @@ __device__ __forceinline__ void router_tile(const __nv_bfloat16* __restrict__ x,
   };
   constexpr int XR = XALL ? 8 : 2;              // rounds of activations held in registers
   uint4 xb[XR][TB];
-  if constexpr (XSMEM) {
-  } else if constexpr (XALL) {
+  if constexpr (XALL) {
 #pragma unroll
     for (int j = 0; j < XR; ++j)
       if (j < rounds) load_x(j, xb[j]);
@@ -145,15 +129,7 @@ __device__ __forceinline__ void router_tile(const __nv_bfloat16* __restrict__ x,
     }
   };
 
-  if constexpr (XSMEM) {
-    const int cpr = H / 8;
-#pragma unroll 1
-    for (int j = 0; j < rounds; ++j) {
-#pragma unroll
-      for (int t = 0; t < TB; ++t) xb[0][t] = sx[(warp * TB + t) * cpr + j * 32 + lane];
-      round_fma(j, xb[0]);
-    }
-  } else if constexpr (XALL) {
+  if constexpr (XALL) {
 #pragma unroll
     for (int j = 0; j < XR; ++j)
       if (j < rounds) round_fma(j, xb[j]);
@@ -269,7 +245,8 @@ __device__ __forceinline__ void topk_cas(float& va, int& ea, float& vb, int& eb)
 // returns slot j: its expert in e_lane and its weight in w_lane.  Logits are
 // read through L2 (another CTA of the same grid may have written them).  All
 // 32 lanes must call it.
-template <int NE>
+// SMEM: lrow is in shared memory (the CTA's own logits).
+template <int NE, bool SMEM = false>
 __device__ __forceinline__ void topk_warp_n(const float* __restrict__ lrow, int E, int K, int lane, int& e_lane,
                                             float& w_lane) {
   float raw[NE], v[NE];
@@ -277,7 +254,7 @@ __device__ __forceinline__ void topk_warp_n(const float* __restrict__ lrow, int 
 #pragma unroll
   for (int i = 0; i < NE; ++i) {
     const int e = lane + 32 * i;
-    raw[i] = e < E ? __ldcg(lrow + e) : -INFINITY;
+    raw[i] = e < E ? (SMEM ? lrow[e] : __ldcg(lrow + e)) : -INFINITY;
     v[i] = raw[i];
     id[i] = e < E ? e : 0x7fffffff;  // padding sorts last
   }
@@ -340,10 +317,11 @@ __device__ __forceinline__ void topk_warp_n(const float* __restrict__ lrow, int 
   w_lane = pj / psum;
 }
 
+template <bool SMEM = false>
 __device__ __forceinline__ void topk_warp(const float* __restrict__ lrow, int E, int K, int lane, int& e_lane,
                                           float& w_lane) {
-  if (E <= 128) topk_warp_n<4>(lrow, E, K, lane, e_lane, w_lane);
-  else topk_warp_n<8>(lrow, E, K, lane, e_lane, w_lane);
+  if (E <= 128) topk_warp_n<4, SMEM>(lrow, E, K, lane, e_lane, w_lane);
+  else topk_warp_n<8, SMEM>(lrow, E, K, lane, e_lane, w_lane);
 }
 
 // One warp per token: the top-k choice and weights, and the per-expert row
@@ -376,28 +354,6 @@ __device__ __forceinline__ int block_sum_int(int v, int* red) {
   int tot = 0;
   for (int w = 0; w < nw; ++w) tot += red[w];
   return tot;
-}
-
-// Exclusive scan of v over the block; returns this thread's prefix, total in *tot.
-__device__ __forceinline__ int block_excl_scan(int v, int* red, int* tot) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  int incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += n;
-  }
-  __syncthreads();
-  if (lane == 31) red[warp] = incl;
-  __syncthreads();
-  int base = 0, all = 0;
-  for (int w = 0; w < nw; ++w) {
-    const int r = red[w];
-    if (w < warp) base += r;
-    all += r;
-  }
-  *tot = all;
-  return base + incl - v;
 }
 
 constexpr int PERM_THREADS = 512;
@@ -523,143 +479,307 @@ __global__ void __launch_bounds__(PERM_THREADS) permute_kernel(const int32_t* __
   }
 }
 
-// Small-batch front end, one launch: router logits, per-token quantization,
-// top-k, and the expert grouping.  Grid and tiles are the router's.
-//  1. every CTA computes its (token block, expert block) logits, and
-//     quantizes its share of the token block's rows into the shared
-//     activation tile (row t = token t);
-//  2. the last CTA of a token block to finish (an acquire-release counter)
-//     takes the top-k of the block's tokens and writes, for every expert e,
-//     the padded row e*128 + t's source (token * K + slot, or -1);
-//  3. the last CTA of the grid derives the expert grouping from all top-k
-//     ids: offsets, the stable token-order permutation, and one GEMM tile
-//     per expert with rows.
-// Counters are returned to zero by the CTA that consumed them.  No CTA ever
-// waits for another.
-template <int TB, int EB, bool XSMEM>
-__global__ void __launch_bounds__(256) front_small_kernel(const FrontArgs p) {
-  extern __shared__ uint4 front_smem[];
+// Per-token NVFP4 quantization of token t into row t of the shared
+// small-batch activation tile, by one warp: the row's global scale (or the
+// calibrated per-tensor scale of the static contract), then each lane's
+// 16-element blocks.
+// xr: the token's H bf16 values (shared or global memory).
+__device__ __forceinline__ void quantize_token_row(const uint4* xr, int t, int H,
+                                                   const float* __restrict__ static_gs, uint8_t* __restrict__ a_codes,
+                                                   float* __restrict__ gs_rows, int lane) {
+  const int nblk = H / SF_VEC;
+  float gs;
+  if (static_gs) {
+    gs = __ldg(static_gs);
+  } else {
+    float amax = 0.0f;
+    for (int b = lane; b < nblk; b += 32) {
+      float v[16];
+      bf16x16_to_f32(xr[2 * b], xr[2 * b + 1], v);
+#pragma unroll
+      for (int q = 0; q < 16; ++q) amax = fmaxf(amax, fabsf(v[q]));
+    }
+    amax = warp_max(amax);
+    gs = nvfp4_global_scale(amax);
+  }
+  for (int b0 = 0; b0 < nblk; b0 += 32) {  // nblk % 16 == 0: uniform bound
+    const int b = b0 + lane;
+    uint2 packed = make_uint2(0u, 0u);
+    uint32_t sf = 0;
+    if (b < nblk) {
+      float v[16];
+      bf16x16_to_f32(xr[2 * b], xr[2 * b + 1], v);
+      sf = nvfp4_quant_block16(v, gs, packed);
+    }
+    // blocks 4m..4m+3 have consecutive scale bytes: one 32-bit store
+    const uint32_t sf4 = sf | (__shfl_down_sync(0xffffffffu, sf, 1) << 8) | (__shfl_down_sync(0xffffffffu, sf, 2) << 16) |
+                         (__shfl_down_sync(0xffffffffu, sf, 3) << 24);
+    if (b < nblk) {
+      *reinterpret_cast<uint2*>(a_codes + operand_offset(t, 8 * b, H / 2)) = packed;
+      if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(a_codes + sf_atom_offset(t, b, nblk)) = sf4;
+    }
+  }
+  if (lane == 0) gs_rows[t] = gs;
+}
+
+// Stages of the front kernel's router-weight ring: one round of the
+// canonical order (256 rows of H, every expert) per stage, double-buffered
+// while two stages fit; each row padded by 16 bytes.
+__host__ __device__ constexpr int front_ring_buffers(int E) { return E <= 128 ? 2 : 1; }
+__host__ __device__ constexpr int front_row_stride(int E) { return 2 * E + 16; }
+__host__ __device__ constexpr int front_stage_bytes(int E) { return 32 * 9 * front_row_stride(E); }
+
+// Small-batch front end (at most 64 tokens), one launch with no hand-off
+// between CTAs on the path the expert GEMMs wait for.  CTA b takes tokens
+// TPC*b .. TPC*b + TPC - 1 over all E experts:
+//  1. router logits in the canonical order: the router weight streams
+//     through a shared-memory ring, one round of the 32 partials (256 rows
+//     of H) per stage; warp w holds the partials of expert units
+//     [w*UPW, w*UPW + UPW) (8 experts each) for all the CTA's tokens, lane p
+//     partial p; then the pairwise tree over the partials;
+//  2. per-token NVFP4 quantization of its tokens into the shared activation
+//     tile (row t = token t), and the clearing of their FP32 output rows for
+//     the atomic finalize;
+//  3. top-k of each of its tokens (one warp per token) from the logits in
+//     shared memory, and every expert's padded-row source for its tokens:
+//     src_of_padrow[e*128 + t] = t*K + slot, or -1;
+//  4. unless the GEMMs run the all-experts schedule, the last CTA of the grid
+//     to finish (an acquire-release counter, returned to zero) derives the
+//     expert grouping from all top-k ids; with that schedule the grouping is
+//     left to an extra CTA of the requantization kernel.
+// A stage holds round j of the router weight: chunk p (Wg rows 256 j + 8 p
+// .. + 7, all E experts) at p * 9 (2E + 16) bytes, row k of the chunk at
+// k (2E + 16) bytes within it (the padding is never read).  Lane p reads
+// chunk p, so the 8 lanes of one shared-memory wavefront hit distinct banks.
+template <int TPC, int UPW>
+__global__ void __launch_bounds__(256, 1) front_small_kernel(const __grid_constant__ FrontArgs p) {
+  extern __shared__ __align__(128) uint8_t front_smem[];
   __shared__ int red[ROUTER_WARPS];
   __shared__ int last;
-  constexpr int TOK = ROUTER_WARPS * TB;  // tokens per token block
+  __shared__ int chosen[TPC][16];
+  __shared__ uint64_t ring_full[2];
+  __shared__ uint64_t x_full;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = p.T, H = p.H, E = p.E, K = p.K;
-  const int tb0 = blockIdx.x * TOK;
+  const int t0 = blockIdx.x * TPC;
+  const int units = E / 8;
+  const int rounds = H / 256;
+  const int nbuf = front_ring_buffers(E);
+  const int row_bytes = 2 * E, row_stride = front_row_stride(E);
+  const int chunk_stride = 9 * row_stride;  // 8 rows of a chunk plus one padding row
+  const int stage_bytes = front_stage_bytes(E);
+  float* slog = reinterpret_cast<float*>(front_smem + (size_t)nbuf * stage_bytes);  // [TPC][E]
+  // the CTA's activation rows [TPC][H] bf16, after the logits
+  const uint4* sx = reinterpret_cast<const uint4*>(front_smem + (size_t)nbuf * stage_bytes + TPC * E * 4);
   const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(p.x);
-  // The w13 GEMM may launch now and stage weights; it reads this kernel's
+  const char* wg = reinterpret_cast<const char*>(p.gate_w);
+  // The w13 GEMM may launch now and stream weights; it reads this kernel's
   // outputs only after its dependency wait.
   pdl_trigger();
-  // Padded row e*128 + t of this CTA's experts and tokens starts as "not
-  // routed here"; the top-k phase marks the K chosen ones after this CTA's
-  // release of the token block's counter.
-  if (threadIdx.x < EB * TOK) {
-    const int e = blockIdx.y * EB + threadIdx.x / TOK, t = tb0 + threadIdx.x % TOK;
-    if (t < T) p.src_of_padrow[e * 128 + t] = -1;
+  const int ntok = min(TPC, T - t0);
+  if (threadIdx.x == 0) {
+    mbar_init(&ring_full[0], 1);
+    mbar_init(&ring_full[1], 1);
+    mbar_init(&x_full, 1);
+    fence_mbarrier_init();
+    // the CTA's token rows, whole, with one bulk copy each
+    mbar_arrive_expect_tx(&x_full, ntok * H * 2);
+    for (int t = 0; t < ntok; ++t)
+      bulk_load(const_cast<uint4*>(sx) + (size_t)t * H / 8, x + (size_t)(t0 + t) * H, H * 2, &x_full);
   }
-  router_tile<TB, EB, false, XSMEM>(x, reinterpret_cast<const __nv_bfloat16*>(p.gate_w), p.bias, p.logits, T, H,
-                                     E);
+  __syncthreads();
 
-  // 1b. per-token NVFP4 quantization (one warp per token)
-  const int nblk = H / SF_VEC;
-  for (int i = blockIdx.y + gridDim.y * warp; i < TOK; i += gridDim.y * ROUTER_WARPS) {
-    const int t = tb0 + i;
-    if (t >= T) break;
-    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
-    float gs;
-    if (p.static_gs) {  // static per-tensor contract: the calibrated scale
-      gs = __ldg(p.static_gs);
-    } else {
-      float amax = 0.0f;
-      for (int b = lane; b < nblk; b += 32) {
-        float v[16];
-        bf16x16_to_f32(__ldg(xr + 2 * b), __ldg(xr + 2 * b + 1), v);
+  // Warp 0 fills stage buffer b with round j.  With the tensor map: one
+  // tensor copy of the round's 32 chunks x 8 rows x E experts, whose box (one
+  // row and 8 columns wider than the data) pads every row with 16 zero bytes
+  // and every chunk with one zero row.  Without it: 256 bulk copies of one
+  // row each into the same layout.
+  const bool use_map = p.wg_map_ok != 0;
+  auto stage = [&](int j, int b) {
+    if (warp != 0) return;
+    uint8_t* dst = front_smem + (size_t)b * stage_bytes;
+    if (use_map) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&ring_full[b], stage_bytes);
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+            "l"(reinterpret_cast<uint64_t>(&p.wg_map)), "r"(0), "r"(0), "r"(j * 32), "r"(smem_u32(&ring_full[b]))
+            : "memory");
+      }
+      return;
+    }
+    if (lane == 0) mbar_arrive_expect_tx(&ring_full[b], 256 * row_bytes);
+    __syncwarp();
+    for (int hr = lane; hr < 256; hr += 32)
+      bulk_load(dst + (hr >> 3) * chunk_stride + (hr & 7) * row_stride, wg + ((size_t)j * 256 + hr) * row_bytes,
+                row_bytes, &ring_full[b]);
+  };
+  stage(0, 0);
+  if (nbuf == 2 && rounds > 1) stage(1, 1);
+  const int ubase = warp * UPW;
+  float2 acc[TPC][UPW * 4];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) amax = fmaxf(amax, fabsf(v[q]));
-      }
-      amax = warp_max(amax);
-      gs = nvfp4_global_scale(amax);
+  for (int t = 0; t < TPC; ++t)
+#pragma unroll
+    for (int i = 0; i < UPW * 4; ++i) acc[t][i] = make_float2(0.0f, 0.0f);
+  bool ring_ok = true;
+  if (!mbar_wait_bounded(&x_full, 0, nullptr)) {
+    if (threadIdx.x == 0) report_device_error(p.status, DEV_ERR_TIMEOUT);
+    ring_ok = false;
+  }
+  // per-token quantization first (warps 0 .. TPC-1, from the staged rows):
+  // the w13 GEMM needs only the activations to start its MMAs
+  if (warp < ntok) quantize_token_row(sx + (size_t)warp * H / 8, t0 + warp, H, p.static_gs, p.a_codes, p.gs_rows, lane);
+  if (p.all_experts) {
+    __syncthreads();
+    if (threadIdx.x == 0) arrive_acq_rel_gpu(&p.sync[FRONT_SYNC_A_READY]);
+  }
+  for (int j = 0; j < rounds; ++j) {
+    const int b = nbuf == 2 ? (j & 1) : 0;
+    const uint32_t parity = (nbuf == 2 ? (j >> 1) : j) & 1;
+    if (!mbar_wait_bounded(&ring_full[b], parity, nullptr)) {
+      // the copy did not land in time: report it; the results are garbage
+      // but every thread still leaves
+      if (ring_ok && threadIdx.x == 0) report_device_error(p.status, DEV_ERR_TIMEOUT);
+      ring_ok = false;
     }
-    for (int b0 = 0; b0 < nblk; b0 += 32) {  // nblk % 16 == 0: uniform bound
-      const int b = b0 + lane;
-      uint2 packed = make_uint2(0u, 0u);
-      uint32_t sf = 0;
-      if (b < nblk) {
-        float v[16];
-        bf16x16_to_f32(__ldg(xr + 2 * b), __ldg(xr + 2 * b + 1), v);
-        sf = nvfp4_quant_block16(v, gs, packed);
+    // this lane's 8-element chunk of round j (chunk j*32 + lane) of each token
+    uint4 xc[TPC];
+#pragma unroll
+    for (int t = 0; t < TPC; ++t) xc[t] = t < ntok ? sx[(size_t)t * H / 8 + j * 32 + lane] : make_uint4(0, 0, 0, 0);
+    // lane p reads chunk p: its rows k = 0..7 (the chunks are 9 (2E + 16)
+    // bytes apart, so the 8 lanes of a wavefront hit distinct banks)
+    const uint8_t* sb = front_smem + (size_t)b * stage_bytes + lane * chunk_stride + ubase * 16;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      float2 x2[TPC];
+#pragma unroll
+      for (int t = 0; t < TPC; ++t) {
+        const uint32_t w32 = (k < 2) ? xc[t].x : (k < 4) ? xc[t].y : (k < 6) ? xc[t].z : xc[t].w;
+        const float xf = (k & 1) ? bf16_hi(w32) : bf16_lo(w32);
+        x2[t] = make_float2(xf, xf);
       }
-      // blocks 4m..4m+3 have consecutive scale bytes: one 32-bit store
-      const uint32_t sf4 = sf | (__shfl_down_sync(0xffffffffu, sf, 1) << 8) |
-                           (__shfl_down_sync(0xffffffffu, sf, 2) << 16) | (__shfl_down_sync(0xffffffffu, sf, 3) << 24);
-      if (b < nblk) {
-        *reinterpret_cast<uint2*>(p.a_codes + operand_offset(t, 8 * b, H / 2)) = packed;
-        if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(p.a_codes + sf_atom_offset(t, b, nblk)) = sf4;
+#pragma unroll
+      for (int i = 0; i < UPW; ++i) {
+        if (ubase + i < units) {  // warp-uniform
+          const uint4 wv = *reinterpret_cast<const uint4*>(sb + k * row_stride + i * 16);
+          const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 w2 = make_float2(bf16_lo(ww[q]), bf16_hi(ww[q]));  // experts 8u+2q, 8u+2q+1
+#pragma unroll
+            for (int t = 0; t < TPC; ++t) acc[t][i * 4 + q] = fma2(x2[t], w2, acc[t][i * 4 + q]);
+          }
+        }
       }
     }
-    if (lane == 0) p.gs_rows[t] = gs;
-    if (p.out_acc) {
-      float4* o = reinterpret_cast<float4*>(p.out_acc + (size_t)t * H);
-      for (int q = lane; q < H / 4; q += 32) o[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    __syncthreads();  // buffer b is free again
+    if (warp == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (nbuf == 2) {
+      if (j + 2 < rounds) stage(j + 2, b);
+    } else if (j + 1 < rounds) {
+      stage(j + 1, 0);
     }
   }
 
-  // 2. top-k, by the last CTA of the token block
+  // Pairwise tree over the 32 partials; value index (t * UPW + i) * 8 + c is
+  // token t0 + t, expert 8 (ubase + i) + c.
+  constexpr int NV = TPC * UPW * 8;
+  float v[NV];
+#pragma unroll
+  for (int t = 0; t < TPC; ++t)
+#pragma unroll
+    for (int i = 0; i < UPW * 4; ++i) {
+      v[t * UPW * 8 + 2 * i] = acc[t][i].x;
+      v[t * UPW * 8 + 2 * i + 1] = acc[t][i].y;
+    }
+  auto put_logit = [&](int idx, float l) {
+    const int t = idx / (UPW * 8), rest = idx % (UPW * 8);
+    const int u = ubase + rest / 8, e = 8 * u + rest % 8;
+    if (u < units && t0 + t < T) {
+      if (p.bias) l = __fadd_rn(l, p.bias[e]);
+      slog[t * E + e] = l;
+      p.logits[(size_t)(t0 + t) * E + e] = l;
+    }
+  };
+  if constexpr (NV < 32) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int i = 0; i < NV; ++i) v[i] = __fadd_rn(v[i], __shfl_xor_sync(0xffffffffu, v[i], o));
+    float mine = v[0];
+#pragma unroll
+    for (int i = 1; i < NV; ++i)
+      if (lane == i) mine = v[i];
+    if (lane < NV) put_logit(lane, mine);
+  } else {
+#pragma unroll
+    for (int lvl = 0; lvl < 5; ++lvl) {
+      const int o = 16 >> lvl;
+      const int half = NV >> (lvl + 1);
+      const bool upper = (lane & o) != 0;
+#pragma unroll
+      for (int i = 0; i < half; ++i) {
+        const float send = upper ? v[i] : v[half + i];
+        const float keep = upper ? v[half + i] : v[i];
+        const float recv = __shfl_xor_sync(0xffffffffu, send, o);
+        v[i] = __fadd_rn(keep, recv);
+      }
+    }
+    constexpr int M = NV / 32;
+#pragma unroll
+    for (int i = 0; i < M; ++i) put_logit(lane * M + i, v[i]);
+  }
   __syncthreads();
-  if (threadIdx.x == 0) last = arrive_acq_rel_gpu(&p.sync[blockIdx.x]) == gridDim.y - 1;
-  __syncthreads();
-  if (last) {
-    for (int i = warp; i < TOK; i += ROUTER_WARPS) {
-      const int t = tb0 + i;
-      if (t >= T) break;
+
+  // top-k (warps 0 .. TPC-1) and the atomic finalize's row clearing (warps
+  // 6, 7), in parallel
+  if (warp < TPC) {
+    const int t = t0 + warp;
+    if (t < T) {
       int e_lane;
       float w;
-      topk_warp(p.logits + (size_t)t * E, E, K, lane, e_lane, w);
+      topk_warp<true>(slog + warp * E, E, K, lane, e_lane, w);
       if (lane < K) {
         p.topk_ids[(size_t)t * K + lane] = e_lane;
         p.topk_w[(size_t)t * K + lane] = w;
-        p.src_of_padrow[e_lane * 128 + t] = t * K + lane;  // the other experts' rows hold -1
+        chosen[warp][lane] = e_lane;
       }
     }
-    if (threadIdx.x == 0) p.sync[blockIdx.x] = 0;
+  } else if (warp >= 6 && p.out_acc) {
+    for (int t = t0; t < min(t0 + TPC, T); ++t) {
+      float4* o = reinterpret_cast<float4*>(p.out_acc + (size_t)t * H);
+      for (int q = (warp - 6) * 32 + lane; q < H / 4; q += 64) o[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < TPC * E; i += blockDim.x) {
+    const int t = i / E, e = i - t * E, tok = t0 + t;
+    if (tok < T) {
+      int src = -1;
+      for (int j = 0; j < K; ++j)
+        if (chosen[t][j] == e) src = tok * K + j;
+      p.src_of_padrow[e * 128 + tok] = src;
+    }
+  }
+  if (p.all_experts) {
+    // routing (and the row clearing) published: the w13 GEMM completes only
+    // after every front CTA got here
+    __syncthreads();
+    if (threadIdx.x == 0) arrive_acq_rel_gpu(&p.sync[FRONT_SYNC_ROUTED]);
+    return;
   }
 
-  // 3. the expert grouping, by the last CTA of the grid
+  // the expert grouping, by the last CTA of the grid
   __syncthreads();
-  if (threadIdx.x == 0) last = arrive_acq_rel_gpu(&p.sync[FRONT_SYNC_WORDS - 1]) == gridDim.x * gridDim.y - 1;
+  if (threadIdx.x == 0) last = arrive_acq_rel_gpu(&p.sync[FRONT_SYNC_WORDS - 1]) == gridDim.x - 1;
   __syncthreads();
   if (!last) return;
-  // T <= 64: the tokens that chose expert e form one 64-bit mask, so counts
-  // and the stable (token-order) rank of every row are population counts.
-  unsigned long long* tok_mask = reinterpret_cast<unsigned long long*>(front_smem);  // [E]
-  int* offs = reinterpret_cast<int*>(tok_mask + 256);                                // [E]
-  const int n = T * K;
-  const int e = threadIdx.x;  // E <= 256 = blockDim.x
-  if (e < E) tok_mask[e] = 0ull;
-  __syncthreads();
-  for (int i = threadIdx.x; i < n; i += blockDim.x)
-    atomicOr(&tok_mask[__ldcg(p.topk_ids + i)], 1ull << (i / K));
-  __syncthreads();
-  const int cnt = e < E ? __popcll(tok_mask[e]) : 0;
-  int total, touched;
-  const int off = block_excl_scan(cnt, red, &total);
-  const int tix = block_excl_scan(cnt > 0 ? 1 : 0, red, &touched);
-  if (e < E) {
-    offs[e] = off;
-    p.expert_offsets[e] = off;
-    if (e == E - 1) {
-      p.expert_offsets[E] = off + cnt;
-      p.num_tiles[0] = touched;
-    }
-    if (cnt > 0) p.tiles[tix] = make_int4(e, e * 128, T, 0);
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const int ei = __ldcg(p.topk_ids + i), t = i / K;
-    const int r = offs[ei] + __popcll(tok_mask[ei] & ((1ull << t) - 1ull));
-    p.src_of_row[r] = i;
-    p.row_of_src[i] = r;
-    p.pad_row_of_src[i] = ei * 128 + t;
-  }
+  unsigned long long* tok_mask = reinterpret_cast<unsigned long long*>(front_smem);  // [256] (the ring is idle)
+  int* offs = reinterpret_cast<int*>(tok_mask + 256);                                // [256]
+  const SmallGroupOut go{p.expert_offsets, p.src_of_row, p.row_of_src, p.pad_row_of_src, p.tiles, p.num_tiles};
+  small_grouping(p.topk_ids, T, K, E, go, tok_mask, offs, red);
   if (threadIdx.x == 0) p.sync[FRONT_SYNC_WORDS - 1] = 0;
 }
 
@@ -734,55 +854,117 @@ int router_smem_bytes(int H, int E) { return H * router_eb(H, E) * 2; }
 namespace {
 
 
-// Dynamic shared memory of the front kernel: the router-weight slice, plus
-// the token block's activation rows when they are staged (XSMEM).
-constexpr int FRONT_XSMEM_LIMIT = 200 * 1024;
-int front_smem_bytes(int H, int eb, int tb, bool xsmem) { return H * eb * 2 + (xsmem ? ROUTER_WARPS * tb * H * 2 : 0); }
+// Dynamic shared memory of the front kernel: the router-weight ring and the
+// CTA's logits (at least the 3 KB the grouping reuses).
+int front_smem_bytes(int H, int E, int tpc) {
+  return std::max(front_ring_buffers(E) * front_stage_bytes(E) + tpc * E * 4 + tpc * H * 2, 3 * 1024);
+}
 
-template <int TB, int EB, bool XSMEM>
-cudaError_t raise_front_attr(int H) {
-  const int bytes = front_smem_bytes(H, EB, TB, XSMEM);
+template <int TPC, int UPW>
+cudaError_t raise_front_attr(int H, int E) {
+  const int bytes = front_smem_bytes(H, E, TPC);
+  if (bytes > 227 * 1024) return cudaErrorInvalidValue;  // hidden sizes beyond 16384 at 128 experts
   cudaFuncAttributes a{};
-  cudaError_t e = cudaFuncGetAttributes(&a, front_small_kernel<TB, EB, XSMEM>);
+  cudaError_t e = cudaFuncGetAttributes(&a, front_small_kernel<TPC, UPW>);
   if (e != cudaSuccess || a.maxDynamicSharedSizeBytes >= bytes) return e;
-  return cudaFuncSetAttribute(front_small_kernel<TB, EB, XSMEM>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  return cudaFuncSetAttribute(front_small_kernel<TPC, UPW>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-template <int TB, int EB, bool XSMEM>
-cudaError_t launch_front_t(const FrontArgs& a, cudaStream_t s) {
-  dim3 grid((a.T + ROUTER_WARPS * TB - 1) / (ROUTER_WARPS * TB), a.E / EB);
-  // first kernel of a forward: ordinary stream order
-  return launch_k(front_small_kernel<TB, EB, XSMEM>, grid, dim3(256), (size_t)front_smem_bytes(a.H, EB, TB, XSMEM), s,
-                  false, a);
-}
+// Tokens per CTA: one up to 32 tokens, two above (at most 32 CTAs at 64
+// tokens, so that most SMs are free for the w13 GEMM launched behind the
+// front kernel; the GEMM is persistent with one CTA per SM and cannot share
+// an SM with a front CTA).  Expert units (8 experts) per warp: E/64 rounded
+// up to 1, 2 or 4.  Calls f with (tokens per CTA, units per warp) as types.
+int front_tpc(int T) { return T <= 32 ? 1 : 2; }
 
-// Tiles of the front kernel: 8 tokens x 8 experts per CTA (E/8 x T/8 CTAs),
-// so the operands staged per CTA stay small (32 bytes per hidden element) and
-// the last CTA of a token block takes one token per warp in the top-k phase.
-// The activation rows are staged in shared memory when they fit.  Calls f
-// with (tokens per warp, experts per CTA, staged) as types.
 template <typename F>
-cudaError_t with_front(int H, int E, F&& f) {
+cudaError_t with_front(int T, int E, F&& f) {
   using std::integral_constant;
-  if (front_smem_bytes(H, 8, 1, true) <= FRONT_XSMEM_LIMIT)
-    return f(integral_constant<int, 1>{}, integral_constant<int, 8>{}, integral_constant<bool, true>{});
-  return f(integral_constant<int, 1>{}, integral_constant<int, 8>{}, integral_constant<bool, false>{});
+  const int upw = (E / 8 + ROUTER_WARPS - 1) / ROUTER_WARPS;
+  if (front_tpc(T) == 1) {
+    if (upw <= 1) return f(integral_constant<int, 1>{}, integral_constant<int, 1>{});
+    if (upw <= 2) return f(integral_constant<int, 1>{}, integral_constant<int, 2>{});
+    return f(integral_constant<int, 1>{}, integral_constant<int, 4>{});
+  }
+  if (upw <= 1) return f(integral_constant<int, 2>{}, integral_constant<int, 1>{});
+  if (upw <= 2) return f(integral_constant<int, 2>{}, integral_constant<int, 2>{});
+  return f(integral_constant<int, 2>{}, integral_constant<int, 4>{});
+}
+
+template <int TPC, int UPW>
+cudaError_t launch_front_t(const FrontArgs& a, cudaStream_t s) {
+  // first kernel of a forward: ordinary stream order
+  return launch_k(front_small_kernel<TPC, UPW>, dim3((a.T + TPC - 1) / TPC), dim3(256),
+                  (size_t)front_smem_bytes(a.H, a.E, TPC), s, false, a);
 }
 
 }  // namespace
 
 
-cudaError_t front_setup(int H, int E) {
-  std::lock_guard<std::mutex> lock(router_attr_mutex);
-  return with_front(H, E, [&](auto tb, auto eb, auto xs) {
-    return raise_front_attr<decltype(tb)::value, decltype(eb)::value, decltype(xs)::value>(H);
-  });
+int front_ctas(int T, int E) {
+  (void)E;
+  const int tpc = front_tpc(T);
+  return (T + tpc - 1) / tpc;
 }
 
-cudaError_t launch_front_small(const FrontArgs& a, cudaStream_t s) {
-  if (a.T > SMALL_BATCH_TOKENS || a.E > 256 || a.K > 16) return cudaErrorInvalidValue;
-  return with_front(a.H, a.E, [&](auto tb, auto eb, auto xs) {
-    return launch_front_t<decltype(tb)::value, decltype(eb)::value, decltype(xs)::value>(a, s);
+cudaError_t front_setup(int H, int E) {
+  std::lock_guard<std::mutex> lock(router_attr_mutex);
+  for (int T : {1, SMALL_BATCH_TOKENS}) {
+    cudaError_t e = with_front(T, E, [&](auto tpc, auto upw) {
+      return raise_front_attr<decltype(tpc)::value, decltype(upw)::value>(H, E);
+    });
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up once through the runtime (the
+// library does not link against the driver library).
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// Router-weight map for the front kernel's ring: Wg [H][E] bf16 viewed as
+// [H/8 chunks][8 rows][E], box of 32 chunks x 9 rows x (E + 8) columns: the
+// row and the columns past the tensor are filled with zeros, which pads the
+// staged rows and chunks (no swizzle).  False when E + 8 exceeds a box (256)
+// or the encoder refuses.
+bool encode_router_map(CUtensorMap* map, const void* gate_w, int H, int E) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn || E + 8 > 256 || H % 256) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)E, 8, (cuuint64_t)H / 8};
+  const cuuint64_t strides[2] = {(cuuint64_t)E * 2, (cuuint64_t)E * 16};
+  const cuuint32_t box[3] = {(cuuint32_t)(E + 8), 9, 32};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(gate_w), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_front_small(FrontArgs& a, cudaStream_t s) {
+  if (a.T > SMALL_BATCH_TOKENS || a.E > 256 || a.K > 16 || a.H % 256) return cudaErrorInvalidValue;
+  a.wg_map_ok = encode_router_map(&a.wg_map, a.gate_w, a.H, a.E) ? 1 : 0;
+  return with_front(a.T, a.E, [&](auto tpc, auto upw) {
+    return launch_front_t<decltype(tpc)::value, decltype(upw)::value>(a, s);
   });
 }
 

@@ -16,6 +16,7 @@
 
 #include "../../include/moe_nvfp4.h"
 #include "common.cuh"
+#include "grouping.cuh"
 #include "kernels.h"
 
 using namespace moe;
@@ -175,6 +176,9 @@ int tile_rows_for(int T) { return T <= SMALL_BATCH_TOKENS ? 64 : 128; }
 // than it saved.
 constexpr int W13_PREFETCH_UNITS = 2;
 constexpr int W2_PREFETCH_UNITS = 2;
+// With the all-experts schedule the prefetched units are exactly the CTA's
+// first ones: two column pairs.
+constexpr int W13_PREFETCH_UNITS_ALL = 4;
 
 // Worst-case number of GEMM tiles of tile_rows rows when T tokens each pick
 // K of E experts (each tile is padded to its own 128-row block).
@@ -297,8 +301,8 @@ moe_status shared_branch(moe_handle* h, const void* x, int T, cudaStream_t s) {
     g.hbuf = h->s_hbuf;
     g.row_amax = h->s_row_amax;
     CK(h, launch_gemm_w13s(g, std::min(h->num_sms, g.w13_pairs), false, h->side));
-    CK(h, launch_requant_rows(h->s_hbuf, h->s_row_amax, h->s_ident, T, h->Is, h->Ipad_s, h->s_h_codes, h->s_h_gs,
-                              h->side));
+    CK(h, launch_requant_rows(h->s_hbuf, h->s_row_amax, h->s_ident, nullptr, 1, 1, nullptr, nullptr, nullptr, T,
+                              h->Is, h->Ipad_s, h->s_h_codes, h->s_h_gs, h->side));
   } else {
     CK(h, launch_gemm_w13(g, h->Is / 128, std::min(h->s_clusters[a_rows == 128], ntiles), a_rows, h->side));
   }
@@ -339,6 +343,14 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
     // their own so that the two streams overlap instead of queueing.
     const int gemm_sms = (h->Is > 0 && small) ? std::max(h->num_sms / 2, h->num_sms - shared_gemm_ctas(h))
                                               : h->num_sms;
+    // Small batches in which nearly every expert gets a row (T*K >= 4E: with
+    // uniform routing at most e^-4 of the experts stay empty) run both GEMMs
+    // over every expert in order: their weight streams need no routing
+    // result and start before the front kernel finishes, and the expert
+    // grouping moves off their path into the requantization kernel (the
+    // static contract has no requantization kernel, so it keeps the tile
+    // list).
+    const bool all_experts = small && (long)T * K >= 4L * E && !h->static_scales;
     CK(h, mark(h, 0, s));
     if (small) {
       // one kernel for router, quantization, top-k and grouping; its time is
@@ -366,6 +378,8 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
       fa.num_tiles = h->num_tiles;
       fa.sync = h->front_sync;
       fa.static_gs = h->static_scales ? h->static_x_gs : nullptr;
+      fa.all_experts = all_experts;
+      fa.status = h->status_dev;
       CK(h, launch_front_small(fa, s));
       for (int i = 1; i <= 4; ++i) CK(h, mark(h, i, s));
     } else {
@@ -384,6 +398,7 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
     }
     // bound on the tile count: one per expert with rows (small batches)
     const int tb = small ? std::min(E, T * K) : tile_bound(T, K, E, tile_rows);
+    const int units_e = all_experts ? E : tb;
     GemmArgs g{};
     g.status = h->status_dev;
     g.tiles = h->tiles;
@@ -401,7 +416,13 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
     g.i_pad = h->Ipad;
     g.src_of_padrow = h->src_of_padrow;
     g.num_experts = E;
-    g.prefetch_units = small ? W13_PREFETCH_UNITS : 0;
+    g.prefetch_units = small ? (all_experts ? W13_PREFETCH_UNITS_ALL : W13_PREFETCH_UNITS) : 0;
+    g.all_experts = all_experts;
+    g.small_T = T;
+    if (all_experts) {  // dynamic schedule on the front kernel's counters
+      g.front_sync = h->front_sync;
+      g.front_ctas = front_ctas(T, E);
+    }
     g.h_gs_static = h->static_scales ? h->static_h_gs : nullptr;
     g.accurate_sigmoid = (h->cfg.flags & MOE_FLAG_ACCURATE_SIGMOID) != 0;
     if (small) {
@@ -412,11 +433,15 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
       g.w13_pairs = h->I / 128;
       g.hbuf = h->hbuf;
       g.row_amax = h->row_amax;
-      CK(h, launch_gemm_w13s(g, std::min(gemm_sms, tb * g.w13_pairs), false, s));
+      CK(h, launch_gemm_w13s(g, std::min(gemm_sms, units_e * g.w13_pairs), false, s));
       // (with static scales the w13 epilogue has already requantized)
-      if (!h->static_scales)
-        CK(h, launch_requant_rows(h->hbuf, h->row_amax, h->pad_row_of_src, T * K, h->I, h->Ipad, h->h_codes, h->h_gs,
-                                s));
+      if (!h->static_scales) {
+        const SmallGroupOut grp{h->expert_offsets, h->src_of_row, h->row_of_src, h->pad_row_of_src, h->tiles,
+                                h->num_tiles};
+        CK(h, launch_requant_rows(h->hbuf, h->row_amax, nullptr, h->topk_ids, K, E, all_experts ? &grp : nullptr,
+                                  all_experts ? h->front_sync : nullptr, h->src_of_padrow, T * K, h->I, h->Ipad,
+                                  h->h_codes, h->h_gs, s));
+      }
     } else {
       CK(h, launch_gemm_w13(g, h->I / 128, std::min(h->w13_clusters[tile_rows == 128], tb), tile_rows, s));
     }
@@ -441,8 +466,10 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
     g2.n_tiles = H / TILE_N;
     g2.num_experts = E;
     g2.prefetch_units = small ? W2_PREFETCH_UNITS : 0;
+    g2.all_experts = all_experts;
+    g2.small_T = T;
     // units are pairs of 128-column tiles
-    CK(h, launch_gemm_w2(g2, std::min(gemm_sms, tb * g2.n_tiles / 2), ordered, tile_rows, s));
+    CK(h, launch_gemm_w2(g2, std::min(gemm_sms, units_e * g2.n_tiles / 2), ordered, tile_rows, s));
     CK(h, mark(h, 6, s));
     // the shared expert's rows join here (its stream's work is done)
     const uint16_t* shared = nullptr;

@@ -124,34 +124,80 @@ def _bf16_bits(t: torch.Tensor) -> np.ndarray:
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def oracle_forward_parallel(wl, tokens):
+class ParallelResult:
+    """Result of ``oracle_forward_parallel`` for n tokens.
+
+    out       float32 [n, H]  the oracle's forward (bf16 values widened)
+    ids       int32 [n, K]    its top-k choice
+    h_gs      {(token, slot): float32} its intermediate's global scales
+    With the GPU's intermediate given:
+    out_gpu_h float32 [n, H]  the oracle's second GEMM and finalize applied to
+                              the GPU's requantized intermediate (the same
+                              requantization decisions on both sides)
+    h_gs_gpu, h_gs_ref float32 [n, K]  the two sides' intermediate global scales
+    flipped   bool [n, K]     rows whose intermediate codes or block scales
+                              differ from the oracle's
+    flipped_blocks, blocks    16-element blocks that differ, and all blocks
+    """
+
+
+def oracle_forward_parallel(wl, tokens, h_gpu=None):
     """``oracle_forward(wl, tokens)`` (per-token scales) computed expert by
     expert in worker processes: routing, per-token quantization and the
     finalize here, each expert's weight quantization and GEMMs in a worker
-    (``tests/oracle_jobs.py``).  Returns (out float32 [n, H] - the bf16
-    output widened, ids [n, K], h_gs {(token, slot): float32})."""
+    (``tests/oracle_jobs.py``).
+
+    ``h_gpu``: optionally the GPU's requantized intermediate of the whole
+    batch, (packed codes [T*K, I/2], block scales [T*K, I/16], global scales
+    [T*K]) indexed by token * K + slot (``MoE.debug_intermediate``).
+    Returns a ``ParallelResult``."""
     from tests import oracle_jobs
 
     tok = np.asarray(tokens, dtype=np.int64)
-    K = wl.shape.K
+    K, H = wl.shape.K, wl.shape.H
     _, ids, w = oracle_route(wl, tok)
     xs = omoe.as_f32(wl.x)[tok]
     codes, sf, gs = onv.quantize_rows(xs)
+    if h_gpu is not None:
+        hc_all, hs_all, hg_all = (np.asarray(a) for a in h_gpu)
     jobs, where = [], []
     for e in np.unique(ids):
         sel_t, sel_j = np.nonzero(ids == e)          # token-ascending, as the oracle's forward
-        jobs.append((_bf16_bits(wl.w13[int(e)]), _bf16_bits(wl.w2[int(e)]), codes[sel_t], sf[sel_t], gs[sel_t]))
+        hj = None
+        if h_gpu is not None:
+            src = tok[sel_t] * K + sel_j
+            hj = (onv.unpack_e2m1(hc_all[src]), hs_all[src], hg_all[src])
+        jobs.append((_bf16_bits(wl.w13[int(e)]), _bf16_bits(wl.w2[int(e)]), codes[sel_t], sf[sel_t], gs[sel_t], hj))
         where.append((sel_t, sel_j))
     results = list(_pool().map(oracle_jobs.expert_job, jobs)) if len(jobs) > 1 else \
         [oracle_jobs.expert_job(j) for j in jobs]
-    y_rows = np.zeros((len(tok), K, wl.shape.H), np.float32)
-    h_gs = {}
-    for (sel_t, sel_j), (y2, hg) in zip(where, results):
-        y_rows[sel_t, sel_j] = y2
+    n = len(tok)
+    y_rows = np.zeros((n, K, H), np.float32)
+    res = ParallelResult()
+    res.ids, res.h_gs = ids, {}
+    if h_gpu is not None:
+        y_gpu = np.zeros((n, K, H), np.float32)
+        res.h_gs_ref = np.zeros((n, K), np.float32)
+        res.h_gs_gpu = hg_all[tok[:, None] * K + np.arange(K)[None, :]].astype(np.float32)
+        res.flipped = np.zeros((n, K), bool)
+        res.flipped_blocks = res.blocks = 0
+    for (sel_t, sel_j), r, job in zip(where, results, jobs):
+        y_rows[sel_t, sel_j] = r["y2"]
         for i, (t, j) in enumerate(zip(sel_t, sel_j)):
-            h_gs[(int(tok[t]), int(j))] = hg[i]
-    out = onv.bf16_to_f32(onv.bf16_round(omoe.finalize(y_rows, w)))
-    return out, ids, h_gs
+            res.h_gs[(int(tok[t]), int(j))] = r["h_gs"][i]
+        if h_gpu is not None:
+            y_gpu[sel_t, sel_j] = r["y2_gpu_h"]
+            res.h_gs_ref[sel_t, sel_j] = r["h_gs"]
+            gc, gsf, _ = job[5]
+            nb = gsf.shape[1]
+            blk = (gc != r["h_codes"]).reshape(len(sel_t), nb, 16).any(2) | (gsf != r["h_sf"])
+            res.flipped[sel_t, sel_j] = blk.any(1)
+            res.flipped_blocks += int(blk.sum())
+            res.blocks += blk.size
+    res.out = onv.bf16_to_f32(onv.bf16_round(omoe.finalize(y_rows, w)))
+    if h_gpu is not None:
+        res.out_gpu_h = onv.bf16_to_f32(onv.bf16_round(omoe.finalize(y_gpu, w)))
+    return res
 
 
 def tile_covering_tokens(ids: np.ndarray, num_experts: int, tile_rows: int = 128):

@@ -80,10 +80,34 @@ def _check_weight_quant(layer, wl, experts):
             assert gs[e] == q.gs[e], f"weight global scale {which} expert {e}"
 
 
-def _check_output(out, wl, tokens, what):
-    ref, _, _ = oracle_forward_parallel(wl, tokens)
+# Requantization decisions of the intermediate are not bit-exact targets (the
+# GPU sums in FP32 on the tensor cores and forms SwiGLU in FP32, the oracle
+# in FP64): a block whose maximum or an element sits within that difference
+# of an E4M3 or E2M1 rounding boundary can take the neighbouring code.  Such
+# blocks must stay this rare.
+MAX_FLIPPED_BLOCK_FRACTION = 2e-3
+
+
+def _check_output(out, wl, tokens, what, layer):
+    """The output of the tokens against the oracle, with the intermediate's
+    requantization decisions separated:
+    * the intermediate's global scales agree (rtol 1e-4) and blocks whose
+      codes or scale differ from the oracle's are rare;
+    * every token's output equals, within the tolerance, the oracle's second
+      GEMM and finalize applied to the GPU's own intermediate (the same
+      decisions on both sides);
+    * every token whose K intermediate rows all match the oracle's exactly
+      equals the oracle's whole forward within the tolerance."""
+    h = tuple(t.cpu().numpy() for t in layer.debug_intermediate())
+    res = oracle_forward_parallel(wl, tokens, h_gpu=h)
     got = out.float().cpu().numpy()[np.asarray(tokens)]
-    return assert_close(got, ref, what=what)
+    np.testing.assert_allclose(res.h_gs_gpu, res.h_gs_ref, rtol=1e-4, err_msg=f"{what}: intermediate global scales")
+    tok_flipped = res.flipped.any(1)
+    print(f"\n{what}: intermediate blocks differing from the oracle {res.flipped_blocks}/{res.blocks}, "
+          f"rows {int(res.flipped.sum())}/{res.flipped.size}, tokens {int(tok_flipped.sum())}/{len(tok_flipped)}")
+    assert res.flipped_blocks <= max(4, MAX_FLIPPED_BLOCK_FRACTION * res.blocks), f"{what}: too many flipped blocks"
+    assert_close(got, res.out_gpu_h, what=f"{what} (downstream of the GPU intermediate)")
+    return assert_close(got[~tok_flipped], res.out[~tok_flipped], what=f"{what} (tokens whose intermediate matches)")
 
 
 def test_decode_graph_replay():
@@ -107,9 +131,9 @@ def test_decode_graph_replay():
     _check_routing(layer, wl, full_permutation=True)
     _check_act_quant(layer, wl)
     tokens = np.arange(wl.T)
-    _check_output(replay, wl, tokens, "graph replay")
+    _check_output(replay, wl, tokens, "graph replay", layer)
     if not torch.equal(eager, replay):  # the atomic finalize adds in arrival order
-        _check_output(eager, wl, tokens, "eager")
+        _check_output(eager, wl, tokens, "eager", layer)
     _check_weight_quant(layer, wl, [0, 77, 127])
     layer.close()
 
@@ -129,7 +153,7 @@ def test_specdecode_deterministic_zipf():
     assert (counts == 0).sum() >= 4, "skewed routing should leave experts without rows"
     assert counts.max() > 4 * counts.mean()
     _check_act_quant(layer, wl, what="zipf deterministic activations")
-    _check_output(outs[0], wl, np.arange(wl.T), "zipf deterministic")
+    _check_output(outs[0], wl, np.arange(wl.T), "zipf deterministic", layer)
 
 
 def test_prefill_token_sweep_one_instance():
@@ -155,7 +179,7 @@ def test_prefill_token_sweep_one_instance():
         else:  # the whole batch: every token's route and the full permutation
             ids, _ = _check_routing(layer, wlT, None, full_permutation=True)
             tokens = np.arange(T) if T <= 256 else tile_covering_tokens(ids, shape.E)
-        _check_output(out, wlT, tokens, f"T={T}")
+        _check_output(out, wlT, tokens, f"T={T}", layer)
     assert layer.debug_buffer_ptrs() == ptrs, "a forward moved a device buffer"
     with pytest.raises(MoEError) as ei:
         layer.forward(torch.zeros(4097, shape.H, dtype=torch.bfloat16, device="cuda"), gate)
@@ -221,6 +245,6 @@ def test_stress_refresh_replay_equals_fresh():
     _, ids_all, _ = oracle_route(wl)
     tokens = np.union1d(tile_covering_tokens(ids_all, shape.E), extra)
     wl_b = synthetic.Workload(shape=shape, x=wl.x, gate_w=wl.gate_w, w13=w13_b, w2=w2_b, bias=None)
-    _check_output(refreshed, wl_b, tokens, "stress after refresh")
+    _check_output(refreshed, wl_b, tokens, "stress after refresh", layer)
     _check_weight_quant(layer, wl_b, [0, 63])
     layer.close()

@@ -227,7 +227,7 @@ def test_sigmoid_forms_flip_rate(T):
         layer.load_shared_weights(w13s.cuda(), w2s.cuda())
         layer.forward(d["x"], d["gate_w"])
         torch.cuda.synchronize()
-        _, hc, hsf, hgs = (t.cpu().numpy() for t in layer.debug_shared())
+        hc, hsf, hgs = (t.cpu().numpy() for t in layer.debug_shared()[1:])
         layer.close()
         np.testing.assert_allclose(hgs, sr["h_gs"], rtol=1e-4)
         codes = np.stack([hc & 0xF, hc >> 4], -1).reshape(T, -1)
