@@ -463,6 +463,41 @@ __device__ __forceinline__ void bf16x16_to_f32(const uint4& a, const uint4& b, f
   }
 }
 
+// One warp requantizes one FP32 row h [I] (I a multiple of 128) with the
+// row's global scale gs into the operand layout at row `prow` of an operand
+// whose rows hold i_pad elements: block scales and codes (codes and scales
+// share the operand buffer).  All 32 lanes must call it.  L2 loads: the row
+// may have been written by other CTAs.
+__device__ __forceinline__ void requant_row_warp(const float* __restrict__ hr, int I, int i_pad, size_t prow, float gs,
+                                                 uint8_t* __restrict__ h_codes, int lane) {
+  const int nblk = I / SF_VEC, k16_row = i_pad / SF_VEC;
+  for (int b0 = 0; b0 < nblk; b0 += 32) {  // nblk = I/16, a multiple of 8: uniform bound
+    const int b = b0 + lane;
+    uint2 packed = make_uint2(0u, 0u);
+    uint32_t sf = 0;
+    if (b < nblk) {
+      float v[16];
+      const float4* src = reinterpret_cast<const float4*>(hr + 16 * b);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 f = __ldcg(src + q);
+        v[4 * q] = f.x;
+        v[4 * q + 1] = f.y;
+        v[4 * q + 2] = f.z;
+        v[4 * q + 3] = f.w;
+      }
+      sf = nvfp4_quant_block16(v, gs, packed);
+    }
+    // blocks 4m..4m+3 have consecutive scale bytes: one 32-bit store
+    const uint32_t sf4 = sf | (__shfl_down_sync(0xffffffffu, sf, 1) << 8) | (__shfl_down_sync(0xffffffffu, sf, 2) << 16) |
+                         (__shfl_down_sync(0xffffffffu, sf, 3) << 24);
+    if (b < nblk) {
+      *reinterpret_cast<uint2*>(h_codes + operand_offset(prow, 8 * b, i_pad / 2)) = packed;
+      if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(h_codes + sf_atom_offset(prow, b, k16_row)) = sf4;
+    }
+  }
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

@@ -109,12 +109,15 @@ struct FrontArgs {
 };
 constexpr int FRONT_SYNC_WORDS = 64;
 // Words of the front kernel's sync block used by the all-experts small-batch
-// path (returned to zero by the requantization kernel): front CTAs that
-// quantized their tokens, front CTAs that routed their tokens, and the
-// dynamic work counter of the w13 GEMM.
+// path (returned to zero by the w2 GEMM): front CTAs that quantized their
+// tokens, front CTAs that routed their tokens, the dynamic work counter of
+// the w13 GEMM, and its requantization counters.
 constexpr int FRONT_SYNC_A_READY = 0;
 constexpr int FRONT_SYNC_ROUTED = 1;
 constexpr int FRONT_SYNC_WORK = 2;
+constexpr int FRONT_SYNC_RQ_ROW = 3;     // the w13 GEMM's requantization: next expanded row
+constexpr int FRONT_SYNC_RQ_EXPERT = 4;  // and next expert whose unrouted rows' maxima return to zero
+constexpr int FRONT_SYNC_RESET = 5;      // words the w2 GEMM returns to zero
 // CTAs of the front kernel's grid for T tokens and E experts.
 int front_ctas(int T, int E);
 cudaError_t front_setup(int H, int E);
@@ -179,6 +182,16 @@ struct GemmArgs {
   // grid size (dynamic schedule, no dependency wait); nullptr otherwise
   uint32_t* front_sync;
   int front_ctas;
+  // all-experts path: finished w13 column pairs per expert (the w13 GEMM
+  // counts and waits on them to requantize, the w2 GEMM returns them to
+  // zero); the w13 GEMM's requantization also needs the top-k ids [T, K],
+  // top_k, and the intermediate width I
+  uint32_t* expert_done;
+  const int32_t* topk_ids_small;
+  int inter;
+  // w2 of the all-experts path: the front kernel's sync words and the
+  // per-expert counts, returned to zero after the dependency wait
+  uint32_t* reset_sync;
   // SwiGLU sigmoid: 0 = 1/2 + tanh.approx(g/2)/2, 1 = 1 / (1 + expf(-g))
   // with an IEEE division
   int accurate_sigmoid;
@@ -199,17 +212,24 @@ cudaError_t launch_gemm_w13(const GemmArgs& a, int n_chunks, int n_clusters, int
 // in shared memory for the whole kernel (K <= 2048).
 cudaError_t launch_gemm_w13s(const GemmArgs& a, int n_ctas, bool resident, cudaStream_t s);
 // The row of expanded row i (token * K + slot) is row_map[i], or with topk_ids
-// given the small-batch padded row topk_ids[i] * 128 + i / K.  grouping: when
-// not null, one extra CTA derives the small batch's expert grouping from
-// topk_ids (T = n_rows / K tokens, E experts) while the others requantize.
-struct SmallGroupOut;
-// front_sync (with grouping): the all-experts path's sync words, returned to
-// zero, and the rows of tokens that did not route to an expert have their
-// maxima cleared (the dynamic w13 GEMM may have formed them).
+// given the small-batch padded row topk_ids[i] * 128 + i / K.
+struct RequantAllExperts {
+  const int32_t* src_of_padrow;  // routing of the padded rows
+  const uint32_t* expert_done;   // finished w13 column pairs per expert
+  const uint32_t* front_sync;    // the front kernel's counters
+  int pairs;                     // column pairs per expert (I / 128)
+  int front_ctas;
+  int E;
+};
+// all: the all-experts path (nullptr otherwise).  The kernel does not wait
+// for the w13 GEMM up front: each row starts once its expert's column pairs
+// are all done (and the routing is), and every CTA waits for the GEMM only at
+// its end - after which it returns to zero the maxima of the rows of tokens
+// that did not route to an expert (the GEMM forms every row until the
+// routing is known).
 cudaError_t launch_requant_rows(const float* hbuf, float* row_amax, const int32_t* row_map,
-                                const int32_t* topk_ids, int K, int E, const SmallGroupOut* grouping,
-                                uint32_t* front_sync, const int32_t* src_of_padrow, int n_rows,
-                                int I, int i_pad, uint8_t* h_codes, float* h_gs, cudaStream_t s);
+                                const int32_t* topk_ids, int K, int n_rows, int I, int i_pad, uint8_t* h_codes,
+                                float* h_gs, const RequantAllExperts* all, int* status, cudaStream_t s);
 cudaError_t launch_gemm_w2(const GemmArgs& a, int n_ctas, bool ordered, int a_rows, cudaStream_t s);
 cudaError_t launch_gemm_plain(const GemmArgs& a, int n_ctas, cudaStream_t s);
 

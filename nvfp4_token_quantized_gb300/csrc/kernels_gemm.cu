@@ -390,6 +390,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
   // Everything above overlaps the previous kernel's tail; its outputs (the
   // tile list, operands, scales) are read only from here on.
   if (!dyn) pdl_wait();
+  if (p.reset_sync && blockIdx.x == 0) {
+    // the all-experts path's counters, no longer read by the earlier kernels
+    if (threadIdx.x < FRONT_SYNC_RESET) p.reset_sync[threadIdx.x] = 0;
+    for (int e = threadIdx.x; e < p.num_experts; e += blockDim.x) p.expert_done[e] = 0;
+  }
   const int nunits = count_units();
 
   if (warp == 0) {
@@ -631,6 +636,16 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
 #pragma unroll
               for (int q = 0; q < 16; ++q) dst[q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
             }
+            if (dyn) {
+              // the unit's column pair is done for its expert once every
+              // epilogue warp stored its rows: the requantization kernel
+              // starts on an expert as soon as all its column pairs are
+              named_bar_sync(1, EPI_WARPS * 32);
+              if (warp == 2 && lane == 0) {
+                __threadfence();
+                atomicAdd(p.expert_done + un.e, 1u);
+              }
+            }
             continue;
           }
           // The CTA's two halves first combine their maxima in shared memory
@@ -689,9 +704,57 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
           if (f0 == 0) p.h_gs[prow] = gs_h;
         }
       }
-      if (dyn && warp == 2 && lane == 0 &&
-          !wait_counter_acquire(p.front_sync + FRONT_SYNC_ROUTED, front_n, nullptr))
-        report_device_error(p.status, DEV_ERR_TIMEOUT);
+      if (dyn) {
+        // No CTA finishes before the routing has: later kernels rely on it
+        // through this kernel's completion.  Meanwhile the CTA's epilogue
+        // warps, out of units, requantize the intermediate: each takes
+        // expanded rows (token * K + slot) from a global counter and starts
+        // one once its expert has all its column pairs done; then experts
+        // from a second counter, whose rows of tokens that did not route
+        // there get their maxima returned to zero (formed while the routing
+        // was not known).  The w2 GEMM waits for this kernel as a whole.
+        bool ok = true;
+        if (lane == 0) ok = wait_counter_acquire(p.front_sync + FRONT_SYNC_ROUTED, front_n, nullptr);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok && lane == 0) report_device_error(p.status, DEV_ERR_TIMEOUT);
+        const int T = p.small_T, K = p.top_k, n_rows = T * K;
+        while (ok) {
+          int r = 0;
+          if (lane == 0) r = (int)atomicAdd(p.front_sync + FRONT_SYNC_RQ_ROW, 1u);
+          r = __shfl_sync(0xffffffffu, r, 0);
+          if (r >= n_rows) break;
+          const int e = __ldcg(p.topk_ids_small + r);
+          if (lane == 0) ok = wait_counter_acquire(p.expert_done + e, (uint32_t)nch, &c.abort_flag);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) {
+            if (lane == 0) report_device_error(p.status, DEV_ERR_TIMEOUT);
+            break;
+          }
+          const size_t prow = (size_t)e * TILE_M + r / K;
+          const float gs_r = nvfp4_global_scale(__ldcg(p.row_amax + prow));
+          requant_row_warp(p.hbuf + prow * p.i_pad, p.inter, p.i_pad, prow, gs_r, p.h_codes, lane);
+          if (lane == 0) {
+            p.h_gs[prow] = gs_r;
+            p.row_amax[prow] = 0.0f;
+          }
+        }
+        while (ok) {
+          int e = 0;
+          if (lane == 0) e = (int)atomicAdd(p.front_sync + FRONT_SYNC_RQ_EXPERT, 1u);
+          e = __shfl_sync(0xffffffffu, e, 0);
+          if (e >= p.num_experts) break;
+          if (lane == 0) ok = wait_counter_acquire(p.expert_done + e, (uint32_t)nch, &c.abort_flag);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) {
+            if (lane == 0) report_device_error(p.status, DEV_ERR_TIMEOUT);
+            break;
+          }
+          for (int t = lane; t < T; t += 32) {
+            const size_t prow = (size_t)e * TILE_M + t;
+            if (__ldcg(p.src_of_padrow + prow) < 0) p.row_amax[prow] = 0.0f;
+          }
+        }
+      }
     } else {
       // pairs: the thread's 128-column tile `half` of the 128 x 256
       // accumulator; plain: its 64-column half of the 128-column buffer

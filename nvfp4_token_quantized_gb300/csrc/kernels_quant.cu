@@ -9,7 +9,6 @@
 #include <algorithm>
 
 #include "common.cuh"
-#include "grouping.cuh"
 #include "kernels.h"
 
 namespace moe {
@@ -93,75 +92,50 @@ __global__ void __launch_bounds__(256, 4) act_quant_kernel(const __nv_bfloat16* 
 // (token * K + slot), at its padded row: topk_ids[row] * 128 + row / K in the
 // small-batch layout, or row_map[row].  Row maximum -> global scale -> block
 // scales and codes, the same arithmetic as the fused w13 epilogue; returns
-// the row's maximum word to zero.  With do_group the last CTA instead derives
-// the batch's expert grouping from topk_ids (the GEMMs of the all-experts
-// schedule do not need it; the parity exports read it).
+// the row's maximum word to zero.
+// do_all (the all-experts path): no dependency wait up front.  A warp waits
+// (bounded, acquire) until the routing is published and its row's expert
+// has all its column pairs done, so rows are requantized while the w13 GEMM
+// still runs its last units; every CTA then waits for the GEMM (so that this
+// kernel completes after it, as later kernels assume) and returns to zero the
+// maxima of rows of tokens that did not route to an expert.
 __global__ void __launch_bounds__(256) requant_rows_kernel(const float* __restrict__ hbuf,
                                                           float* __restrict__ row_amax,
                                                           const int32_t* __restrict__ row_map,
-                                                          const int32_t* __restrict__ topk_ids, int K, int E,
-                                                          const SmallGroupOut grp, int do_group,
-                                                          uint32_t* __restrict__ front_sync,
-                                                          const int32_t* __restrict__ src_of_padrow, int n_rows,
+                                                          const int32_t* __restrict__ topk_ids, int K, int n_rows,
                                                           int I, int i_pad, uint8_t* __restrict__ h_codes,
-                                                          float* __restrict__ h_gs) {
+                                                          float* __restrict__ h_gs, const RequantAllExperts all,
+                                                          int do_all, int* __restrict__ status) {
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   pdl_trigger();
-  pdl_wait();
-  if (front_sync) {
-    // The all-experts path: the w13 GEMM (complete now) may have formed the
-    // rows of tokens that did not route to an expert; their maxima return to
-    // zero here (a routed row's own warp clears its word below).  Then the
-    // front kernel's counters and the GEMM's work counter return to zero.
-    const int T = n_rows / K;
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < E * T; i += gridDim.x * blockDim.x) {
-      const int prow = (i / T) * 128 + i % T;
-      if (src_of_padrow[prow] < 0) row_amax[prow] = 0.0f;
+  if (!do_all) pdl_wait();
+  if (row < n_rows) {
+    bool ok = true;
+    if (do_all) {
+      if (lane == 0)
+        ok = wait_counter_acquire(all.front_sync + FRONT_SYNC_ROUTED, (uint32_t)all.front_ctas, nullptr) &&
+             wait_counter_acquire(all.expert_done + __ldcg(topk_ids + row), (uint32_t)all.pairs, nullptr);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok && lane == 0) report_device_error(status, DEV_ERR_TIMEOUT);
     }
-    if (blockIdx.x == 0 && threadIdx.x < 3) front_sync[threadIdx.x] = 0;
-  }
-  if (do_group && blockIdx.x == gridDim.x - 1) {
-    __shared__ unsigned long long tok_mask[256];
-    __shared__ int offs[256];
-    __shared__ int red[8];
-    small_grouping(topk_ids, n_rows / K, K, E, grp, tok_mask, offs, red);
-    return;
-  }
-  if (row >= n_rows) return;
-  const int prow = topk_ids ? __ldg(topk_ids + row) * 128 + row / K : row_map[row];
-  const float amax = row_amax[prow];
-  const float gs = nvfp4_global_scale(amax);
-  const float* hr = hbuf + (size_t)prow * i_pad;
-  const int nblk = I / SF_VEC, k16_row = i_pad / SF_VEC;
-  for (int b0 = 0; b0 < nblk; b0 += 32) {  // nblk = I/16, a multiple of 8: uniform bound
-    const int b = b0 + lane;
-    uint2 packed = make_uint2(0u, 0u);
-    uint32_t sf = 0;
-    if (b < nblk) {
-      float v[16];
-      const float4* src = reinterpret_cast<const float4*>(hr + 16 * b);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 f = src[q];
-        v[4 * q] = f.x;
-        v[4 * q + 1] = f.y;
-        v[4 * q + 2] = f.z;
-        v[4 * q + 3] = f.w;
+    if (ok) {
+      const int prow = topk_ids ? __ldcg(topk_ids + row) * 128 + row / K : row_map[row];
+      const float gs = nvfp4_global_scale(__ldcg(row_amax + prow));
+      requant_row_warp(hbuf + (size_t)prow * i_pad, I, i_pad, prow, gs, h_codes, lane);
+      if (lane == 0) {
+        h_gs[prow] = gs;
+        row_amax[prow] = 0.0f;
       }
-      sf = nvfp4_quant_block16(v, gs, packed);
-    }
-    // blocks 4m..4m+3 have consecutive scale bytes: one 32-bit store
-    const uint32_t sf4 = sf | (__shfl_down_sync(0xffffffffu, sf, 1) << 8) | (__shfl_down_sync(0xffffffffu, sf, 2) << 16) |
-                         (__shfl_down_sync(0xffffffffu, sf, 3) << 24);
-    if (b < nblk) {
-      *reinterpret_cast<uint2*>(h_codes + operand_offset(prow, 8 * b, i_pad / 2)) = packed;
-      if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(h_codes + sf_atom_offset(prow, b, k16_row)) = sf4;
     }
   }
-  if (lane == 0) {
-    h_gs[prow] = gs;
-    row_amax[prow] = 0.0f;
+  if (do_all) {
+    pdl_wait();
+    const int T = n_rows / K;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < all.E * T; i += gridDim.x * blockDim.x) {
+      const int prow = (i / T) * 128 + i % T;
+      if (all.src_of_padrow[prow] < 0) row_amax[prow] = 0.0f;
+    }
   }
 }
 
@@ -438,15 +412,12 @@ cudaError_t launch_sf_to_atoms(const uint8_t* sf, int rows, int k16, uint8_t* at
 }
 
 cudaError_t launch_requant_rows(const float* hbuf, float* row_amax, const int32_t* row_map,
-                                const int32_t* topk_ids, int K, int E, const SmallGroupOut* grouping,
-                                uint32_t* front_sync, const int32_t* src_of_padrow, int n_rows,
-                                int I, int i_pad, uint8_t* h_codes, float* h_gs, cudaStream_t s) {
-  if (grouping && (!topk_ids || E > 256 || n_rows / K > 64)) return cudaErrorInvalidValue;
-  if (front_sync && (!topk_ids || !src_of_padrow)) return cudaErrorInvalidValue;
-  const SmallGroupOut g = grouping ? *grouping : SmallGroupOut{};
-  const unsigned grid = (n_rows + 7) / 8 + (grouping ? 1 : 0);
-  return launch_k(requant_rows_kernel, dim3(grid), dim3(256), 0, s, true, hbuf, row_amax, row_map, topk_ids, K, E,
-                  g, grouping ? 1 : 0, front_sync, src_of_padrow, n_rows, I, i_pad, h_codes, h_gs);
+                                const int32_t* topk_ids, int K, int n_rows, int I, int i_pad, uint8_t* h_codes,
+                                float* h_gs, const RequantAllExperts* all, int* status, cudaStream_t s) {
+  if (all && !topk_ids) return cudaErrorInvalidValue;
+  const RequantAllExperts a = all ? *all : RequantAllExperts{};
+  return launch_k(requant_rows_kernel, dim3((n_rows + 7) / 8), dim3(256), 0, s, true, hbuf, row_amax, row_map,
+                  topk_ids, K, n_rows, I, i_pad, h_codes, h_gs, a, all ? 1 : 0, status);
 }
 
 cudaError_t launch_finalize_atomic(const float* out_acc, const uint16_t* shared, float shared_scale, void* out, int T,

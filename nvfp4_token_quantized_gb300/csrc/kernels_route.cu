@@ -763,24 +763,21 @@ __global__ void __launch_bounds__(256, 1) front_small_kernel(const __grid_consta
       p.src_of_padrow[e * 128 + tok] = src;
     }
   }
-  if (p.all_experts) {
-    // routing (and the row clearing) published: the w13 GEMM completes only
-    // after every front CTA got here
-    __syncthreads();
-    if (threadIdx.x == 0) arrive_acq_rel_gpu(&p.sync[FRONT_SYNC_ROUTED]);
-    return;
-  }
-
-  // the expert grouping, by the last CTA of the grid
+  // Routing (and the row clearing) published.  With the all-experts
+  // schedule the w13 GEMM completes only after every front CTA arrived on
+  // the routed counter (the w2 GEMM returns it to zero); otherwise a counter
+  // of its own (returned to zero below).  The last CTA to arrive derives the
+  // expert grouping: on the all-experts path no GEMM waits for it.
   __syncthreads();
-  if (threadIdx.x == 0) last = arrive_acq_rel_gpu(&p.sync[FRONT_SYNC_WORDS - 1]) == gridDim.x - 1;
+  uint32_t* ctr = p.all_experts ? &p.sync[FRONT_SYNC_ROUTED] : &p.sync[FRONT_SYNC_WORDS - 1];
+  if (threadIdx.x == 0) last = arrive_acq_rel_gpu(ctr) == gridDim.x - 1;
   __syncthreads();
   if (!last) return;
   unsigned long long* tok_mask = reinterpret_cast<unsigned long long*>(front_smem);  // [256] (the ring is idle)
   int* offs = reinterpret_cast<int*>(tok_mask + 256);                                // [256]
   const SmallGroupOut go{p.expert_offsets, p.src_of_row, p.row_of_src, p.pad_row_of_src, p.tiles, p.num_tiles};
   small_grouping(p.topk_ids, T, K, E, go, tok_mask, offs, red);
-  if (threadIdx.x == 0) p.sync[FRONT_SYNC_WORDS - 1] = 0;
+  if (threadIdx.x == 0 && !p.all_experts) p.sync[FRONT_SYNC_WORDS - 1] = 0;
 }
 
 template <int TB, int EB, bool XALL>

@@ -16,7 +16,6 @@
 
 #include "../../include/moe_nvfp4.h"
 #include "common.cuh"
-#include "grouping.cuh"
 #include "kernels.h"
 
 using namespace moe;
@@ -54,6 +53,7 @@ struct moe_handle {
   int4* tiles = nullptr;
   int32_t* num_tiles = nullptr;
   uint32_t* front_sync = nullptr;  // completion counters of the small-batch front kernel
+  uint32_t* expert_done = nullptr; // all-experts path: finished w13 column pairs per expert [256]
   // Shared expert (Is > 0): its NVFP4 weights, the token-ordered activation
   // and intermediate operands (row t = token t, 128-row tiles), the
   // identity row map, its tile list, its bf16 output rows, and the second
@@ -301,8 +301,8 @@ moe_status shared_branch(moe_handle* h, const void* x, int T, cudaStream_t s) {
     g.hbuf = h->s_hbuf;
     g.row_amax = h->s_row_amax;
     CK(h, launch_gemm_w13s(g, std::min(h->num_sms, g.w13_pairs), false, h->side));
-    CK(h, launch_requant_rows(h->s_hbuf, h->s_row_amax, h->s_ident, nullptr, 1, 1, nullptr, nullptr, nullptr, T,
-                              h->Is, h->Ipad_s, h->s_h_codes, h->s_h_gs, h->side));
+    CK(h, launch_requant_rows(h->s_hbuf, h->s_row_amax, h->s_ident, nullptr, 1, T, h->Is, h->Ipad_s, h->s_h_codes,
+                              h->s_h_gs, nullptr, h->status_dev, h->side));
   } else {
     CK(h, launch_gemm_w13(g, h->Is / 128, std::min(h->s_clusters[a_rows == 128], ntiles), a_rows, h->side));
   }
@@ -422,6 +422,10 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
     if (all_experts) {  // dynamic schedule on the front kernel's counters
       g.front_sync = h->front_sync;
       g.front_ctas = front_ctas(T, E);
+      g.expert_done = h->expert_done;
+      g.topk_ids_small = h->topk_ids;
+      g.top_k = K;
+      g.inter = h->I;
     }
     g.h_gs_static = h->static_scales ? h->static_h_gs : nullptr;
     g.accurate_sigmoid = (h->cfg.flags & MOE_FLAG_ACCURATE_SIGMOID) != 0;
@@ -434,14 +438,11 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
       g.hbuf = h->hbuf;
       g.row_amax = h->row_amax;
       CK(h, launch_gemm_w13s(g, std::min(gemm_sms, units_e * g.w13_pairs), false, s));
-      // (with static scales the w13 epilogue has already requantized)
-      if (!h->static_scales) {
-        const SmallGroupOut grp{h->expert_offsets, h->src_of_row, h->row_of_src, h->pad_row_of_src, h->tiles,
-                                h->num_tiles};
-        CK(h, launch_requant_rows(h->hbuf, h->row_amax, nullptr, h->topk_ids, K, E, all_experts ? &grp : nullptr,
-                                  all_experts ? h->front_sync : nullptr, h->src_of_padrow, T * K, h->I, h->Ipad,
-                                  h->h_codes, h->h_gs, s));
-      }
+      // (with static scales the w13 epilogue has already requantized; on the
+      // all-experts path the w13 GEMM's CTAs requantize once out of units)
+      if (!h->static_scales && !all_experts)
+        CK(h, launch_requant_rows(h->hbuf, h->row_amax, nullptr, h->topk_ids, K, T * K, h->I, h->Ipad, h->h_codes,
+                                  h->h_gs, nullptr, h->status_dev, s));
     } else {
       CK(h, launch_gemm_w13(g, h->I / 128, std::min(h->w13_clusters[tile_rows == 128], tb), tile_rows, s));
     }
@@ -468,6 +469,8 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
     g2.prefetch_units = small ? W2_PREFETCH_UNITS : 0;
     g2.all_experts = all_experts;
     g2.small_T = T;
+    g2.reset_sync = all_experts ? h->front_sync : nullptr;
+    g2.expert_done = h->expert_done;
     // units are pairs of 128-column tiles
     CK(h, launch_gemm_w2(g2, std::min(gemm_sms, units_e * g2.n_tiles / 2), ordered, tile_rows, s));
     CK(h, mark(h, 6, s));
@@ -578,6 +581,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
   A(h->tiles, sizeof(int4) * (size_t)h->tile_cap);
   A(h->num_tiles, sizeof(int32_t) * 4);
   A(h->front_sync, sizeof(uint32_t) * FRONT_SYNC_WORDS);
+  A(h->expert_done, sizeof(uint32_t) * 256);
   if (Is > 0) {
     h->Is = Is;
     h->Ipad_s = (Is + 255) / 256 * 256;
