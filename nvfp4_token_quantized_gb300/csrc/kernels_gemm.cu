@@ -83,6 +83,13 @@ constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr int HALF_MAX_BYTES = 2 * 2 * TILE_M * 4;  // w13: per-half row maxima, two m-tile buffers
 constexpr int CTRL_BYTES = 256;
+// Ordered w2 epilogue: each epilogue warp stages its 32 rows, 64 columns
+// (128 bytes of bf16) at a time, in shared memory with a 16-byte pad per row
+// (conflict-free 16-byte writes of one row per lane, reads of one row per 8
+// lanes), so that every store instruction writes four whole 128-byte row
+// segments instead of 32 scattered 16-byte pieces.
+constexpr int EPI_ROW_STRIDE = 144;
+constexpr int EPI_STAGE_BYTES = 8 * 32 * EPI_ROW_STRIDE;
 constexpr int MAX_SMEM = 232448;
 static_assert(TMEM_SF_BASE + MAX_STAGES * TMEM_SF_STAGE <= TMEM_COLS, "tensor memory overflow");
 static_assert(TMEM_SF_BASE + MAX_STAGES_PAIR * TMEM_SF_STAGE_PAIR <= TMEM_COLS, "tensor memory overflow");
@@ -126,9 +133,10 @@ __host__ __device__ constexpr int b_slot_bytes(bool pair) { return pair ? 2 * B_
 __host__ __device__ constexpr int stage_bytes(int a_rows, bool pair = false) {
   return a_slot_bytes(a_rows) + b_slot_bytes(pair);
 }
-__host__ __device__ constexpr int smem_bytes_for(int stages, int nch, int a_rows, bool pair = false) {
+__host__ __device__ constexpr int smem_bytes_for(int stages, int nch, int a_rows, bool pair = false,
+                                                 bool stage_out = false) {
   return stages * stage_bytes(a_rows, pair) + a_tail_bytes(a_rows) + CTRL_BYTES + 2 * nch * TILE_M * 4 +
-         HALF_MAX_BYTES + 1024;
+         HALF_MAX_BYTES + (stage_out ? EPI_STAGE_BYTES : 0) + 1024;
 }
 // Resident activations (the small-batch w13 GEMM, whose tiles all read the
 // same shared activation tile): all K stages of A stay in shared memory for
@@ -186,13 +194,15 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
   // [2][2][128] w13 row maxima of the two column halves of a CTA (m-tile
   // buffer i & 1, then half)
   float* half_max = reinterpret_cast<float*>(part + (MODE == MODE_W13 ? 2 * gridDim.x * TILE_M : 0));
+  // ordered w2: the epilogue warps' output staging, [8 warps][32 rows][EPI_ROW_STRIDE]
+  uint8_t* epi_stage = reinterpret_cast<uint8_t*>(half_max) + HALF_MAX_BYTES;
   {
     // The layout above must fit the launch's dynamic shared memory; if the
     // host sized it differently, report and leave before touching any of it
     // (the condition is the same in every CTA of the grid).
     uint32_t dyn;
     asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
-    const uint8_t* end = reinterpret_cast<const uint8_t*>(half_max) + HALF_MAX_BYTES;
+    const uint8_t* end = epi_stage + (MODE == MODE_W2_ORDERED ? EPI_STAGE_BYTES : 0);
     if (end > smem_raw + dyn) {
       if (threadIdx.x == 0) report_device_error(p.status, DEV_ERR_BAD_STATE);
       return;
@@ -769,6 +779,14 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
           src = row_ok ? p.src_of_padrow[prow] : -1;
           row_ok = src >= 0;  // a token that did not pick this expert
         }
+        // the row's scales and routing weight, loaded while the MMAs run
+        float alpha = 1.0f, wj = 1.0f;
+        if constexpr (MODE == MODE_W2_ATOMIC || MODE == MODE_W2_ORDERED) {
+          if (warp_rows && row_ok) {
+            alpha = __fdiv_rn(1.0f, __fmul_rn(p.gs_rows[prow], p.gs_w[un.e]));
+            if constexpr (MODE == MODE_W2_ATOMIC) wj = p.topk_w[src];
+          }
+        }
         // pairs: one 128 x 256 accumulator (buffer 0) holding both tiles
         const int buf = PAIR ? 0 : n & 1;
         bool ready;
@@ -794,31 +812,51 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
         if (ready && warp_rows && row_ok) {
           const int col = PAIR ? (un.col + half) * TILE_N : un.col * TILE_N + 64 * half;
           if constexpr (MODE == MODE_W2_ATOMIC || MODE == MODE_W2_ORDERED) {
-            const float alpha = __fdiv_rn(1.0f, __fmul_rn(p.gs_rows[prow], p.gs_w[un.e]));
             if constexpr (MODE == MODE_W2_ATOMIC) {
-              const float wj = p.topk_w[src];
               const int tok = src / (p.top_k > 0 ? p.top_k : 1);
               float* dst = p.out_acc + (size_t)tok * p.hidden + col;
 #pragma unroll
               for (int q = 0; q < COLS; q += 4)
                 red_add_v4(dst + q, __fmul_rn(wj, __fmul_rn(a[q], alpha)), __fmul_rn(wj, __fmul_rn(a[q + 1], alpha)),
                            __fmul_rn(wj, __fmul_rn(a[q + 2], alpha)), __fmul_rn(wj, __fmul_rn(a[q + 3], alpha)));
-            } else {
-              // the (token, slot) row of the expert output, rounded to bf16
-              uint4* dst = reinterpret_cast<uint4*>(p.ybuf + (size_t)src * p.hidden + col);
-#pragma unroll
-              for (int q = 0; q < COLS / 8; ++q) {
-                uint32_t w[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                  w[i] = pack_bf16x2(__fmul_rn(a[8 * q + 2 * i], alpha), __fmul_rn(a[8 * q + 2 * i + 1], alpha));
-                dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
-              }
             }
           } else {
             float4* dst = reinterpret_cast<float4*>(p.d + (size_t)prow * p.ldd + col);
 #pragma unroll
             for (int q = 0; q < COLS / 4; ++q) dst[q] = make_float4(a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
+          }
+        }
+        if constexpr (MODE == MODE_W2_ORDERED) {
+          // the (token, slot) rows of the expert output, rounded to bf16,
+          // through the warp's staging rows (the warp's calls are uniform:
+          // warp_rows is; rows without a routed token store nothing)
+          if (warp_rows) {
+            const int col = (un.col + half) * TILE_N;
+            const int my_src = (ready && row_ok) ? src : -1;
+            uint8_t* stg = epi_stage + (warp - 2) * (32 * EPI_ROW_STRIDE);
+#pragma unroll
+            for (int pass = 0; pass < COLS / 64; ++pass) {
+              uint4* srow = reinterpret_cast<uint4*>(stg + lane * EPI_ROW_STRIDE);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const int c0 = pass * 64 + 8 * q;
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  w[i] = pack_bf16x2(__fmul_rn(a[c0 + 2 * i], alpha), __fmul_rn(a[c0 + 2 * i + 1], alpha));
+                srow[q] = make_uint4(w[0], w[1], w[2], w[3]);
+              }
+              __syncwarp();
+              // lanes 8j .. 8j + 7 store row 4i + j
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const int r = 4 * i + (lane >> 3);
+                const int rsrc = __shfl_sync(0xffffffffu, my_src, r);
+                const uint4 v = reinterpret_cast<const uint4*>(stg + r * EPI_ROW_STRIDE)[lane & 7];
+                if (rsrc >= 0) reinterpret_cast<uint4*>(p.ybuf + (size_t)rsrc * p.hidden + col + pass * 64)[lane & 7] = v;
+              }
+              __syncwarp();
+            }
           }
         }
       }
@@ -836,9 +874,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
   }
 }
 
-constexpr int stages_for(int nch, int a_rows, bool pair = false) {
+constexpr int stages_for(int nch, int a_rows, bool pair = false, bool stage_out = false) {
   for (int s = pair ? MAX_STAGES_PAIR : MAX_STAGES; s >= 3; --s)
-    if (smem_bytes_for(s, nch, a_rows, pair) <= MAX_SMEM) return s;
+    if (smem_bytes_for(s, nch, a_rows, pair, stage_out) <= MAX_SMEM) return s;
   return 0;
 }
 constexpr int stages_for_res(int nch, int a_rows, bool pair = false) {
@@ -850,7 +888,8 @@ constexpr int stages_for_res(int nch, int a_rows, bool pair = false) {
 template <int MODE, int A_ROWS, int STAGES, bool ARES>
 constexpr int kernel_smem(int nch) {
   constexpr bool pair = pair_mode(MODE);
-  return ARES ? smem_bytes_res(STAGES, nch, A_ROWS, pair) : smem_bytes_for(STAGES, nch, A_ROWS, pair);
+  return ARES ? smem_bytes_res(STAGES, nch, A_ROWS, pair)
+              : smem_bytes_for(STAGES, nch, A_ROWS, pair, MODE == MODE_W2_ORDERED);
 }
 
 // The shared-memory cap belongs to the kernel instantiation, which handles of
@@ -907,6 +946,9 @@ cudaError_t launch(const GemmArgs& a, dim3 grid, int nch, cudaStream_t s) {
 // clusters one stage less.
 constexpr int W2_STAGES_128 = stages_for(0, 128, true);
 constexpr int W2_STAGES_64 = stages_for(0, 64, true);
+// the ordered w2 epilogue's output staging takes a ring stage
+constexpr int W2O_STAGES_128 = stages_for(0, 128, true, true);
+constexpr int W2O_STAGES_64 = stages_for(0, 64, true, true);
 constexpr int PLAIN_STAGES = stages_for(0, 128);
 constexpr int W13_STAGES_128 = stages_for(6, 128, true);
 constexpr int W13_STAGES_128_L = stages_for(16, 128, true);
@@ -917,6 +959,7 @@ constexpr int W13S_STAGES = stages_for(0, 64, true);
 static_assert(W2_STAGES_128 >= 4 && PLAIN_STAGES >= 4 && W13_STAGES_128_L >= 3 && W13_STAGES_64_L >= 3 && W13S_STAGES_RES >= 3,
               "ring too shallow");
 static_assert(W13_STAGES_128 >= 4 && W13S_STAGES >= 4, "ring too shallow");
+static_assert(W2O_STAGES_128 >= 3 && W2O_STAGES_64 >= 3, "ring too shallow");
 
 template <typename F>
 cudaError_t with_w13(int nch, int a_rows, F&& f) {
@@ -945,8 +988,8 @@ cudaError_t gemm_setup_attributes(int nch) {
   if ((e = set_attrs<MODE_W13S, 64, W13S_STAGES, false>(0)) != cudaSuccess) return e;
   if ((e = set_attrs<MODE_W2_ATOMIC, 128, W2_STAGES_128>(0)) != cudaSuccess) return e;
   if ((e = set_attrs<MODE_W2_ATOMIC, 64, W2_STAGES_64>(0)) != cudaSuccess) return e;
-  if ((e = set_attrs<MODE_W2_ORDERED, 128, W2_STAGES_128>(0)) != cudaSuccess) return e;
-  if ((e = set_attrs<MODE_W2_ORDERED, 64, W2_STAGES_64>(0)) != cudaSuccess) return e;
+  if ((e = set_attrs<MODE_W2_ORDERED, 128, W2O_STAGES_128>(0)) != cudaSuccess) return e;
+  if ((e = set_attrs<MODE_W2_ORDERED, 64, W2O_STAGES_64>(0)) != cudaSuccess) return e;
   return set_attrs<MODE_PLAIN, 128, PLAIN_STAGES>(0);
 }
 
@@ -982,10 +1025,10 @@ cudaError_t launch_gemm_w13s(const GemmArgs& a, int n_ctas, bool resident, cudaS
 cudaError_t launch_gemm_w2(const GemmArgs& a, int n_ctas, bool ordered, int a_rows, cudaStream_t s) {
   const dim3 grid(n_ctas, 1, 1);
   if (a_rows == 64) {
-    if (ordered) return launch<MODE_W2_ORDERED, 64, W2_STAGES_64>(a, grid, 0, s);
+    if (ordered) return launch<MODE_W2_ORDERED, 64, W2O_STAGES_64>(a, grid, 0, s);
     return launch<MODE_W2_ATOMIC, 64, W2_STAGES_64>(a, grid, 0, s);
   }
-  if (ordered) return launch<MODE_W2_ORDERED, 128, W2_STAGES_128>(a, grid, 0, s);
+  if (ordered) return launch<MODE_W2_ORDERED, 128, W2O_STAGES_128>(a, grid, 0, s);
   return launch<MODE_W2_ATOMIC, 128, W2_STAGES_128>(a, grid, 0, s);
 }
 

@@ -15,6 +15,10 @@ namespace moe {
 
 namespace {
 
+// Blocks per lane whose codes the activation quantizer holds in registers
+// across its dependency wait (rows of up to 32 * 8 * 16 = 4096 elements).
+constexpr int AQ_MAX_BLOCKS = 8;
+
 // One warp per token.  Lane L owns the 16-element blocks L, L+32, ...
 // The token's codes, block scales and global scale are written to each of its
 // K expanded rows (the rows of its K experts in the padded expert-grouped
@@ -54,15 +58,50 @@ __global__ void __launch_bounds__(256, 4) act_quant_kernel(const __nv_bfloat16* 
     gs = nvfp4_global_scale(amax);
   }
 
-  pdl_wait();
-  int prow[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) prow[j] = j < K ? pad_row_of_src[(size_t)t * K + j] : 0;
-
+  // Codes and block scales of the row, computed before the dependency wait
+  // (they depend only on x) and held in registers: lane L owns the blocks
+  // L, L + 32, ... (at most AQ_MAX_BLOCKS of them; longer rows take the
+  // loop below, which quantizes after the wait).  nblk is a multiple of 16:
+  // the loop bounds are warp-uniform, and blocks 4m..4m+3 of a row (one
+  // lane group) have consecutive scale bytes, written as one 32-bit word by
+  // the group's first lane.
   const size_t row_bytes = (size_t)H / 2;
-  // nblk is a multiple of 16: the loop bound is warp-uniform, and blocks
-  // 4m..4m+3 of a row (one lane group) have consecutive scale bytes, written
-  // as one 32-bit word by the group's first lane.
+  const int nb_lane = (nblk + 31) / 32;
+  if (nb_lane <= AQ_MAX_BLOCKS) {
+    uint2 packed[AQ_MAX_BLOCKS];
+    uint32_t sf4[AQ_MAX_BLOCKS];
+#pragma unroll
+    for (int i = 0; i < AQ_MAX_BLOCKS; ++i) {
+      if (i < nb_lane) {
+        const int b = 32 * i + lane;
+        uint32_t sf = 0;
+        packed[i] = make_uint2(0u, 0u);
+        if (b < nblk) {
+          float v[16];
+          bf16x16_to_f32(__ldg(xr + 2 * b), __ldg(xr + 2 * b + 1), v);
+          sf = nvfp4_quant_block16(v, gs, packed[i]);
+        }
+        sf4[i] = sf | (__shfl_down_sync(0xffffffffu, sf, 1) << 8) | (__shfl_down_sync(0xffffffffu, sf, 2) << 16) |
+                 (__shfl_down_sync(0xffffffffu, sf, 3) << 24);
+      }
+    }
+    pdl_wait();
+    for (int j = 0; j < K; ++j) {
+      const int prow = pad_row_of_src[(size_t)t * K + j];
+#pragma unroll
+      for (int i = 0; i < AQ_MAX_BLOCKS; ++i) {
+        const int b = 32 * i + lane;
+        if (i < nb_lane && b < nblk) {
+          *reinterpret_cast<uint2*>(a_codes + operand_offset(prow, 8 * b, (int)row_bytes)) = packed[i];
+          if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(a_sf + sf_atom_offset(prow, b, nblk)) = sf4[i];
+        }
+      }
+      if (lane == 0) gs_rows[prow] = gs;
+    }
+    return;
+  }
+
+  pdl_wait();
   for (int b0 = 0; b0 < nblk; b0 += 32) {
     const int b = b0 + lane;
     const bool active = b < nblk;
@@ -76,12 +115,10 @@ __global__ void __launch_bounds__(256, 4) act_quant_kernel(const __nv_bfloat16* 
     const uint32_t sf4 = sf | (__shfl_down_sync(0xffffffffu, sf, 1) << 8) | (__shfl_down_sync(0xffffffffu, sf, 2) << 16) |
                          (__shfl_down_sync(0xffffffffu, sf, 3) << 24);
     if (active) {
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        if (j < K) {
-          *reinterpret_cast<uint2*>(a_codes + operand_offset(prow[j], 8 * b, (int)row_bytes)) = packed;
-          if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(a_sf + sf_atom_offset(prow[j], b, nblk)) = sf4;
-        }
+      for (int j = 0; j < K; ++j) {
+        const int prow = pad_row_of_src[(size_t)t * K + j];
+        *reinterpret_cast<uint2*>(a_codes + operand_offset(prow, 8 * b, (int)row_bytes)) = packed;
+        if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(a_sf + sf_atom_offset(prow, b, nblk)) = sf4;
       }
     }
   }
