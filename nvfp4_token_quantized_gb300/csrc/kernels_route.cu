@@ -217,103 +217,95 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const __nv_bfloat16*
 }
 
 // (value, expert) order of the top-k: larger logit first, ties to the lower
-// expert id.
-__device__ __forceinline__ bool topk_before(float av, int ae, float bv, int be) {
-  return av > bv || (av == bv && ae < be);
+// expert id.  As one 64-bit key: the logit's bits mapped to an unsigned
+// integer of the same order (-0 taken as +0, so that equal logits tie) in the
+// high word, the complement of the expert id in the low word; the larger key
+// comes first.
+__device__ __forceinline__ uint64_t topk_key(float v, int e) {
+  const uint32_t b = __float_as_uint(__fadd_rn(v, 0.0f));  // -0 -> +0
+  const uint32_t o = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return ((uint64_t)o << 32) | (uint32_t)~e;
+}
+__device__ __forceinline__ float topk_key_value(uint32_t o) {
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
 }
 
-// Compare-exchange of two candidates: the one first in topk_before order
-// ends up in slot a.
-__device__ __forceinline__ void topk_cas(float& va, int& ea, float& vb, int& eb) {
-  if (topk_before(vb, eb, va, ea)) {
-    const float tv = va;
-    const int te = ea;
-    va = vb;
-    ea = eb;
-    vb = tv;
-    eb = te;
-  }
+// Compare-exchange of two keys: the larger ends up in a.
+__device__ __forceinline__ void topk_cas(uint64_t& a, uint64_t& b) {
+  const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
+  a = hi;
+  b = lo;
 }
 
 // Top-k of one token's logits by one warp.  Lane l holds the NE candidates
-// l, l + 32, ... (E <= 32 NE) and sorts them by (logit desc, expert asc), a
-// total order since expert ids are unique; each of the K rounds takes the
-// best lane head over the warp (a butterfly argmax in the same order) and
-// the lane that held it moves on to its next candidate.  Softmax over all E
-// experts (each lane sums its raw logits in ascending expert order, then the
-// xor tree), chosen probabilities renormalised in slot order.  Lane j < K
-// returns slot j: its expert in e_lane and its weight in w_lane.  Logits are
-// read through L2 (another CTA of the same grid may have written them).  All
-// 32 lanes must call it.
+// l, l + 32, ... (E <= 32 NE) as keys sorted descending; each of the K rounds
+// takes the largest lane head over the warp - two warp-wide unsigned maxima
+// (redux.sync), of the high words, then of the low words among the lanes
+// holding that high word - and the lane that held it moves on to its next
+// candidate.  Softmax over all E experts (each lane sums its raw logits in
+// ascending expert order, then the xor tree), chosen probabilities
+// renormalised in slot order.  Lane j < K returns slot j: its expert in e_lane
+// and its weight in w_lane.  Logits are read through L2 (another CTA of the
+// same grid may have written them).  All 32 lanes must call it.
 // SMEM: lrow is in shared memory (the CTA's own logits).
 template <int NE, bool SMEM = false>
 __device__ __forceinline__ void topk_warp_n(const float* __restrict__ lrow, int E, int K, int lane, int& e_lane,
                                             float& w_lane) {
-  float raw[NE], v[NE];
-  int id[NE];
+  float raw[NE];
+  uint64_t key[NE];
 #pragma unroll
   for (int i = 0; i < NE; ++i) {
     const int e = lane + 32 * i;
     raw[i] = e < E ? (SMEM ? lrow[e] : __ldcg(lrow + e)) : -INFINITY;
-    v[i] = raw[i];
-    id[i] = e < E ? e : 0x7fffffff;  // padding sorts last
+    key[i] = e < E ? topk_key(raw[i], e) : 0ull;  // padding sorts last
   }
   // sorting network: 5 exchanges for 4 candidates, 19 for 8
   if constexpr (NE == 4) {
-    topk_cas(v[0], id[0], v[1], id[1]);
-    topk_cas(v[2], id[2], v[3], id[3]);
-    topk_cas(v[0], id[0], v[2], id[2]);
-    topk_cas(v[1], id[1], v[3], id[3]);
-    topk_cas(v[1], id[1], v[2], id[2]);
+    topk_cas(key[0], key[1]);
+    topk_cas(key[2], key[3]);
+    topk_cas(key[0], key[2]);
+    topk_cas(key[1], key[3]);
+    topk_cas(key[1], key[2]);
   } else {
     static_assert(NE == 8, "4 or 8 candidates per lane");
     constexpr int net[19][2] = {{0, 2}, {1, 3}, {4, 6}, {5, 7}, {0, 4}, {1, 5}, {2, 6}, {3, 7}, {0, 1}, {2, 3},
                                 {4, 5}, {6, 7}, {2, 4}, {3, 5}, {1, 4}, {3, 6}, {1, 2}, {3, 4}, {5, 6}};
 #pragma unroll
-    for (int c = 0; c < 19; ++c) topk_cas(v[net[c][0]], id[net[c][0]], v[net[c][1]], id[net[c][1]]);
+    for (int c = 0; c < 19; ++c) topk_cas(key[net[c][0]], key[net[c][1]]);
   }
-  float l_lane = -INFINITY, m = 0.0f, s = 0.0f;
-  e_lane = 0;
+  uint32_t win_hi = 0, win_lo = 0, first_hi = 0;
 #pragma unroll 1
   for (int j = 0; j < K; ++j) {
-    float bv = v[0];
-    int be = id[0];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (topk_before(ov, oe, bv, be)) {
-        bv = ov;
-        be = oe;
-      }
-    }
-    if (j == 0) {
-      // the maximum logit: the softmax denominator over all experts
-      m = bv;
-#pragma unroll
-      for (int i = 0; i < NE; ++i)
-        if (lane + 32 * i < E) s += expf(raw[i] - m);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    }
+    const uint32_t hi = (uint32_t)(key[0] >> 32), lo = (uint32_t)key[0];
+    const uint32_t mhi = __reduce_max_sync(0xffffffffu, hi);
+    const uint32_t mlo = __reduce_max_sync(0xffffffffu, hi == mhi ? lo : 0u);
+    if (j == 0) first_hi = mhi;
     if (lane == j) {
-      l_lane = bv;
-      e_lane = be;
+      win_hi = mhi;
+      win_lo = mlo;
     }
-    if (id[0] == be) {  // this lane's head was taken
+    if (hi == mhi && lo == mlo) {  // this lane's head was taken
 #pragma unroll
-      for (int i = 0; i + 1 < NE; ++i) {
-        v[i] = v[i + 1];
-        id[i] = id[i + 1];
-      }
-      v[NE - 1] = -INFINITY;
-      id[NE - 1] = 0x7fffffff;
+      for (int i = 0; i + 1 < NE; ++i) key[i] = key[i + 1];
+      key[NE - 1] = 0ull;
     }
   }
-  const float pj = lane < K ? expf(l_lane - m) / s : 0.0f;
+  // the maximum logit: the softmax denominator over all experts
+  const float m = topk_key_value(first_hi);
+  float s = 0.0f;
+#pragma unroll
+  for (int i = 0; i < NE; ++i)
+    if (lane + 32 * i < E) s += expf(raw[i] - m);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  e_lane = lane < K ? (int)~win_lo : 0;
+  const float pj = lane < K ? expf(topk_key_value(win_hi) - m) / s : 0.0f;
   float psum = 0.0f;
-#pragma unroll 1
-  for (int j = 0; j < K; ++j) psum += __shfl_sync(0xffffffffu, pj, j);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float q = __shfl_sync(0xffffffffu, pj, j);
+    if (j < K) psum += q;
+  }
   w_lane = pj / psum;
 }
 
