@@ -273,10 +273,9 @@ MOE_API const char* moe_stage_name(int i);
  * runtime whose memory pool already holds all free device memory (a
  * cudaMalloc there fails), or a step that cannot afford the device-wide
  * synchronisation a cudaMalloc/cudaFree implies.  Such callers have no
- * moe_handle to hold a workspace, so the intermediate router logits and the
- * per-expert row counters live in one fixed array in the library's device
- * code: MOE_ROUTE_NOALLOC_MAX_LOGITS floats of logits plus 256 counters
- * (about 4 MiB per device, reserved when the library's device code is loaded
+ * moe_handle to hold a workspace, so the intermediate router logits live in
+ * one fixed array in the library's device code: MOE_ROUTE_NOALLOC_MAX_LOGITS
+ * floats (4 MiB per device, reserved when the library's device code is loaded
  * on that device).  After the first call on a device, nothing is allocated by
  * a call, by CUDA or otherwise.  Under CUDA's default lazy module loading the
  * device code (and with it the array) is loaded on a device by the first call

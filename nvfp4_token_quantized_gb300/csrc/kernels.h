@@ -16,11 +16,10 @@ cudaError_t router_setup(int H, int E);
 cudaError_t router_setup_max(int bytes);
 // Dynamic shared memory one router launch for (H, E) needs.
 int router_smem_bytes(int H, int E);
-// Also clears counts[E] for the top-k kernel.
 cudaError_t launch_router_logits(const void* x, const void* gate_w, const float* bias, float* logits, int T,
-                                 int H, int E, int32_t* counts, cudaStream_t s);
+                                 int H, int E, cudaStream_t s);
 cudaError_t launch_topk(const float* logits, int T, int E, int K, int32_t* topk_ids, float* topk_w,
-                        int32_t* counts, cudaStream_t s);
+                        cudaStream_t s);
 struct PermuteOut {
   int32_t* expert_offsets;  // [E+1]
   int32_t* src_of_row;      // [R]
@@ -31,8 +30,8 @@ struct PermuteOut {
   int32_t* num_tiles;       // [1]
 };
 // tile_rows: 128 rows per GEMM tile.
-cudaError_t launch_permute(const int32_t* topk_ids, const int32_t* counts, int T, int K, int E, int tile_rows,
-                           const PermuteOut& o, cudaStream_t s);
+cudaError_t launch_permute(const int32_t* topk_ids, int T, int K, int E, int tile_rows, const PermuteOut& o,
+                           cudaStream_t s);
 
 // ---- quantization (kernels_quant.cu) ----
 // static_gs: nullptr for per-token global scales, else the calibrated

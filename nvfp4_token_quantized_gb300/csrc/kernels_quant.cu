@@ -15,9 +15,10 @@ namespace moe {
 
 namespace {
 
-// Blocks per lane whose codes the activation quantizer holds in registers
-// across its dependency wait (rows of up to 32 * 8 * 16 = 4096 elements).
-constexpr int AQ_MAX_BLOCKS = 8;
+// Block pairs per lane whose codes the activation quantizer holds in
+// registers across its dependency wait (rows of up to 32 * 4 * 32 = 4096
+// elements).
+constexpr int AQ_MAX_PAIRS = 4;
 
 // One warp per token.  Lane L owns the 16-element blocks L, L+32, ...
 // The token's codes, block scales and global scale are written to each of its
@@ -59,41 +60,46 @@ __global__ void __launch_bounds__(256, 4) act_quant_kernel(const __nv_bfloat16* 
   }
 
   // Codes and block scales of the row, computed before the dependency wait
-  // (they depend only on x) and held in registers: lane L owns the blocks
-  // L, L + 32, ... (at most AQ_MAX_BLOCKS of them; longer rows take the
-  // loop below, which quantizes after the wait).  nblk is a multiple of 16:
-  // the loop bounds are warp-uniform, and blocks 4m..4m+3 of a row (one
-  // lane group) have consecutive scale bytes, written as one 32-bit word by
-  // the group's first lane.
+  // (they depend only on x) and held in registers: lane L owns the block
+  // pairs L, L + 32, ... (blocks 2p and 2p + 1: one 16-byte unit of codes;
+  // at most AQ_MAX_PAIRS pairs, longer rows take the loop below, which
+  // quantizes after the wait).  nblk is a multiple of 16, so the loop bounds
+  // are warp-uniform; blocks 4m..4m+3 (lanes 2k, 2k + 1) have consecutive
+  // scale bytes, written as one 32-bit word by the even lane.
   const size_t row_bytes = (size_t)H / 2;
-  const int nb_lane = (nblk + 31) / 32;
-  if (nb_lane <= AQ_MAX_BLOCKS) {
-    uint2 packed[AQ_MAX_BLOCKS];
-    uint32_t sf4[AQ_MAX_BLOCKS];
+  const int npair = nblk / 2;
+  const int np_lane = (npair + 31) / 32;
+  if (np_lane <= AQ_MAX_PAIRS) {
+    uint4 packed[AQ_MAX_PAIRS];
+    uint32_t sf4[AQ_MAX_PAIRS];
 #pragma unroll
-    for (int i = 0; i < AQ_MAX_BLOCKS; ++i) {
-      if (i < nb_lane) {
-        const int b = 32 * i + lane;
-        uint32_t sf = 0;
-        packed[i] = make_uint2(0u, 0u);
-        if (b < nblk) {
+    for (int i = 0; i < AQ_MAX_PAIRS; ++i) {
+      if (i < np_lane) {
+        const int pr = 32 * i + lane;
+        uint32_t sf2 = 0;
+        packed[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (pr < npair) {
           float v[16];
-          bf16x16_to_f32(__ldg(xr + 2 * b), __ldg(xr + 2 * b + 1), v);
-          sf = nvfp4_quant_block16(v, gs, packed[i]);
+          uint2 c0, c1;
+          bf16x16_to_f32(__ldg(xr + 4 * pr), __ldg(xr + 4 * pr + 1), v);
+          const uint32_t s0 = nvfp4_quant_block16(v, gs, c0);
+          bf16x16_to_f32(__ldg(xr + 4 * pr + 2), __ldg(xr + 4 * pr + 3), v);
+          const uint32_t s1 = nvfp4_quant_block16(v, gs, c1);
+          packed[i] = make_uint4(c0.x, c0.y, c1.x, c1.y);
+          sf2 = s0 | (s1 << 8);
         }
-        sf4[i] = sf | (__shfl_down_sync(0xffffffffu, sf, 1) << 8) | (__shfl_down_sync(0xffffffffu, sf, 2) << 16) |
-                 (__shfl_down_sync(0xffffffffu, sf, 3) << 24);
+        sf4[i] = sf2 | (__shfl_down_sync(0xffffffffu, sf2, 1) << 16);
       }
     }
     pdl_wait();
     for (int j = 0; j < K; ++j) {
       const int prow = pad_row_of_src[(size_t)t * K + j];
 #pragma unroll
-      for (int i = 0; i < AQ_MAX_BLOCKS; ++i) {
-        const int b = 32 * i + lane;
-        if (i < nb_lane && b < nblk) {
-          *reinterpret_cast<uint2*>(a_codes + operand_offset(prow, 8 * b, (int)row_bytes)) = packed[i];
-          if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(a_sf + sf_atom_offset(prow, b, nblk)) = sf4[i];
+      for (int i = 0; i < AQ_MAX_PAIRS; ++i) {
+        const int pr = 32 * i + lane;
+        if (i < np_lane && pr < npair) {
+          *reinterpret_cast<uint4*>(a_codes + operand_offset(prow, 16 * pr, (int)row_bytes)) = packed[i];
+          if ((lane & 1) == 0) *reinterpret_cast<uint32_t*>(a_sf + sf_atom_offset(prow, 2 * pr, nblk)) = sf4[i];
         }
       }
       if (lane == 0) gs_rows[prow] = gs;

@@ -202,17 +202,13 @@ __device__ __forceinline__ void router_tile(const __nv_bfloat16* __restrict__ x,
   }
 }
 
-// The router kernel: one (token block, expert block) tile per CTA.  It also
-// clears the per-expert row counters the top-k kernel fills.
+// The router kernel: one (token block, expert block) tile per CTA.
 template <int TB, int EB, bool XALL>
 __global__ void __launch_bounds__(256) router_logits_kernel(const __nv_bfloat16* __restrict__ x,
                                                            const __nv_bfloat16* __restrict__ wg,
                                                            const float* __restrict__ bias,
-                                                           float* __restrict__ logits, int T, int H, int E,
-                                                           int32_t* __restrict__ counts) {
+                                                           float* __restrict__ logits, int T, int H, int E) {
   pdl_trigger();
-  if (blockIdx.x == 0 && blockIdx.y == 0)
-    for (int e = threadIdx.x; e < E; e += blockDim.x) counts[e] = 0;
   router_tile<TB, EB, XALL>(x, wg, bias, logits, T, H, E);
 }
 
@@ -316,11 +312,9 @@ __device__ __forceinline__ void topk_warp(const float* __restrict__ lrow, int E,
   else topk_warp_n<8, SMEM>(lrow, E, K, lane, e_lane, w_lane);
 }
 
-// One warp per token: the top-k choice and weights, and the per-expert row
-// counts.
+// One warp per token: the top-k choice and weights.
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int T, int E, int K,
-                                                  int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
-                                                  int32_t* __restrict__ counts) {
+                                                  int32_t* __restrict__ topk_ids, float* __restrict__ topk_w) {
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   pdl_trigger();
@@ -332,54 +326,75 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
   if (lane < K) {
     topk_ids[(size_t)t * K + lane] = e;
     topk_w[(size_t)t * K + lane] = w;
-    atomicAdd(&counts[e], 1);
   }
-}
-
-__device__ __forceinline__ int block_sum_int(int v, int* red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  int tot = 0;
-  for (int w = 0; w < nw; ++w) tot += red[w];
-  return tot;
 }
 
 constexpr int PERM_THREADS = 512;
 constexpr int PERM_TPT = 8;  // tokens per thread per pass
 
-// One CTA per expert: offsets from the counts, then a stable compaction of
-// the (token, slot) pairs that chose this expert, in token order.  The
-// expert's rows are cut into GEMM tiles of tile_rows (32 or 128) rows; each
-// tile starts its own 128-row block of the padded operand layout, so a tile's
-// rows always sit at the head of one block-scale atom.
-__global__ void __launch_bounds__(PERM_THREADS) permute_kernel(const int32_t* __restrict__ topk_ids,
-                                                              const int32_t* __restrict__ counts, int T, int K,
+// One CTA per expert: every expert's row count (a shared-memory histogram
+// of all the top-k ids, which the CTA reads anyway), offsets from the
+// counts, then a stable compaction of the (token, slot) pairs that chose this
+// expert, in token order.  The expert's rows are cut into GEMM tiles of
+// tile_rows (32 or 128) rows; each tile starts its own 128-row block of the
+// padded operand layout, so a tile's rows always sit at the head of one
+// block-scale atom.
+__global__ void __launch_bounds__(PERM_THREADS) permute_kernel(const int32_t* __restrict__ topk_ids, int T, int K,
                                                               int E, int tile_shift, PermuteOut o) {
   __shared__ int red[PERM_THREADS / 32];
+  __shared__ int hist[256];  // E <= 256
   const int e = blockIdx.x;
   const int tile_rows = 1 << tile_shift;   // 32 or 128 rows per GEMM tile
   pdl_trigger();
+  for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
   pdl_wait();
-  int c_lt = 0, p_lt = 0, n_lt = 0;
-  for (int i = threadIdx.x; i < e; i += blockDim.x) {
-    const int c = counts[i];
-    const int nt = (c + tile_rows - 1) >> tile_shift;
-    c_lt += c;
-    p_lt += nt * 128;                      // every tile starts a 128-row block
-    n_lt += nt;
+  // Tokens per thread per pass: up to PERM_TPT, fewer for small batches so
+  // that every warp takes part.  Up to PERM_THREADS * PERM_TPT tokens the
+  // histogram is filled by the compaction's own loads (one pass); above, by
+  // a pass of its own first.
+  const int tpt = min(PERM_TPT, (T + PERM_THREADS - 1) / PERM_THREADS);
+  const bool one_pass = T <= PERM_THREADS * PERM_TPT;
+  if (!one_pass) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < T * K; i += blockDim.x) atomicAdd(&hist[__ldg(topk_ids + i)], 1);
   }
-  const int off = block_sum_int(c_lt, red);
-  const int poff = block_sum_int(p_lt, red);
-  const int tbase = block_sum_int(n_lt, red);
-  const int cnt = counts[e];
+  int off = 0, poff = 0, tbase = 0, cnt = 0;
+  // offsets of this expert's rows, padded rows and tiles: sums over the
+  // experts below e by warp 0, broadcast through red[0..2] (all threads call)
+  auto offsets = [&]() {
+    __syncthreads();  // the histogram is complete
+    if (threadIdx.x < 32) {
+      int c_lt = 0, p_lt = 0, n_lt = 0;
+      for (int i = threadIdx.x; i < e; i += 32) {
+        const int c = hist[i];
+        const int nt = (c + tile_rows - 1) >> tile_shift;
+        c_lt += c;
+        p_lt += nt * 128;                  // every tile starts a 128-row block
+        n_lt += nt;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        c_lt += __shfl_xor_sync(0xffffffffu, c_lt, o);
+        p_lt += __shfl_xor_sync(0xffffffffu, p_lt, o);
+        n_lt += __shfl_xor_sync(0xffffffffu, n_lt, o);
+      }
+      if (threadIdx.x == 0) {
+        red[0] = c_lt;
+        red[1] = p_lt;
+        red[2] = n_lt;
+      }
+    }
+    __syncthreads();
+    off = red[0];
+    poff = red[1];
+    tbase = red[2];
+    cnt = hist[e];
+  };
+  if (!one_pass) offsets();
 
-  // Pass over PERM_THREADS * PERM_TPT tokens: warp w takes the block's
-  // tokens [w * 32 * PERM_TPT, +32 * PERM_TPT), lane l the tokens l, l + 32,
-  // ... of them, so one load instruction covers 32 consecutive token rows.
+  // Pass over PERM_THREADS * tpt tokens: warp w takes the block's tokens
+  // [w * 32 * tpt, +32 * tpt), lane l the tokens l, l + 32, ... of them, so
+  // one load instruction covers 32 consecutive token rows.
   // A row's rank among the expert's rows (token order) is: the rows of the
   // earlier passes (carry), of the earlier warps (a scan over the warps'
   // counts), of the warp's earlier 32-token groups, and of the lower lanes
@@ -387,8 +402,8 @@ __global__ void __launch_bounds__(PERM_THREADS) permute_kernel(const int32_t* __
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned lanes_below = (1u << lane) - 1u;
   int carry = 0;
-  for (int base = 0; base < T; base += PERM_THREADS * PERM_TPT) {
-    const int wbase = base + warp * 32 * PERM_TPT;
+  for (int base = 0; base < T; base += PERM_THREADS * tpt) {
+    const int wbase = base + warp * 32 * tpt;
     int slot[PERM_TPT];
     unsigned bal[PERM_TPT];
     int wcount = 0;
@@ -396,7 +411,7 @@ __global__ void __launch_bounds__(PERM_THREADS) permute_kernel(const int32_t* __
     for (int i = 0; i < PERM_TPT; ++i) {
       slot[i] = -1;
       const int t = wbase + 32 * i + lane;
-      if (t < T) {
+      if (i < tpt && t < T) {
         // the token's K <= 16 ids into registers first (16- or 8-byte loads
         // when K allows), then the comparisons
         int id[16];
@@ -426,11 +441,15 @@ __global__ void __launch_bounds__(PERM_THREADS) permute_kernel(const int32_t* __
         }
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-          if (j < K && id[j] == e) slot[i] = j;
+          if (j < K) {
+            if (id[j] == e) slot[i] = j;
+            if (one_pass) atomicAdd(&hist[id[j]], 1);
+          }
       }
       bal[i] = __ballot_sync(0xffffffffu, slot[i] >= 0);
       wcount += __popc(bal[i]);
     }
+    if (one_pass) offsets();
     // exclusive scan of the warps' counts
     __syncthreads();  // red[] is free again (previous pass or block sums)
     if (lane == 0) red[warp] = wcount;
@@ -774,13 +793,13 @@ __global__ void __launch_bounds__(256, 1) front_small_kernel(const __grid_consta
 
 template <int TB, int EB, bool XALL>
 cudaError_t launch_router_t(const void* x, const void* gate_w, const float* bias, float* logits, int T, int H,
-                            int E, int32_t* counts, cudaStream_t s) {
+                            int E, cudaStream_t s) {
   dim3 grid((T + ROUTER_WARPS * TB - 1) / (ROUTER_WARPS * TB), E / EB);
   const size_t smem = (size_t)H * EB * 2;
   // first kernel of a forward: ordinary stream order (it may depend on the caller's work)
   return launch_k(router_logits_kernel<TB, EB, XALL>, grid, dim3(256), smem, s, false,
                   reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<const __nv_bfloat16*>(gate_w), bias,
-                  logits, T, H, E, counts);
+                  logits, T, H, E);
 }
 
 // Expert block: the widest of 32 / 16 / 8 experts that divides E and keeps
@@ -958,26 +977,27 @@ cudaError_t launch_front_small(FrontArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_router_logits(const void* x, const void* gate_w, const float* bias, float* logits, int T,
-                                 int H, int E, int32_t* counts, cudaStream_t s) {
+                                 int H, int E, cudaStream_t s) {
   const int eb = router_eb(H, E);
   const bool small = router_small(T, H);
-  if (eb == 32) return small ? launch_router_t<2, 32, true>(x, gate_w, bias, logits, T, H, E, counts, s)
-                             : launch_router_t<4, 32, false>(x, gate_w, bias, logits, T, H, E, counts, s);
-  if (eb == 16) return small ? launch_router_t<2, 16, true>(x, gate_w, bias, logits, T, H, E, counts, s)
-                             : launch_router_t<4, 16, false>(x, gate_w, bias, logits, T, H, E, counts, s);
-  return small ? launch_router_t<4, 8, true>(x, gate_w, bias, logits, T, H, E, counts, s)
-               : launch_router_t<4, 8, false>(x, gate_w, bias, logits, T, H, E, counts, s);
+  if (eb == 32) return small ? launch_router_t<2, 32, true>(x, gate_w, bias, logits, T, H, E, s)
+                             : launch_router_t<4, 32, false>(x, gate_w, bias, logits, T, H, E, s);
+  if (eb == 16) return small ? launch_router_t<2, 16, true>(x, gate_w, bias, logits, T, H, E, s)
+                             : launch_router_t<4, 16, false>(x, gate_w, bias, logits, T, H, E, s);
+  return small ? launch_router_t<4, 8, true>(x, gate_w, bias, logits, T, H, E, s)
+               : launch_router_t<4, 8, false>(x, gate_w, bias, logits, T, H, E, s);
 }
 
 cudaError_t launch_topk(const float* logits, int T, int E, int K, int32_t* topk_ids, float* topk_w,
-                        int32_t* counts, cudaStream_t s) {
-  return launch_k(topk_kernel, dim3((T + 7) / 8), dim3(256), 0, s, true, logits, T, E, K, topk_ids, topk_w, counts);
+                        cudaStream_t s) {
+  return launch_k(topk_kernel, dim3((T + 7) / 8), dim3(256), 0, s, true, logits, T, E, K, topk_ids, topk_w);
 }
 
-cudaError_t launch_permute(const int32_t* topk_ids, const int32_t* counts, int T, int K, int E, int tile_rows,
+cudaError_t launch_permute(const int32_t* topk_ids, int T, int K, int E, int tile_rows,
                            const PermuteOut& o, cudaStream_t s) {
   const int shift = tile_rows == 32 ? 5 : 7;
-  return launch_k(permute_kernel, dim3(E), dim3(PERM_THREADS), 0, s, true, topk_ids, counts, T, K, E, shift, o);
+  if (E > 256) return cudaErrorInvalidValue;
+  return launch_k(permute_kernel, dim3(E), dim3(PERM_THREADS), 0, s, true, topk_ids, T, K, E, shift, o);
 }
 
 }  // namespace moe

@@ -47,7 +47,7 @@ struct moe_handle {
 
   // routing workspace
   float* logits = nullptr;
-  int32_t *topk_ids = nullptr, *counts = nullptr, *expert_offsets = nullptr;
+  int32_t *topk_ids = nullptr, *expert_offsets = nullptr;
   float* topk_w = nullptr;
   int32_t *src_of_row = nullptr, *row_of_src = nullptr, *pad_row_of_src = nullptr, *src_of_padrow = nullptr;
   int4* tiles = nullptr;
@@ -383,13 +383,13 @@ moe_status forward_impl(moe_handle* h, const void* x, const void* gate_w, const 
       CK(h, launch_front_small(fa, s));
       for (int i = 1; i <= 4; ++i) CK(h, mark(h, i, s));
     } else {
-      CK(h, launch_router_logits(x, gate_w, bias, h->logits, T, H, E, h->counts, s));
+      CK(h, launch_router_logits(x, gate_w, bias, h->logits, T, H, E, s));
       CK(h, mark(h, 1, s));
-      CK(h, launch_topk(h->logits, T, E, K, h->topk_ids, h->topk_w, h->counts, s));
+      CK(h, launch_topk(h->logits, T, E, K, h->topk_ids, h->topk_w, s));
       CK(h, mark(h, 2, s));
       PermuteOut po{h->expert_offsets, h->src_of_row, h->row_of_src, h->pad_row_of_src,
                     h->src_of_padrow,  h->tiles,      h->num_tiles};
-      CK(h, launch_permute(h->topk_ids, h->counts, T, K, E, tile_rows, po, s));
+      CK(h, launch_permute(h->topk_ids, T, K, E, tile_rows, po, s));
       CK(h, mark(h, 3, s));
       CK(h, launch_act_quant(x, T, H, K, h->pad_row_of_src, h->a_codes, h->a_sf, h->gs_rows,
                              h->static_scales ? h->static_x_gs : nullptr,
@@ -572,7 +572,6 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
   A(h->logits, sizeof(float) * (size_t)T * E);
   A(h->topk_ids, sizeof(int32_t) * (size_t)T * K);
   A(h->topk_w, sizeof(float) * (size_t)T * K);
-  A(h->counts, sizeof(int32_t) * E);
   A(h->expert_offsets, sizeof(int32_t) * (E + 1));
   A(h->src_of_row, sizeof(int32_t) * (size_t)h->Rmax);
   A(h->row_of_src, sizeof(int32_t) * (size_t)h->Rmax);

@@ -23,12 +23,11 @@
 #include "moe_nvfp4.h"
 
 static constexpr size_t LOGITS_BYTES = sizeof(float) * (size_t)MOE_ROUTE_NOALLOC_MAX_LOGITS;
-static constexpr size_t COUNTS_BYTES = sizeof(int32_t) * 256;  // one counter per expert, E <= 256
 
-// The whole scratch of the routing: [logits: MOE_ROUTE_NOALLOC_MAX_LOGITS
-// floats (4 MiB) | counts: 256 int32].  One copy per device, created when the
-// library's device code is loaded on that device.
-static __device__ __align__(256) unsigned char g_route_scratch[LOGITS_BYTES + COUNTS_BYTES];
+// The whole scratch of the routing: the logits, MOE_ROUTE_NOALLOC_MAX_LOGITS
+// floats (4 MiB).  One copy per device, created when the library's device
+// code is loaded on that device.
+static __device__ __align__(256) unsigned char g_route_scratch[LOGITS_BYTES];
 
 namespace {
 
@@ -101,11 +100,9 @@ moe_status moe_route_noalloc(const void* x, const void* gate_w, const float* gat
   if (moe::router_smem_bytes(H, E) > d->smem_cap) return MOE_ERR_UNSUPPORTED;
 
   float* logits = reinterpret_cast<float*>(d->base);
-  int32_t* counts = reinterpret_cast<int32_t*>(d->base + LOGITS_BYTES);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the logits kernel clears counts[0, E) before the top-k kernel adds to them
-  cudaError_t e = moe::launch_router_logits(x, gate_w, gate_bias, logits, T, H, E, counts, s);
-  if (e == cudaSuccess) e = moe::launch_topk(logits, T, E, K, topk_ids, topk_w, counts, s);
+  cudaError_t e = moe::launch_router_logits(x, gate_w, gate_bias, logits, T, H, E, s);
+  if (e == cudaSuccess) e = moe::launch_topk(logits, T, E, K, topk_ids, topk_w, s);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return MOE_ERR_CUDA;
