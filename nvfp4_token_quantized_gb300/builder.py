@@ -3,9 +3,11 @@
 Compiles every ``csrc/*.cu`` translation unit with nvcc (in parallel, one
 ``-gencode`` for sm_103a) and links them into
 ``nvfp4_token_quantized_gb300/_lib/libmoe_nvfp4.so``.  The CUDA runtime is
-linked statically and the kernels move their operands with plain bulk copies
-(no tensor maps), so the library needs no link against libcuda.  Works the
-same on x86_64 and aarch64 hosts (no host-architecture flags).
+linked statically; the GEMM operands move by plain bulk copies, and the one
+tensor map (the small-batch front kernel's router-weight ring) is encoded
+through the runtime's driver entry point, so the library needs no link
+against libcuda.  Works the same on x86_64 and aarch64 hosts (no
+host-architecture flags).
 """
 
 from __future__ import annotations
