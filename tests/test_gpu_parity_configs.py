@@ -248,3 +248,24 @@ def test_stress_refresh_replay_equals_fresh():
     _check_output(refreshed, wl_b, tokens, "stress after refresh", layer)
     _check_weight_quant(layer, wl_b, [0, 63])
     layer.close()
+
+
+@pytest.mark.parametrize("T,H,E,K", [(5000, 256, 16, 4), (80, 4352, 8, 2)])
+def test_long_batch_and_wide_rows(T, H, E, K):
+    """Paths the benchmark shapes do not reach: more than 4096 tokens (the
+    permutation counts its experts in a pass of its own before ranking) and
+    rows wider than 4096 elements (the activation quantizer forms codes after
+    its dependency wait instead of holding them in registers).  Routing, the
+    whole permutation and every token's quantization are bit-exact; every
+    token's output is checked as in the other workloads."""
+    shape = synthetic.MoEShape(name="edge", T=T, H=H, E=E, K=K, I=128, max_num_tokens=T)
+    wl = synthetic.make_workload(shape, T=T, seed=5)
+    d = to_dev(wl)
+    layer = _layer(shape)
+    layer.load_weights(d["w13"], d["w2"])
+    out = layer.forward(d["x"], d["gate_w"])
+    torch.cuda.synchronize()
+    _check_routing(layer, wl, full_permutation=True)
+    _check_act_quant(layer, wl)
+    _check_output(out, wl, np.arange(T), f"T={T} H={H}", layer)
+    layer.close()

@@ -146,3 +146,4 @@ def test_tied_logits_take_the_lower_expert(E, K, T):
     assert np.array_equal(got, ids), "tie order differs from the oracle"
     np.testing.assert_allclose(r["topk_w"].cpu().numpy(), weights, rtol=1e-5, atol=1e-7)
     layer.close()
+
