@@ -13,13 +13,15 @@
 //               256 rows of pre-swizzled codes are contiguous) - running
 //               ahead across unit boundaries;
 //   warp 1      tensor-memory allocation and the single MMA-issuing thread:
-//               block scales shared -> tensor memory (tcgen05.cp), then four
-//               K=64 MMAs per 256-element stage: N = 256 into the one
+//               four K=64 MMAs per 256-element stage: N = 256 into the one
 //               256-column accumulator (pairs), or N = 128 into one of two
 //               128-column buffers (plain);
 //   warps 2-9   epilogue, two warps per tensor-memory lane quadrant: warp w
 //               reads lanes [32 (w % 4), +32) and takes column half
-//               (w - 2) / 4 of every accumulator, one row per thread.
+//               (w - 2) / 4 of every accumulator, one row per thread;
+//   warp 10     per stage, the block scales shared -> tensor memory
+//               (tcgen05.cp), committed to a barrier the MMA thread waits
+//               on, so that the copies' issue runs ahead of the MMAs.
 // With two accumulator buffers (plain) the epilogue drains unit u while the
 // tensor cores compute unit u+1; with one 256-column accumulator (pairs) the
 // tensor cores wait only for the epilogue's tensor-memory reads (each thread
@@ -80,9 +82,12 @@ constexpr int TMEM_SF_STAGE_PAIR = 48;       // 16 columns SFA + 32 columns SFB 
 constexpr uint32_t IDESC_PAIR = idesc_fp4(TILE_M, 2 * TILE_N);
 constexpr int MAX_STAGES_PAIR = 5;
 constexpr int EPI_WARPS = 8;
-constexpr int THREADS = 64 + 32 * EPI_WARPS;
+// warp 0 producer, warp 1 MMA issuer, warps 2..9 epilogue, warp 10 the block
+// scales' copies to tensor memory
+constexpr int SF_WARP = 2 + EPI_WARPS;
+constexpr int THREADS = 64 + 32 * EPI_WARPS + 32;
 constexpr int HALF_MAX_BYTES = 2 * 2 * TILE_M * 4;  // w13: per-half row maxima, two m-tile buffers
-constexpr int CTRL_BYTES = 256;
+constexpr int CTRL_BYTES = 384;
 // Ordered w2 epilogue: each epilogue warp stages its 32 rows, 64 columns
 // (128 bytes of bf16) at a time, in shared memory with a 16-byte pad per row
 // (conflict-free 16-byte writes of one row per lane, reads of one row per 8
@@ -118,6 +123,8 @@ struct Ctrl {
   // epilogue warps (q_empty)
   uint64_t q_full[UNIT_QUEUE];
   uint64_t q_empty[UNIT_QUEUE];
+  // a stage's block scales are in tensor memory (committed by the scale warp)
+  uint64_t sf_ready[MAX_STAGES];
   uint32_t tmem_base;
   int abort_flag;
   int q_unit[UNIT_QUEUE];
@@ -317,6 +324,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&c.full[s], 1);
       mbar_init(&c.empty[s], 1);
+      mbar_init(&c.sf_ready[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&c.acc_full[b], 1);
@@ -325,7 +333,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
     mbar_init(&c.a_full, 1);
     for (int q = 0; q < UNIT_QUEUE; ++q) {
       mbar_init(&c.q_full[q], 1);
-      mbar_init(&c.q_empty[q], 1 + EPI_WARPS);
+      mbar_init(&c.q_empty[q], 2 + EPI_WARPS);  // the MMA thread, the scale warp, the epilogue warps
     }
     c.abort_flag = 0;
     if (MODE == MODE_W13)
@@ -406,6 +414,17 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
     for (int e = threadIdx.x; e < p.num_experts; e += blockDim.x) p.expert_done[e] = 0;
   }
   const int nunits = count_units();
+  // block scales of one stage, shared memory -> tensor memory
+  auto copy_stage_scales = [&](uint32_t sfa_t, uint32_t sfb_t, const uint8_t* slot_a, const uint8_t* slot_b) {
+    constexpr int SFB_COLS = PAIR ? 8 : 4;  // B scale columns per K block
+#pragma unroll
+    for (int kb = 0; kb < 4; ++kb) {
+      tc_copy_sf(sfa_t + kb * 4, smem_desc_sf(smem_u32(slot_a + kb * SF_ATOM_BYTES)));
+      tc_copy_sf(sfb_t + kb * SFB_COLS, smem_desc_sf(smem_u32(slot_b + kb * SF_ATOM_BYTES)));
+      if (PAIR)
+        tc_copy_sf(sfb_t + kb * SFB_COLS + 4, smem_desc_sf(smem_u32(slot_b + OPERAND_SF_BYTES + kb * SF_ATOM_BYTES)));
+    }
+  };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -509,7 +528,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
         const uint32_t d_tmem = tmem + buf * TILE_N;
         for (int ks = 0; ks < KS; ++ks, ++g) {
           const int s = g % STAGES;
-          if (!mbar_wait_bounded(&c.full[s], (g / STAGES) & 1, &c.abort_flag)) {
+          // the stage's operands landed, and the scale warp's copies of its
+          // block scales completed
+          if (!mbar_wait_bounded(&c.full[s], (g / STAGES) & 1, &c.abort_flag) ||
+              !mbar_wait_bounded(&c.sf_ready[s], (g / STAGES) & 1, &c.abort_flag)) {
             c.abort_flag = 1;
             report_device_error(p.status, DEV_ERR_TIMEOUT);
             break;
@@ -520,14 +542,6 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
           const uint8_t* slot_a = sA + (ARES ? ks : s) * A_SLOT;
           const uint8_t* slot_b = sB + s * BS;
           constexpr int SFB_COLS = PAIR ? 8 : 4;  // B scale columns per K block
-#pragma unroll
-          for (int kb = 0; kb < 4; ++kb) {
-            tc_copy_sf(sfa_t + kb * 4, smem_desc_sf(smem_u32(slot_a + kb * SF_ATOM_BYTES)));
-            tc_copy_sf(sfb_t + kb * SFB_COLS, smem_desc_sf(smem_u32(slot_b + kb * SF_ATOM_BYTES)));
-            if (PAIR)
-              tc_copy_sf(sfb_t + kb * SFB_COLS + 4,
-                         smem_desc_sf(smem_u32(slot_b + OPERAND_SF_BYTES + kb * SF_ATOM_BYTES)));
-          }
           const uint32_t a_base = smem_u32(slot_a + OPERAND_SF_BYTES);
           const uint32_t b_base = smem_u32(slot_b + (PAIR ? 2 : 1) * OPERAND_SF_BYTES);
 #pragma unroll
@@ -539,6 +553,37 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
         // Always signal, even after an abort: the epilogue waits for the
         // MMAs already issued before it lets tensor memory go.
         tc_commit(&c.acc_full[buf]);
+      }
+    }
+    __syncwarp();
+  } else if (warp == SF_WARP) {
+    if (lane == 0) {
+      // ---------------- block-scale copies ----------------
+      // Per stage, once its operands landed: the block scales into the
+      // stage's tensor-memory slot, committed to sf_ready[s] for the MMA
+      // thread.  (A slot's previous scales were read by the MMAs of the
+      // stage STAGES earlier, which completed before the producer refilled
+      // the ring slot whose landing this waits for.)
+      bool ok = !ARES || first >= nunits || mbar_wait_bounded(&c.a_full, 0, &c.abort_flag);
+      uint32_t g = 0;
+      for (int n = 0; ok; ++n) {
+        const int u = dyn ? queued_unit(n, true) : static_unit(n);
+        if (u < 0 || c.abort_flag) break;
+        for (int ks = 0; ks < KS; ++ks, ++g) {
+          const int s = g % STAGES;
+          if (!mbar_wait_bounded(&c.full[s], (g / STAGES) & 1, &c.abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sfa_t = tmem + TMEM_SF_BASE + s * SF_STAGE;
+          copy_stage_scales(sfa_t, sfa_t + 16, sA + (ARES ? ks : s) * A_SLOT, sB + s * BS);
+          tc_commit(&c.sf_ready[s]);
+        }
+      }
+      if (!ok) {
+        c.abort_flag = 1;
+        report_device_error(p.status, DEV_ERR_TIMEOUT);
       }
     }
     __syncwarp();
