@@ -1,13 +1,13 @@
 // route_noalloc.cu - moe_route_noalloc: router logits, top-k selection and
 // renormalised routing weights without a handle and without allocating.
 //
-// The routing arithmetic is the forward's own: the same router-tile and top-k
-// device functions (moe_forward runs them as router_logits_kernel and
-// topk_kernel above 64 tokens, and inside front_small_kernel at or below), so
-// the result is bit-identical to the routing moe_forward computes.  The only
-// difference is where the intermediate lives: the FP32 logits [T, E] and the
-// per-expert row counters go to one file-scope device array of fixed size
-// instead of a handle's workspace.
+// The routing arithmetic is the forward's own: the kernels moe_forward runs
+// above 64 tokens (router_logits_kernel, topk_kernel); at or below 64 tokens
+// moe_forward forms the logits inside front_small_kernel in the same
+// canonical FP32 order and selects with the same warp top-k, so the result is
+// bit-identical to the routing moe_forward computes.  The only difference is
+// where the intermediate lives: the FP32 logits [T, E] go to one file-scope
+// device array of fixed size instead of a handle's workspace.
 //
 // The first call on a device does the set-up for that device (looks the
 // array's address up and raises the router kernel's shared-memory cap).  With
