@@ -1,6 +1,6 @@
 """moe_route_noalloc: routing with no handle and no device allocation.
 
-Its scratch (router logits and per-expert counters) is a fixed array in the
+Its scratch (the router logits) is a fixed array in the
 library's device code.  Checked against the routing the handle-based forward
 computes for the same inputs (moe_forward_ex, read back with
 moe_debug_routing), on two calls in a row; the size limit is refused before
