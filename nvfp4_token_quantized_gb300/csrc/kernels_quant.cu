@@ -92,8 +92,10 @@ __global__ void __launch_bounds__(256, 4) act_quant_kernel(const __nv_bfloat16* 
       }
     }
     pdl_wait();
+    // the K expanded rows, loaded at once (lane j holds row j)
+    const int my_prow = lane < K ? pad_row_of_src[(size_t)t * K + lane] : 0;
     for (int j = 0; j < K; ++j) {
-      const int prow = pad_row_of_src[(size_t)t * K + j];
+      const int prow = __shfl_sync(0xffffffffu, my_prow, j);
 #pragma unroll
       for (int i = 0; i < AQ_MAX_PAIRS; ++i) {
         const int pr = 32 * i + lane;
@@ -108,6 +110,7 @@ __global__ void __launch_bounds__(256, 4) act_quant_kernel(const __nv_bfloat16* 
   }
 
   pdl_wait();
+  const int my_prow = lane < K ? pad_row_of_src[(size_t)t * K + lane] : 0;
   for (int b0 = 0; b0 < nblk; b0 += 32) {
     const int b = b0 + lane;
     const bool active = b < nblk;
@@ -120,15 +123,15 @@ __global__ void __launch_bounds__(256, 4) act_quant_kernel(const __nv_bfloat16* 
     }
     const uint32_t sf4 = sf | (__shfl_down_sync(0xffffffffu, sf, 1) << 8) | (__shfl_down_sync(0xffffffffu, sf, 2) << 16) |
                          (__shfl_down_sync(0xffffffffu, sf, 3) << 24);
-    if (active) {
-      for (int j = 0; j < K; ++j) {
-        const int prow = pad_row_of_src[(size_t)t * K + j];
+    for (int j = 0; j < K; ++j) {
+      const int prow = __shfl_sync(0xffffffffu, my_prow, j);
+      if (active) {
         *reinterpret_cast<uint2*>(a_codes + operand_offset(prow, 8 * b, (int)row_bytes)) = packed;
         if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(a_sf + sf_atom_offset(prow, b, nblk)) = sf4;
       }
     }
   }
-  if (lane < K) gs_rows[pad_row_of_src[(size_t)t * K + lane]] = gs;
+  if (lane < K) gs_rows[my_prow] = gs;
 }
 
 // Requantization of the small-batch w13 output: one warp per expanded row

@@ -343,10 +343,12 @@ __global__ void __launch_bounds__(PERM_THREADS) permute_kernel(const int32_t* __
                                                               int E, int tile_shift, PermuteOut o) {
   __shared__ int red[PERM_THREADS / 32];
   __shared__ int hist[256];  // E <= 256
+  // per-warp histograms (no contention between warps), summed into hist
+  __shared__ int hist_w[PERM_THREADS / 32][256];
   const int e = blockIdx.x;
   const int tile_rows = 1 << tile_shift;   // 32 or 128 rows per GEMM tile
   pdl_trigger();
-  for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
+  for (int i = threadIdx.x; i < (PERM_THREADS / 32) * 256; i += blockDim.x) (&hist_w[0][0])[i] = 0;
   pdl_wait();
   // Tokens per thread per pass: up to PERM_TPT, fewer for small batches so
   // that every warp takes part.  Up to PERM_THREADS * PERM_TPT tokens the
@@ -356,13 +358,20 @@ __global__ void __launch_bounds__(PERM_THREADS) permute_kernel(const int32_t* __
   const bool one_pass = T <= PERM_THREADS * PERM_TPT;
   if (!one_pass) {
     __syncthreads();
-    for (int i = threadIdx.x; i < T * K; i += blockDim.x) atomicAdd(&hist[__ldg(topk_ids + i)], 1);
+    for (int i = threadIdx.x; i < T * K; i += blockDim.x) atomicAdd(&hist_w[threadIdx.x >> 5][__ldg(topk_ids + i)], 1);
   }
   int off = 0, poff = 0, tbase = 0, cnt = 0;
   // offsets of this expert's rows, padded rows and tiles: sums over the
   // experts below e by warp 0, broadcast through red[0..2] (all threads call)
   auto offsets = [&]() {
-    __syncthreads();  // the histogram is complete
+    __syncthreads();  // the warps' histograms are complete
+    for (int i = threadIdx.x; i < E; i += blockDim.x) {
+      int c = 0;
+#pragma unroll
+      for (int w = 0; w < PERM_THREADS / 32; ++w) c += hist_w[w][i];
+      hist[i] = c;
+    }
+    __syncthreads();
     if (threadIdx.x < 32) {
       int c_lt = 0, p_lt = 0, n_lt = 0;
       for (int i = threadIdx.x; i < e; i += 32) {
@@ -443,7 +452,7 @@ __global__ void __launch_bounds__(PERM_THREADS) permute_kernel(const int32_t* __
         for (int j = 0; j < 16; ++j)
           if (j < K) {
             if (id[j] == e) slot[i] = j;
-            if (one_pass) atomicAdd(&hist[id[j]], 1);
+            if (one_pass) atomicAdd(&hist_w[threadIdx.x >> 5][id[j]], 1);
           }
       }
       bal[i] = __ballot_sync(0xffffffffu, slot[i] >= 0);
