@@ -876,7 +876,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_fp4_kernel(const __grid_const
           // through the warp's staging rows (the warp's calls are uniform:
           // warp_rows is; rows without a routed token store nothing)
           if (warp_rows) {
-            const int col = (un.col + half) * TILE_N;
+            const int col = PAIR ? (un.col + half) * TILE_N : un.col * TILE_N + 64 * half;
             const int my_src = (ready && row_ok) ? src : -1;
             uint8_t* stg = epi_stage + (warp - 2) * (32 * EPI_ROW_STRIDE);
 #pragma unroll
