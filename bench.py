@@ -52,12 +52,17 @@ FP4_OVER_BF16 = 6.0
 
 def kernels_per_forward(s, T, shared_inter=0):
     """Kernel launches of one forward: router, top-k, permute, quantize, w13,
-    w2, finalize.  Up to 64 tokens: one fused front end, w13, the row
-    requantization, w2, finalize (the bench runs per-token scales).  A shared
-    expert adds its own stream's tile list, quantize, w13, w2, and up to 64
-    tokens the row requantization between them."""
+    w2, finalize.  Up to 64 tokens: one fused front end, w13, w2, finalize,
+    plus the row requantization kernel unless nearly every expert gets a row
+    (T*K >= 4E: the w13 GEMM then requantizes in its own tail; the bench runs
+    per-token scales).  A shared expert adds its own stream's tile list,
+    quantize, w13, w2, and up to 64 tokens the row requantization between
+    them."""
     shared = (5 if T <= SMALL_BATCH_TOKENS else 4) if shared_inter else 0
-    return (7 if T > SMALL_BATCH_TOKENS else 5) + shared
+    if T > SMALL_BATCH_TOKENS:
+        return 7 + shared
+    all_experts = T * s.K >= 4 * s.E
+    return (4 if all_experts else 5) + shared
 
 
 def ordered_finalize(s, T):
