@@ -100,9 +100,10 @@ struct FrontArgs {
   int32_t* num_tiles;
   uint32_t* sync;             // FRONT_SYNC_WORDS counters, zero between launches
   const float* static_gs;     // calibrated per-tensor scale (static contract), or nullptr
-  // The GEMMs run the all-experts schedule and do not wait for the grouping
-  // (expert_offsets, src_of_row, row_of_src, pad_row_of_src, tiles): the
-  // requantization kernel derives it instead.
+  // The GEMMs run the all-experts schedule: they take the activations and
+  // the routing from the sync counters and do not wait for the grouping
+  // (expert_offsets, src_of_row, row_of_src, pad_row_of_src, tiles), which
+  // the last front CTA to publish its routing derives off their path.
   int all_experts;
   int* status;                // device status word (a bounded wait that ran out)
 };
