@@ -29,6 +29,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -392,12 +393,21 @@ def measured_peaks():
 GEMM_SOURCES = ("common.cuh", "kernels.h", "kernels_gemm.cu", "moe_host.cu")
 
 
+def _code_only(text):
+    """C++ source with its comments removed and whitespace collapsed, so that
+    a comment edit does not count as a change of the kernel.  (The GEMM
+    sources hold no string literal with a comment marker in it.)"""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "nvfp4_token_quantized_gb300", "csrc")
     for f in GEMM_SOURCES:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(f.encode() + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
