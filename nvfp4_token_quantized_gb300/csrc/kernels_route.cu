@@ -20,6 +20,13 @@ namespace moe {
 namespace {
 
 constexpr int ROUTER_WARPS = 8;
+// Large batches: each warp's activations stream through a shared-memory
+// ring of ROUTER_XRING rounds, filled two rounds ahead by cp.async.
+constexpr int ROUTER_XRING = 3;
+// Bytes of a router instantiation's activation ring (0 for XALL).
+__host__ __device__ constexpr int router_xring_bytes(int TB, bool XALL, int WARPS) {
+  return XALL ? 0 : WARPS * ROUTER_XRING * TB * 512;
+}
 
 // Swizzle of the 16-byte units of one (k, partial) row of the staged router
 // weight so that the 8 lanes of one shared-memory wavefront hit distinct banks.
@@ -42,9 +49,10 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
 }
 
 // Logits of one (token block, expert block) tile, for a CTA of a grid
-// (ceil(T / (8*TB)), E / EB) of 256 threads = 8 warps; dynamic shared
+// (ceil(T / (WARPS*TB)), E / EB) of WARPS warps; dynamic shared
 // memory H * EB * 2 bytes holding the CTA's whole router-weight slice,
-// laid out [round j][k][partial p][EB] (row h = 256 j + 8 p + k).
+// laid out [round j][k][partial p][EB] (row h = 256 j + 8 p + k), then
+// (without XALL) the warps' activation rings.
 // Warp w handles tokens t0..t0+TB-1; lane p is partial p of every
 // (token, expert) pair of the CTA's expert block: it accumulates chunks
 // c = p, p+32, ... in ascending order with one fused multiply-add per element,
@@ -52,9 +60,11 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
 //
 // XALL: every round's activations are loaded into registers up front (one
 // memory round trip; H <= 2048), for small token counts where latency rules.
+// Otherwise round j's activations arrive in ring slot j % ROUTER_XRING,
+// copied two rounds ahead.
 // Ends with a __syncthreads-free store of the logits; the caller may reuse
 // the shared memory only after its own barrier.
-template <int TB, int EB, bool XALL>
+template <int TB, int EB, bool XALL, int WARPS>
 __device__ __forceinline__ void router_tile(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ wg,
                                             const float* __restrict__ bias, float* __restrict__ logits, int T,
                                             int H, int E) {
@@ -65,10 +75,10 @@ __device__ __forceinline__ void router_tile(const __nv_bfloat16* __restrict__ x,
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e0 = blockIdx.y * EB;
-  const int t0 = (blockIdx.x * ROUTER_WARPS + warp) * TB;
+  const int t0 = (blockIdx.x * WARPS + warp) * TB;
   const int rounds = H / 256;
 
-  for (int h = threadIdx.x; h < H; h += 256) {
+  for (int h = threadIdx.x; h < H; h += 32 * WARPS) {
     const int j = h >> 8, hr = h & 255, k = hr & 7, p = (hr >> 3) & 31;
     const char* src = reinterpret_cast<const char*>(wg + (size_t)h * E + e0);
 #pragma unroll
@@ -87,16 +97,37 @@ __device__ __forceinline__ void router_tile(const __nv_bfloat16* __restrict__ x,
       xv[t] = tok < T ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok * H + 8 * c)) : make_uint4(0, 0, 0, 0);
     }
   };
-  constexpr int XR = XALL ? 8 : 2;              // rounds of activations held in registers
+  // the activation ring: this warp's after the weight slice, slot r, token
+  // t, lane p at [r][t][p]; each lane copies and later reads only its own
+  // 16-byte pieces, so the ring needs no barrier (rows past T read as zeros)
+  uint4* xs_w = sw + (size_t)H * EB * 2 / 16 + (size_t)warp * ROUTER_XRING * TB * 32;
+  auto issue_x = [&](int j) {
+    const int c = j * 32 + lane;
+    uint4* slot = xs_w + (j % ROUTER_XRING) * TB * 32;
+#pragma unroll
+    for (int t = 0; t < TB; ++t) {
+      const int tok = t0 + t;
+      const __nv_bfloat16* src = x + (tok < T ? (size_t)tok * H + 8 * c : 0);
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(slot + t * 32 + lane)), "l"(src),
+                   "r"(tok < T ? 16 : 0)
+                   : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  constexpr int XR = XALL ? 8 : 1;              // rounds of activations held in registers
   uint4 xb[XR][TB];
   if constexpr (XALL) {
 #pragma unroll
     for (int j = 0; j < XR; ++j)
       if (j < rounds) load_x(j, xb[j]);
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
   } else {
-    load_x(0, xb[0]);
+    issue_x(0);
+    if (rounds > 1) issue_x(1);
+    // the weight slice (the oldest group) has landed
+    if (rounds > 1) asm volatile("cp.async.wait_group 2;" ::: "memory");
+    else asm volatile("cp.async.wait_group 1;" ::: "memory");
   }
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
   __syncthreads();
 
   float2 acc[TB][EB / 2];
@@ -134,13 +165,16 @@ __device__ __forceinline__ void router_tile(const __nv_bfloat16* __restrict__ x,
     for (int j = 0; j < XR; ++j)
       if (j < rounds) round_fma(j, xb[j]);
   } else {
-    for (int j = 0; j < rounds; j += 2) {   // two register buffers, fixed indices
-      if (j + 1 < rounds) load_x(j + 1, xb[1]);
+    for (int j = 0; j < rounds; ++j) {
+      if (j + 2 < rounds) issue_x(j + 2);   // into the slot round j - 1 used
+      // groups issued after round j's may stay in flight
+      if (j + 2 < rounds) asm volatile("cp.async.wait_group 2;" ::: "memory");
+      else if (j + 1 < rounds) asm volatile("cp.async.wait_group 1;" ::: "memory");
+      else asm volatile("cp.async.wait_group 0;" ::: "memory");
+      const uint4* slot = xs_w + (j % ROUTER_XRING) * TB * 32;
+#pragma unroll
+      for (int t = 0; t < TB; ++t) xb[0][t] = slot[t * 32 + lane];
       round_fma(j, xb[0]);
-      if (j + 1 < rounds) {
-        if (j + 2 < rounds) load_x(j + 2, xb[0]);
-        round_fma(j + 1, xb[1]);
-      }
     }
   }
 
@@ -203,13 +237,13 @@ __device__ __forceinline__ void router_tile(const __nv_bfloat16* __restrict__ x,
 }
 
 // The router kernel: one (token block, expert block) tile per CTA.
-template <int TB, int EB, bool XALL>
-__global__ void __launch_bounds__(256) router_logits_kernel(const __nv_bfloat16* __restrict__ x,
+template <int TB, int EB, bool XALL, int WARPS>
+__global__ void __launch_bounds__(32 * WARPS) router_logits_kernel(const __nv_bfloat16* __restrict__ x,
                                                            const __nv_bfloat16* __restrict__ wg,
                                                            const float* __restrict__ bias,
                                                            float* __restrict__ logits, int T, int H, int E) {
   pdl_trigger();
-  router_tile<TB, EB, XALL>(x, wg, bias, logits, T, H, E);
+  router_tile<TB, EB, XALL, WARPS>(x, wg, bias, logits, T, H, E);
 }
 
 // (value, expert) order of the top-k: larger logit first, ties to the lower
@@ -800,13 +834,13 @@ __global__ void __launch_bounds__(256, 1) front_small_kernel(const __grid_consta
   if (threadIdx.x == 0 && !p.all_experts) p.sync[FRONT_SYNC_WORDS - 1] = 0;
 }
 
-template <int TB, int EB, bool XALL>
+template <int TB, int EB, bool XALL, int WARPS = ROUTER_WARPS>
 cudaError_t launch_router_t(const void* x, const void* gate_w, const float* bias, float* logits, int T, int H,
                             int E, cudaStream_t s) {
-  dim3 grid((T + ROUTER_WARPS * TB - 1) / (ROUTER_WARPS * TB), E / EB);
-  const size_t smem = (size_t)H * EB * 2;
+  dim3 grid((T + WARPS * TB - 1) / (WARPS * TB), E / EB);
+  const size_t smem = (size_t)H * EB * 2 + router_xring_bytes(TB, XALL, WARPS);
   // first kernel of a forward: ordinary stream order (it may depend on the caller's work)
-  return launch_k(router_logits_kernel<TB, EB, XALL>, grid, dim3(256), smem, s, false,
+  return launch_k(router_logits_kernel<TB, EB, XALL, WARPS>, grid, dim3(32 * WARPS), smem, s, false,
                   reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<const __nv_bfloat16*>(gate_w), bias,
                   logits, T, H, E);
 }
@@ -825,12 +859,15 @@ bool router_small(int T, int H) { return T <= 512 && H <= 2048; }
 // Raises (never lowers) the dynamic shared-memory cap of one router
 // instantiation to `bytes`.  The cap belongs to the kernel, not to a handle,
 // so a handle with a narrower hidden size must not shrink it under another.
-template <int TB, int EB, bool XALL>
-cudaError_t raise_router_attr(int bytes) {
+// `bytes` is the weight slice's size, to which the activation ring is added
+// (with_ring), or the whole cap.
+template <int TB, int EB, bool XALL, int WARPS = ROUTER_WARPS>
+cudaError_t raise_router_attr(int bytes, bool with_ring = true) {
+  if (with_ring) bytes += router_xring_bytes(TB, XALL, WARPS);
   cudaFuncAttributes a{};
-  cudaError_t e = cudaFuncGetAttributes(&a, router_logits_kernel<TB, EB, XALL>);
+  cudaError_t e = cudaFuncGetAttributes(&a, router_logits_kernel<TB, EB, XALL, WARPS>);
   if (e != cudaSuccess || a.maxDynamicSharedSizeBytes >= bytes) return e;
-  return cudaFuncSetAttribute(router_logits_kernel<TB, EB, XALL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(router_logits_kernel<TB, EB, XALL, WARPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               bytes);
 }
 
@@ -858,15 +895,15 @@ cudaError_t router_setup(int H, int E) {
 cudaError_t router_setup_max(int bytes) {
   std::lock_guard<std::mutex> lock(router_attr_mutex);
   cudaError_t e;
-  if ((e = raise_router_attr<4, 32, false>(bytes)) != cudaSuccess) return e;
-  if ((e = raise_router_attr<2, 32, true>(bytes)) != cudaSuccess) return e;
-  if ((e = raise_router_attr<4, 16, false>(bytes)) != cudaSuccess) return e;
-  if ((e = raise_router_attr<2, 16, true>(bytes)) != cudaSuccess) return e;
-  if ((e = raise_router_attr<4, 8, false>(bytes)) != cudaSuccess) return e;
-  return raise_router_attr<4, 8, true>(bytes);
+  if ((e = raise_router_attr<4, 32, false>(bytes, false)) != cudaSuccess) return e;
+  if ((e = raise_router_attr<2, 32, true>(bytes, false)) != cudaSuccess) return e;
+  if ((e = raise_router_attr<4, 16, false>(bytes, false)) != cudaSuccess) return e;
+  if ((e = raise_router_attr<2, 16, true>(bytes, false)) != cudaSuccess) return e;
+  if ((e = raise_router_attr<4, 8, false>(bytes, false)) != cudaSuccess) return e;
+  return raise_router_attr<4, 8, true>(bytes, false);
 }
 
-int router_smem_bytes(int H, int E) { return H * router_eb(H, E) * 2; }
+int router_smem_bytes(int H, int E) { return H * router_eb(H, E) * 2 + router_xring_bytes(4, false, ROUTER_WARPS); }
 
 namespace {
 
