@@ -43,7 +43,10 @@
  *   over the 32 partials); top-k by logit (ties to the lower expert id);
  *   weights = softmax over all experts, chosen ones renormalised.
  *   Requires hidden % 256 == 0, inter % 128 == 0, num_experts % 8 == 0,
- *   num_experts <= 256, 1 <= top_k <= min(num_experts, 16).
+ *   num_experts <= 256, 1 <= top_k <= min(num_experts, 16), and a router
+ *   tile within one CTA's shared memory (hidden x 8..32 experts of the
+ *   router weight in bf16 plus 48 KB of activation rings: hidden <= 11264 on
+ *   sm_103a).
  *
  * Memory and ownership: every pointer argument is a device pointer on the
  * handle's device unless stated otherwise.  Inputs are borrowed and read in
@@ -296,11 +299,11 @@ MOE_API const char* moe_stage_name(int i);
  * pointer; enqueued on `stream` (NULL = legacy default stream) with no host
  * synchronisation.  All buffers are the caller's.
  *
- * Limits and errors: hidden % 256 == 0, num_experts % 8 == 0,
- * num_experts <= 256, 1 <= top_k <= min(num_experts, 16), otherwise
- * MOE_ERR_UNSUPPORTED; num_tokens * num_experts above
- * MOE_ROUTE_NOALLOC_MAX_LOGITS returns MOE_ERR_TOO_MANY_TOKENS (split the
- * batch); NULL or misaligned pointers MOE_ERR_INVALID_ARG; a device other
+ * Limits and errors: hidden % 256 == 0, hidden <= 11264 (the router tile's
+ * shared memory), num_experts % 8 == 0, num_experts <= 256,
+ * 1 <= top_k <= min(num_experts, 16), otherwise MOE_ERR_UNSUPPORTED;
+ * num_tokens * num_experts above MOE_ROUTE_NOALLOC_MAX_LOGITS returns
+ * MOE_ERR_TOO_MANY_TOKENS (split the batch); NULL or misaligned pointers MOE_ERR_INVALID_ARG; a device other
  * than sm_103 MOE_ERR_UNSUPPORTED; num_tokens == 0 does nothing.
  *
  * The first call on each device does that device's set-up (loads the device

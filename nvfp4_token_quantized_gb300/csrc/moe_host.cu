@@ -531,6 +531,8 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
     cudaGetLastError();
     return MOE_ERR_UNSUPPORTED;
   }
+  // the router's weight slice and activation rings share one CTA's memory
+  if ((size_t)router_smem_bytes(H, E) > prop.sharedMemPerBlockOptin) return MOE_ERR_UNSUPPORTED;
   DeviceGuard dg(cfg->device);
   moe_handle* h = new moe_handle();
   h->cfg = *cfg;

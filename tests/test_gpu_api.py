@@ -120,3 +120,23 @@ def test_narrower_handle_leaves_wider_one_working():
     assert torch.equal(before.view(torch.int16), after.view(torch.int16))
     b.close()
     a.close()
+
+
+def test_hidden_beyond_the_router_tile_is_refused():
+    # the router keeps a [hidden x 8] slice of its weight and 48 KB of
+    # activation rings in one CTA's shared memory: hidden 11520 needs 228 KB
+    # in all, over the 227 KB a CTA may hold; the create and the no-handle
+    # routing refuse it before any allocation or launch
+    from nvfp4_token_quantized_gb300 import MoE
+    from nvfp4_token_quantized_gb300.binding import load_library
+
+    built()
+    UNSUPPORTED = 8
+    assert _status(lambda: MoE(hidden=11520, inter=256, num_experts=64, top_k=4, max_num_tokens=16)) == UNSUPPORTED
+    x = torch.zeros(2, 11520, dtype=torch.bfloat16, device="cuda")
+    g = torch.zeros(11520, 64, dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty(2, 4, dtype=torch.int32, device="cuda")
+    w = torch.empty(2, 4, dtype=torch.float32, device="cuda")
+    lib = load_library()
+    assert lib.moe_route_noalloc(x.data_ptr(), g.data_ptr(), None, 2, 11520, 64, 4, ids.data_ptr(), w.data_ptr(),
+                                 None) == UNSUPPORTED
