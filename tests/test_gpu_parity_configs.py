@@ -250,14 +250,16 @@ def test_stress_refresh_replay_equals_fresh():
     layer.close()
 
 
-@pytest.mark.parametrize("T,H,E,K", [(5000, 256, 16, 4), (80, 4352, 8, 2)])
+@pytest.mark.parametrize("T,H,E,K", [(5000, 256, 16, 4), (80, 4352, 8, 2), (600, 512, 32, 4)])
 def test_long_batch_and_wide_rows(T, H, E, K):
     """Paths the benchmark shapes do not reach: more than 4096 tokens (the
-    permutation counts its experts in a pass of its own before ranking) and
+    permutation counts its experts in a pass of its own before ranking),
     rows wider than 4096 elements (the activation quantizer forms codes after
-    its dependency wait instead of holding them in registers).  Routing, the
-    whole permutation and every token's quantization are bit-exact; every
-    token's output is checked as in the other workloads."""
+    its dependency wait instead of holding them in registers), and the
+    router's 32-expert blocks with streamed activations (more than 512
+    tokens, H <= 1536).  Routing, the whole permutation and every token's
+    quantization are bit-exact; every token's output is checked as in the
+    other workloads."""
     shape = synthetic.MoEShape(name="edge", T=T, H=H, E=E, K=K, I=128, max_num_tokens=T)
     wl = synthetic.make_workload(shape, T=T, seed=5)
     d = to_dev(wl)
